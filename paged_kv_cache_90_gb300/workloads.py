@@ -1,0 +1,332 @@
+"""Seeded synthetic inputs for the paged decode path.
+
+This module holds no attention arithmetic.  It draws tensors from seeded
+``torch.Generator`` streams on the CPU and lays out block tables, slot mappings and
+copy-on-write pairs through :mod:`block_manager`.  The GPU kernels and the CPU oracle
+are both fed these same tensors.
+
+Shapes follow the workloads the pages describe: a pool of fixed-size blocks with
+scattered (shuffled) physical ids, block size 16 by default, Llama-3-8B-like heads
+(32 query / 8 KV heads, head_dim 128; gufacode.com "PagedAttention:KV cache 的页表革命",
+section "GPU 上 KV cache 池子有多大"), mixed lengths, shared prefixes with parallel
+sampling (vasteelab.pages.dev "PagedAttentionとは？", section "負荷試験"), GQA head
+sharing and an 8-bit KV cache (ultralytics.com glossary "PagedAttention", section
+"관련 기법").
+
+Cache layout: ``[num_blocks, num_kv_heads, block_size, head_dim]``, innermost
+contiguous.  The ultralytics.com PyTorch example's pool ``[num_blocks, block_size,
+head_dim]`` is its one-head case.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import List, Optional, Sequence
+
+import torch
+
+from .block_manager import BlockAllocator, BlockManager, blocks_needed, validate_cow_pairs
+
+DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}
+DTYPE_NAMES = {v: k for k, v in DTYPES.items()}
+_E4M3_MAX = 448.0
+_CHUNK = 1 << 24
+
+
+@dataclass
+class DecodeStep:
+    """Inputs of one decode step: each sequence appends one token, then attends."""
+    query: torch.Tensor          # [S, Hq, D]
+    new_key: torch.Tensor        # [S, Hk, D] (source dtype: f32 or bf16)
+    new_value: torch.Tensor      # [S, Hk, D]
+    slot_mapping: torch.Tensor   # [S] int64, slot of each new token
+    block_tables: torch.Tensor   # [S, MB] int32, padded with -1
+    context_lens: torch.Tensor   # [S] int32, counts the new token
+    cow_pairs: torch.Tensor      # [n, 2] int64 (src, dst), copied before the append
+
+
+@dataclass
+class Workload:
+    name: str
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    max_blocks_per_seq: int
+    scale: float
+    k_scale: float
+    v_scale: float
+    key_cache: torch.Tensor      # initial pool contents [NB, Hk, bs, D]
+    value_cache: torch.Tensor
+    steps: List[DecodeStep] = field(default_factory=list)
+    seed: int = 0
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.steps[0].query.shape[0])
+
+    @property
+    def kv_dtype(self) -> torch.dtype:
+        return self.key_cache.dtype
+
+    @property
+    def q_dtype(self) -> torch.dtype:
+        return self.steps[0].query.dtype
+
+
+def _randn(shape, dtype: torch.dtype, g: torch.Generator) -> torch.Tensor:
+    """N(0, 1) draws rounded to ``dtype``, generated in chunks to bound memory."""
+    n = math.prod(shape)
+    out = torch.empty(n, dtype=dtype)
+    for i in range(0, n, _CHUNK):
+        m = min(_CHUNK, n - i)
+        out[i:i + m] = torch.randn(m, generator=g, dtype=torch.float32)
+    return out.view(*shape)
+
+
+def _quantize_e4m3(x: torch.Tensor, scale: float) -> torch.Tensor:
+    """Pool contents for an 8-bit cache: ``x / scale`` cast by torch's own
+    float8_e4m3fn conversion (input generation only)."""
+    out = torch.empty(x.shape, dtype=torch.float8_e4m3fn)
+    xf, of = x.reshape(-1), out.view(-1)
+    for i in range(0, xf.numel(), _CHUNK):
+        of[i:i + _CHUNK] = (xf[i:i + _CHUNK].float() / scale).to(torch.float8_e4m3fn)
+    return out
+
+
+def _amax(x: torch.Tensor) -> float:
+    xf = x.reshape(-1)
+    m = 0.0
+    for i in range(0, xf.numel(), _CHUNK):
+        m = max(m, float(xf[i:i + _CHUNK].float().abs().max()))
+    return m
+
+
+def _make_pool(nb, hk, bs, d, kv_dtype: str, g: torch.Generator):
+    """Random K and V pools (every slot holds N(0,1)-shaped data, used or not)."""
+    src = torch.bfloat16 if kv_dtype == "e4m3" else DTYPES[kv_dtype]
+    k = _randn((nb, hk, bs, d), src, g)
+    v = _randn((nb, hk, bs, d), src, g)
+    if kv_dtype != "e4m3":
+        return k, v, 1.0, 1.0
+    k_scale = float(torch.tensor(_amax(k) / _E4M3_MAX, dtype=torch.float32))
+    v_scale = float(torch.tensor(_amax(v) / _E4M3_MAX, dtype=torch.float32))
+    return _quantize_e4m3(k, k_scale), _quantize_e4m3(v, v_scale), k_scale, v_scale
+
+
+def _step(mgr: BlockManager, seq_ids: Sequence, g: torch.Generator, hq: int, hk: int,
+          d: int, q_dtype: torch.dtype, src_dtype: torch.dtype, mb: int) -> DecodeStep:
+    """Every sequence in ``seq_ids`` appends one token (copy-on-write first if its
+    target block is shared); then the step's query and new K/V are drawn."""
+    slots, pairs = [], []
+    for sid in seq_ids:
+        slot, pair = mgr.append_token(sid)
+        slots.append(slot)
+        if pair is not None:
+            pairs.append(pair)
+    validate_cow_pairs(pairs, mgr.alloc.num_blocks)
+    s = len(seq_ids)
+    query = _randn((s, hq, d), q_dtype, g)
+    new_key = _randn((s, hk, d), src_dtype, g)
+    new_value = _randn((s, hk, d), src_dtype, g)
+    return DecodeStep(
+        query=query, new_key=new_key, new_value=new_value,
+        slot_mapping=torch.tensor(slots, dtype=torch.int64),
+        block_tables=torch.tensor(mgr.block_table_rows(seq_ids, mb), dtype=torch.int32).view(s, mb),
+        context_lens=torch.tensor([mgr.seqs[i].length for i in seq_ids], dtype=torch.int32),
+        cow_pairs=torch.tensor(pairs, dtype=torch.int64).view(-1, 2),
+    )
+
+
+def _occupied_slots(mgr: BlockManager) -> torch.Tensor:
+    """Flat slot indices that hold a cached token right now."""
+    occ = set()
+    for s in mgr.seqs.values():
+        for pos in range(s.length):
+            occ.add(s.slot(pos, mgr.bs))
+    return torch.tensor(sorted(occ), dtype=torch.int64)
+
+
+def _poison(cache: torch.Tensor, occupied: torch.Tensor) -> None:
+    """Overwrite every slot that holds no token with NaN, so that a kernel which
+    reads an unused tail slot or an unreferenced block is caught."""
+    nb, hk, bs, d = cache.shape
+    keep = torch.zeros(nb * bs, dtype=torch.bool)
+    keep[occupied] = True
+    keep = keep.view(nb, 1, bs, 1).expand(nb, hk, bs, d)
+    if cache.dtype == torch.float8_e4m3fn:
+        raw = cache.view(torch.uint8)
+        raw[~keep] = 0x7F
+    else:
+        cache[~keep] = float("nan")
+
+
+def _finish(name, seed, hq, hk, d, bs, nb, mb, kc, vc, ks, vs, steps, scale=None) -> Workload:
+    return Workload(name=name, num_heads=hq, num_kv_heads=hk, head_dim=d, block_size=bs,
+                    num_blocks=nb, max_blocks_per_seq=mb,
+                    scale=float(scale if scale is not None else 1.0 / math.sqrt(d)),
+                    k_scale=ks, v_scale=vs, key_cache=kc, value_cache=vc, steps=steps, seed=seed)
+
+
+def variable_length_decode(name: str, seed: int, lengths: Sequence[int], num_heads: int,
+                           num_kv_heads: int, head_dim: int, block_size: int, kv_dtype: str,
+                           q_dtype: str = "bf16", num_steps: int = 1, pool_slack: float = 0.10,
+                           num_blocks: Optional[int] = None, poison: bool = False,
+                           scale: Optional[float] = None) -> Workload:
+    """Sequences with the given context lengths *after* the first append.
+
+    The pool holds the needed blocks (for all ``num_steps`` appends) plus
+    ``pool_slack`` spare ones, handed out in a seeded random order so every table is a
+    scattered set of physical ids.  Each step appends one token per sequence.
+    """
+    g = torch.Generator().manual_seed(seed)
+    lengths = [int(x) for x in lengths]
+    if min(lengths) < 1:
+        raise ValueError("every context length must count the appended token")
+    need = sum(blocks_needed(L + num_steps - 1, block_size) for L in lengths)
+    nb = num_blocks if num_blocks is not None else int(math.ceil(need * (1.0 + pool_slack)))
+    mb = max(blocks_needed(L + num_steps - 1, block_size) for L in lengths)
+    perm = torch.randperm(nb, generator=g).tolist()
+    mgr = BlockManager(BlockAllocator(nb, block_size, perm))
+    seq_ids = list(range(len(lengths)))
+    for sid, L in zip(seq_ids, lengths):
+        mgr.add_sequence(sid, L - 1)
+    kc, vc, ks, vs = _make_pool(nb, num_kv_heads, block_size, head_dim, kv_dtype, g)
+    if poison:
+        occ = _occupied_slots(mgr)
+        _poison(kc, occ)
+        _poison(vc, occ)
+    src = torch.bfloat16 if kv_dtype == "e4m3" else DTYPES[kv_dtype]
+    steps = [_step(mgr, seq_ids, g, num_heads, num_kv_heads, head_dim, DTYPES[q_dtype], src, mb)
+             for _ in range(num_steps)]
+    mgr.check_structure()
+    return _finish(name, seed, num_heads, num_kv_heads, head_dim, block_size, nb, mb,
+                   kc, vc, ks, vs, steps, scale)
+
+
+# --- the five workloads -----------------------------------------------------------
+
+def tiny(seed: int = 1, poison: bool = True) -> Workload:
+    """3 sequences of 5, 17 and 40 tokens, 4 query = 4 KV heads, head_dim 64,
+    block size 16, a pool of 64 blocks, fp32 data, scale 1/8."""
+    return variable_length_decode("tiny_f32", seed, [5, 17, 40], 4, 4, 64, 16, "f32",
+                                  q_dtype="f32", num_blocks=64, poison=poison)
+
+
+def scalar_example(physical: Sequence[int] = (4, 1), num_blocks: int = 8,
+                   head_dim: int = 1, dtype: str = "f32") -> Workload:
+    """The pages' scalar case: one head, keys 0, query 1, values 1..5, four tokens
+    per block, logical blocks 0 and 1 at the given physical blocks
+    (paweldubiel.com "PagedAttention", sections "Mecanismo y detalles" and
+    "El orden del texto no es la dirección de memoria").  ``head_dim`` > 1 pads the
+    head with zeros: q.k is unchanged and every extra output column is 0."""
+    bs, L = 4, 5
+    dt = DTYPES[dtype]
+    kc = torch.zeros(num_blocks, 1, bs, head_dim, dtype=dt)
+    vc = torch.zeros(num_blocks, 1, bs, head_dim, dtype=dt)
+    for pos in range(L):
+        vc[physical[pos // bs], 0, pos % bs, 0] = float(pos + 1)
+    q = torch.zeros(1, 1, head_dim, dtype=dt)
+    q[0, 0, 0] = 1.0
+    mb = len(physical)
+    step = DecodeStep(
+        query=q, new_key=torch.zeros(0, 1, head_dim, dtype=dt),
+        new_value=torch.zeros(0, 1, head_dim, dtype=dt),
+        slot_mapping=torch.zeros(0, dtype=torch.int64),
+        block_tables=torch.tensor([list(physical)], dtype=torch.int32),
+        context_lens=torch.tensor([L], dtype=torch.int32),
+        cow_pairs=torch.zeros(0, 2, dtype=torch.int64))
+    return Workload(name="scalar_example", num_heads=1, num_kv_heads=1, head_dim=head_dim,
+                    block_size=bs, num_blocks=num_blocks, max_blocks_per_seq=mb, scale=1.0,
+                    k_scale=1.0, v_scale=1.0, key_cache=kc, value_cache=vc, steps=[step])
+
+
+def llama3_8b_decode(seed: int = 2, num_seqs: int = 64, len_range=(128, 2048),
+                     block_size: int = 16, kv_dtype: str = "bf16", poison: bool = False) -> Workload:
+    """Llama-3-8B-shaped decode layer: ``num_seqs`` sequences whose cached lengths are
+    uniform in ``len_range``; one new token each; 32/8 heads, head_dim 128."""
+    g = torch.Generator().manual_seed(seed)
+    old = torch.randint(len_range[0], len_range[1] + 1, (num_seqs,), generator=g).tolist()
+    return variable_length_decode(f"llama3_8b_decode_s{num_seqs}_bs{block_size}_{kv_dtype}",
+                                  seed, [L + 1 for L in old], 32, 8, 128, block_size, kv_dtype,
+                                  poison=poison)
+
+
+def long_context(seed: int = 3, block_size: int = 16, num_seqs: int = 8,
+                 context_len: int = 32768, poison: bool = False) -> Workload:
+    """Long-context decode: every sequence holds ``context_len`` tokens after its
+    append; 32/8 heads, head_dim 128, bf16."""
+    return variable_length_decode(f"long_context_s{num_seqs}_L{context_len}_bs{block_size}",
+                                  seed, [context_len] * num_seqs, 32, 8, 128, block_size, "bf16",
+                                  poison=poison)
+
+
+def continuous_batching(seed: int = 5, block_size: int = 16, kv_dtype: str = "bf16",
+                        num_seqs: int = 256, num_steps: int = 10, median: float = 512.0,
+                        sigma: float = 1.0, cap: int = 8192, poison: bool = False) -> Workload:
+    """Continuous-batching mix: lengths round(lognormal(ln median, sigma)) clamped to
+    [1, cap], ``num_steps`` decode steps each appending one token per sequence (a new
+    block is taken whenever a sequence's last block is full)."""
+    g = torch.Generator().manual_seed(seed)
+    z = torch.randn(num_seqs, generator=g, dtype=torch.float64)
+    lens = torch.exp(math.log(median) + sigma * z).round().clamp(1, cap).long().tolist()
+    return variable_length_decode(f"continuous_batching_s{num_seqs}_bs{block_size}_{kv_dtype}",
+                                  seed, lens, 32, 8, 128, block_size, kv_dtype,
+                                  num_steps=num_steps, poison=poison)
+
+
+def shared_prefix_cow(seed: int = 4, num_groups: int = 32, group_size: int = 4,
+                      prefix_blocks: int = 64, suffix_range=(16, 512), block_size: int = 16,
+                      pool_slack: float = 0.10, poison: bool = False) -> Workload:
+    """Shared prefix + parallel sampling with copy-on-write.
+
+    Every sequence's table starts with the same ``prefix_blocks`` physical blocks.
+    Each group of ``group_size`` samples shares a suffix of ``u`` tokens, u uniform in
+    ``suffix_range`` and not a multiple of the block size, so the group's last block is
+    partly filled and shared.  The step appends one token to every sample: the first
+    ``group_size - 1`` writers of a group get a private copy of that block (the copy
+    pairs of the step), the last one writes in place.
+    """
+    g = torch.Generator().manual_seed(seed)
+    us = []
+    while len(us) < num_groups:
+        u = int(torch.randint(suffix_range[0], suffix_range[1] + 1, (1,), generator=g))
+        if u % block_size:
+            us.append(u)
+    need = prefix_blocks + sum(blocks_needed(u, block_size) + group_size - 1 for u in us)
+    nb = int(math.ceil(need * (1.0 + pool_slack)))
+    perm = torch.randperm(nb, generator=g).tolist()
+    mgr = BlockManager(BlockAllocator(nb, block_size, perm))
+    mgr.add_sequence("prefix", prefix_blocks * block_size)
+    seq_ids = []
+    for gi, u in enumerate(us):
+        head = (gi, 0)
+        mgr.fork("prefix", head)
+        for _ in range(u):
+            _, pair = mgr.append_token(head)
+            assert pair is None
+        seq_ids.append(head)
+        for j in range(1, group_size):
+            mgr.fork(head, (gi, j))
+            seq_ids.append((gi, j))
+    mgr.free_sequence("prefix")
+    mb = prefix_blocks + max(blocks_needed(u + 1, block_size) for u in us)
+    kc, vc, ks, vs = _make_pool(nb, 8, block_size, 128, "bf16", g)
+    if poison:
+        occ = _occupied_slots(mgr)
+        _poison(kc, occ)
+        _poison(vc, occ)
+    step = _step(mgr, seq_ids, g, 32, 8, 128, torch.bfloat16, torch.bfloat16, mb)
+    mgr.check_structure()
+    return _finish(f"shared_prefix_cow_g{num_groups}x{group_size}", seed, 32, 8, 128, block_size,
+                   nb, mb, kc, vc, ks, vs, [step])
+
+
+WORKLOADS = {
+    "tiny": tiny,
+    "llama3_8b_decode": llama3_8b_decode,
+    "long_context": long_context,
+    "shared_prefix_cow": shared_prefix_cow,
+    "continuous_batching": continuous_batching,
+}

@@ -1,0 +1,392 @@
+"""Pins for the CPU oracle: values the pages print, closed forms, invariants, and
+library routines that the oracle's arithmetic reduces to.  None of these needs a GPU
+and none of them reads the oracle's own code back as its expectation."""
+import itertools
+import json
+import math
+from pathlib import Path
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_90_gb300 import workloads as wl
+from paged_kv_cache_90_gb300.block_manager import BlockAllocator, BlockManager
+
+GOLDEN = Path(__file__).parent / "golden"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build_oracle():
+    oracle.build()
+
+
+def _materialize(w, step=0):
+    """Caches after the step's copy-on-write pairs and new-token writes (the state
+    the decode of that step reads)."""
+    st = w.steps[step]
+    kc, vc = w.key_cache.clone(), w.value_cache.clone()
+    if st.cow_pairs.numel():
+        oracle.copy_blocks(kc, st.cow_pairs)
+        oracle.copy_blocks(vc, st.cow_pairs)
+    if st.slot_mapping.numel():
+        oracle.reshape_and_cache(st.new_key, st.new_value, kc, vc, st.slot_mapping,
+                                 w.k_scale, w.v_scale)
+    return kc, vc
+
+
+def _decode(w, step=0, kc=None, vc=None):
+    st = w.steps[step]
+    if kc is None:
+        kc, vc = _materialize(w, step)
+    return oracle.paged_attention_decode(st.query, kc, vc, st.block_tables, st.context_lens,
+                                         w.scale, w.k_scale, w.v_scale)
+
+
+# --- the scalar worked example ----------------------------------------------------
+
+def test_scalar_example_printed_layouts():
+    g = json.loads((GOLDEN / "scalar_example.json").read_text())
+    for layout in g["layouts"]:
+        w = wl.scalar_example(physical=layout, num_blocks=8)
+        out = _decode(w)
+        assert out.shape == (1, 1, 1)
+        assert abs(float(out[0, 0, 0]) - g["expected_output"]) <= 4 * np.finfo(np.float64).eps * 3
+
+
+@pytest.mark.parametrize("head_dim", [1, 64])
+def test_scalar_example_every_layout(head_dim):
+    """Output 3 for every placement of the two logical blocks in a pool of 6; a head
+    padded with zeros to 64 dims leaves column 0 at 3 and the rest at 0."""
+    for a, b in itertools.permutations(range(6), 2):
+        w = wl.scalar_example(physical=(a, b), num_blocks=6, head_dim=head_dim)
+        out = _decode(w)[0, 0]
+        assert abs(float(out[0]) - 3.0) <= 1e-15
+        assert torch.all(out[1:] == 0)
+
+
+# --- closed forms -----------------------------------------------------------------
+
+def _small(seed, lengths, hq=4, hk=2, d=16, bs=4, kv="bf16", q="bf16", poison=False):
+    return wl.variable_length_decode("t", seed, lengths, hq, hk, d, bs, kv, q_dtype=q,
+                                     poison=poison)
+
+
+def _gather(cache, table, k, L, bs):
+    """Contiguous [L, D] rows of KV head k for one sequence, by torch indexing."""
+    n = -(-L // bs)
+    blocks = cache[table[:n].long()]            # [n, Hk, bs, D]
+    return blocks[:, k].reshape(n * bs, -1)[:L]
+
+
+def test_single_token_returns_its_value():
+    """L = 1: the one weight is exactly 1, so the output is V[0] exactly."""
+    w = _small(11, [1, 1, 1], kv="bf16")
+    kc, vc = _materialize(w)
+    out = _decode(w, kc=kc, vc=vc)
+    st = w.steps[0]
+    for s in range(3):
+        for h in range(w.num_heads):
+            k = h // (w.num_heads // w.num_kv_heads)
+            v0 = _gather(vc, st.block_tables[s], k, 1, w.block_size)[0].double()
+            assert torch.equal(out[s, h], v0)
+
+
+def test_equal_keys_give_mean_of_values():
+    """All keys equal -> all weights 1/L -> output = mean of the values (the scalar
+    example's argument, for any L and any head_dim)."""
+    w = _small(12, [7, 33, 50], d=32, kv="f32", q="f32")
+    kc, vc = _materialize(w)
+    kc[:] = 0.25
+    out = _decode(w, kc=kc, vc=vc)
+    st = w.steps[0]
+    for s in range(3):
+        L = int(st.context_lens[s])
+        for h in range(w.num_heads):
+            k = h // (w.num_heads // w.num_kv_heads)
+            mean = _gather(vc, st.block_tables[s], k, L, w.block_size).double().mean(0)
+            assert torch.allclose(out[s, h], mean, rtol=0, atol=1e-14)
+
+
+def test_peaked_scores_select_one_value():
+    """One key aligned with the query by a margin Delta over the others: the output is
+    within 2 * max|V| * (L-1) e^-Delta of that key's value."""
+    d, L, bs = 16, 24, 8
+    w = _small(13, [L], hq=1, hk=1, d=d, bs=bs, kv="f32", q="f32")
+    st = w.steps[0]
+    st.query.zero_()
+    st.query[0, 0, 0] = 1.0
+    jstar, delta = 17, 40.0
+    table = st.block_tables[0]
+    kc, vc = _materialize(w)
+    for j in range(L):
+        blk, off = int(table[j // bs]), j % bs
+        kc[blk, 0, off].zero_()
+        kc[blk, 0, off, 0] = delta if j == jstar else 0.0
+    w.scale = 1.0
+    out = _decode(w, kc=kc, vc=vc)[0, 0]
+    v = _gather(vc, table, 0, L, bs).double()
+    bound = 2 * v.abs().max() * (L - 1) * math.exp(-delta)
+    assert torch.max(torch.abs(out - v[jstar])) <= bound + 1e-15
+
+
+# --- equality with dense attention (a library routine) ------------------------------
+
+@pytest.mark.parametrize("kv,q,hq,hk,d,bs", [
+    ("f32", "f32", 4, 4, 64, 16),
+    ("bf16", "bf16", 8, 2, 128, 16),
+    ("bf16", "bf16", 4, 1, 64, 8),
+    ("bf16", "f32", 6, 2, 64, 32),
+    ("e4m3", "bf16", 8, 2, 128, 16),
+    ("f32", "f32", 3, 3, 16, 4),
+])
+def test_equals_dense_sdpa(kv, q, hq, hk, d, bs):
+    """Paged attention equals contiguous attention over the gathered context:
+    torch's scaled_dot_product_attention in float64, K/V heads repeated for the query
+    groups, against the oracle."""
+    lens = [1, 5, bs, bs + 1, 3 * bs - 1, 70]
+    w = _small(20 + d + bs, lens, hq=hq, hk=hk, d=d, bs=bs, kv=kv, q=q, poison=True)
+    kc, vc = _materialize(w)
+    out = _decode(w, kc=kc, vc=vc)
+    st = w.steps[0]
+    g = hq // hk
+    for s, L in enumerate(st.context_lens.tolist()):
+        ks = torch.stack([_gather(kc, st.block_tables[s], k, L, bs) for k in range(hk)])
+        vs = torch.stack([_gather(vc, st.block_tables[s], k, L, bs) for k in range(hk)])
+        ks = ks.double() * w.k_scale
+        vs = vs.double() * w.v_scale
+        ks = ks.repeat_interleave(g, dim=0)[None]      # [1, Hq, L, D]
+        vs = vs.repeat_interleave(g, dim=0)[None]
+        qs = st.query[s].double()[None, :, None, :]    # [1, Hq, 1, D]
+        ref = torch.nn.functional.scaled_dot_product_attention(qs, ks, vs, scale=w.scale)
+        assert torch.allclose(out[s], ref[0, :, 0], rtol=0, atol=1e-12), (s, L)
+
+
+# --- invariants ---------------------------------------------------------------------
+
+def test_physical_permutation_invariance():
+    """Moving blocks to other physical ids (and renumbering the tables) leaves the
+    output bit-identical."""
+    w = _small(31, [9, 40, 65, 3], kv="bf16", poison=True)
+    k0, v0 = _materialize(w)
+    base = _decode(w, kc=k0, vc=v0)
+    g = torch.Generator().manual_seed(99)
+    perm = torch.randperm(w.num_blocks, generator=g)
+    kc = torch.empty_like(k0)
+    vc = torch.empty_like(v0)
+    kc[perm] = k0
+    vc[perm] = v0
+    st = w.steps[0]
+    bt = st.block_tables.clone()
+    used = bt >= 0
+    bt[used] = perm[bt[used].long()].to(torch.int32)
+    moved = oracle.paged_attention_decode(st.query, kc, vc, bt, st.context_lens, w.scale)
+    assert torch.equal(base, moved)
+
+
+def test_shared_prefix_equals_private_copies():
+    """Tables that share physical blocks give the same output as tables whose blocks
+    were first copied into private blocks."""
+    w = wl.shared_prefix_cow(seed=4, num_groups=3, group_size=4, prefix_blocks=4,
+                             suffix_range=(5, 40), poison=True)
+    kc, vc = w.key_cache.clone(), w.value_cache.clone()
+    shared = oracle.run_workload_step(w, 0, kc, vc)
+    st = w.steps[0]
+    s = st.block_tables.shape[0]
+    nblk = [-(-int(L) // w.block_size) for L in st.context_lens]
+    total = sum(nblk)
+    kp = torch.full((total,) + tuple(kc.shape[1:]), float("nan"), dtype=kc.dtype)
+    vp = torch.full_like(kp, float("nan"))
+    bt = torch.full((s, st.block_tables.shape[1]), -1, dtype=torch.int32)
+    nxt = 0
+    for i in range(s):
+        for j in range(nblk[i]):
+            src = int(st.block_tables[i, j])
+            kp[nxt], vp[nxt] = kc[src], vc[src]
+            bt[i, j] = nxt
+            nxt += 1
+    private = oracle.paged_attention_decode(st.query, kp, vp, bt, st.context_lens, w.scale)
+    assert torch.equal(shared, private)
+    # sharing is real: the prefix blocks appear in every table
+    first = set(st.block_tables[:, 0].tolist())
+    assert len(first) == 1
+
+
+def test_unused_slots_are_never_read():
+    """NaN in unused tail slots, in unreferenced blocks and -1 table padding leave the
+    output equal to the unpoisoned run."""
+    clean = _small(41, [3, 17, 31, 64], kv="bf16", poison=False)
+    dirty = _small(41, [3, 17, 31, 64], kv="bf16", poison=True)
+    a, b = _decode(clean), _decode(dirty)
+    assert torch.isfinite(b).all()
+    assert torch.equal(a, b)
+    assert torch.isnan(dirty.key_cache.float()).any()
+
+
+def test_zero_length_gives_zeros():
+    w = _small(42, [4, 9], kv="f32", q="f32")
+    st = w.steps[0]
+    st.context_lens[0] = 0
+    out = _decode(w)
+    assert torch.all(out[0] == 0)
+
+
+def test_invalid_table_entry_is_reported():
+    w = _small(43, [9], kv="f32", q="f32")
+    w.steps[0].block_tables[0, 1] = w.num_blocks + 5
+    with pytest.raises(ValueError):
+        _decode(w)
+
+
+# --- cache write and copy-on-write -------------------------------------------------
+
+def test_cache_write_block_table_example():
+    """12 tokens at 4 per block through table [7, 2, 11]: tokens 0-3 land in physical
+    block 7, 4-7 in block 2, 8-11 in block 11, in position order."""
+    g = json.loads((GOLDEN / "block_maps.json").read_text())["table_example"]
+    bs, n, table = g["block_size"], g["num_tokens"], g["block_table"]
+    order = table + [b for b in range(16) if b not in table]
+    mgr = BlockManager(BlockAllocator(16, bs, order))
+    slots = mgr.add_sequence("r", n)
+    assert mgr.seqs["r"].blocks == table
+    keys = torch.arange(n * 2 * 8, dtype=torch.float32).view(n, 2, 8)
+    kc = torch.full((16, 2, bs, 8), -1.0)
+    vc = torch.full((16, 2, bs, 8), -1.0)
+    oracle.reshape_and_cache(keys, -keys, kc, vc, torch.tensor(slots))
+    for lb, (lo, hi) in enumerate(g["token_ranges"]):
+        phys = table[lb]
+        for t in range(lo, hi + 1):
+            assert torch.equal(kc[phys, :, t % bs], keys[t])
+            assert torch.equal(vc[phys, :, t % bs], -keys[t])
+    untouched = [b for b in range(16) if b not in table]
+    assert torch.all(kc[untouched] == -1.0)
+
+
+def test_cache_write_pytorch_example_round_trip():
+    """40 keys at block size 16 from the free list [41, 7, 19, 2, 33]: table
+    [41, 7, 19]; reading the pool back through the table returns the keys intact;
+    8 unused slots against 2008 for a 2,048-token reservation."""
+    g = json.loads((GOLDEN / "block_maps.json").read_text())["pytorch_example"]
+    bs, d, nb, n = g["block_size"], g["head_dim"], g["pool_blocks"], g["num_tokens"]
+    free = g["free_blocks"] + [b for b in range(nb) if b not in g["free_blocks"]]
+    mgr = BlockManager(BlockAllocator(nb, bs, free))
+    slots = mgr.add_sequence("req", n)
+    table = mgr.seqs["req"].blocks
+    assert len(table) == g["blocks_needed"]
+    assert table == g["block_table"]
+    keys = torch.randn(n, 1, d, generator=torch.Generator().manual_seed(0))
+    pool = torch.zeros(nb, 1, bs, d)
+    oracle.reshape_and_cache(keys, keys, pool, pool.clone(), torch.tensor(slots))
+    gathered = pool[table][:, 0].reshape(-1, d)[:n]
+    assert torch.equal(gathered, keys[:, 0]) == g["keys_intact"]
+    assert mgr.unused_slots("req") == g["unused_slots_paged"]
+    assert g["reservation"] - n == g["unused_slots_reserved"]
+
+
+def test_cache_write_skips_negative_slots():
+    keys = torch.ones(3, 1, 4)
+    kc = torch.zeros(4, 1, 2, 4)
+    vc = torch.zeros(4, 1, 2, 4)
+    oracle.reshape_and_cache(keys, keys, kc, vc, torch.tensor([-1, 5, -7]))
+    assert torch.equal(kc.view(8, 4)[5], torch.ones(4))
+    assert float(kc.sum()) == 4.0
+
+
+def test_copy_blocks_is_whole_block_byte_copy():
+    cache = torch.randn(6, 2, 4, 8, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
+    ref = cache.clone()
+    oracle.copy_blocks(cache, [(1, 4), (3, 0)])
+    assert torch.equal(cache[4].view(torch.int16), ref[1].view(torch.int16))
+    assert torch.equal(cache[0].view(torch.int16), ref[3].view(torch.int16))
+    for b in (1, 2, 3, 5):
+        assert torch.equal(cache[b].view(torch.int16), ref[b].view(torch.int16))
+
+
+def test_copy_on_write_step_matches_private_write():
+    """After the copy pairs and the write, each sample sees the shared prefix plus
+    its own new token; the shared block's other holders keep the old contents."""
+    w = wl.shared_prefix_cow(seed=5, num_groups=2, group_size=4, prefix_blocks=2,
+                             suffix_range=(3, 30))
+    st = w.steps[0]
+    assert st.cow_pairs.shape == (2 * 3, 2)
+    kc, vc = w.key_cache.clone(), w.value_cache.clone()
+    oracle.run_workload_step(w, 0, kc, vc)
+    for i in range(st.block_tables.shape[0]):
+        L = int(st.context_lens[i])
+        slot = int(st.slot_mapping[i])
+        blk, off = slot // w.block_size, slot % w.block_size
+        assert int(st.block_tables[i, (L - 1) // w.block_size]) == blk
+        assert torch.equal(kc[blk, :, off].view(torch.int16), st.new_key[i].view(torch.int16))
+        # the rest of that block equals the source block it was copied from
+        for s_, d_ in st.cow_pairs.tolist():
+            if d_ == blk:
+                assert torch.equal(kc[blk, :, :off].view(torch.int16),
+                                   w.key_cache[s_, :, :off].view(torch.int16))
+
+
+# --- number formats --------------------------------------------------------------
+
+def test_e4m3_decode_all_codes_vs_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    mine = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok])
+    assert np.isnan(mine[[0x7F, 0xFF]]).all()
+    assert mine[0x7E] == 448.0 and mine[0x01] == 2.0 ** -9
+
+
+def test_e4m3_encode_vs_torch_in_range():
+    """Round-to-nearest-even against torch's float8_e4m3fn cast, for random values
+    over the whole range and for every midpoint between neighbouring codes (and one
+    binary32 ulp either side of it)."""
+    g = torch.Generator().manual_seed(7)
+    rnd = (torch.rand(200000, generator=g) * 2 - 1) * torch.exp2(torch.rand(200000, generator=g) * 22 - 13)
+    rnd = rnd.clamp(-448, 448)
+    mags = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    mids = (mags[:-1] + mags[1:]) / 2
+    mids32 = torch.tensor(mids, dtype=torch.float32)
+    up = torch.nextafter(mids32, torch.tensor(1e9))
+    dn = torch.nextafter(mids32, torch.tensor(-1e9))
+    x = torch.cat([rnd, mids32, up, dn, -mids32, -up, -dn, torch.tensor([0.0, -0.0, 448.0, -448.0])])
+    x = x.clamp(-448, 448)
+    mine = oracle.e4m3_encode(x.numpy())
+    ref = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(mine, ref)
+
+
+def test_e4m3_encode_saturates_and_round_trips():
+    big = np.array([448.0001, 464.0, 1e6, 3e38, np.inf], dtype=np.float32)
+    assert np.all(oracle.e4m3_encode(big) == 0x7E)
+    assert np.all(oracle.e4m3_encode(-big) == 0xFE)
+    assert oracle.e4m3_encode(np.array([np.nan], dtype=np.float32))[0] == 0x7F
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    vals = oracle.e4m3_decode(codes).astype(np.float32)
+    assert np.array_equal(oracle.e4m3_encode(vals), codes)
+
+
+def test_bf16_decode_all_patterns_vs_torch():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    mine = oracle.bf16_decode(bits)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok])
+
+
+def test_fp8_cache_write_matches_torch_cast():
+    """The 8-bit cache write (binary32 division by the per-tensor scale, then e4m3)
+    agrees with torch's cast of the same quotient for in-range data."""
+    w = _small(51, [5, 9], kv="e4m3", d=64, bs=8)
+    st = w.steps[0]
+    kc, vc = w.key_cache.clone(), w.value_cache.clone()
+    oracle.reshape_and_cache(st.new_key, st.new_value, kc, vc, st.slot_mapping,
+                             w.k_scale, w.v_scale)
+    for t, slot in enumerate(st.slot_mapping.tolist()):
+        blk, off = slot // w.block_size, slot % w.block_size
+        qk = (st.new_key[t].float() / w.k_scale).clamp(-448, 448).to(torch.float8_e4m3fn)
+        qv = (st.new_value[t].float() / w.v_scale).clamp(-448, 448).to(torch.float8_e4m3fn)
+        assert torch.equal(kc[blk, :, off].view(torch.uint8), qk.view(torch.uint8))
+        assert torch.equal(vc[blk, :, off].view(torch.uint8), qv.view(torch.uint8))
