@@ -1,0 +1,222 @@
+/*
+ * pkv.h — C ABI of the GB300 paged KV-cache decode library (libpkv.so).
+ *
+ * Three operations make up the decode hot path of PagedAttention:
+ *
+ *   pkv_reshape_and_cache        write each new token's K and V into the cache slot
+ *                                named by its slot mapping;
+ *   pkv_copy_blocks              copy whole physical blocks (copy-on-write of blocks
+ *                                shared between sequences);
+ *   pkv_paged_attention_decode   single-query attention of every sequence over its
+ *                                cached tokens, read through its block table.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Tensors.  Every array is described by a pkv_tensor: a DEVICE pointer, a dtype, up to
+ *   4 dimensions and their strides in ELEMENTS.  The library never takes ownership of
+ *   a caller's buffer, never frees one, and keeps no pointer past the call (work is
+ *   queued on the caller's stream, so buffers must stay alive until that work ends).
+ *   The descriptors themselves are read during the call only.
+ * KV cache layout.  key_cache / value_cache are [num_blocks, num_kv_heads, block_size,
+ *   head_dim] with the last two dimensions contiguous (stride[3] == 1,
+ *   stride[2] == head_dim), so the bs x head_dim tile of one (block, KV head) is one
+ *   contiguous run of bytes.  stride[0] and stride[1] are free (K and V may be views
+ *   of one larger tensor) but, like the base pointer, must be multiples of 16 bytes.
+ * Dtypes.  Caches: PKV_F32, PKV_BF16 or PKV_FP8_E4M3 (OCP E4M3FN: bias 7, max 448,
+ *   no infinity).  An e4m3 cache carries its per-tensor dequantisation scale in the
+ *   descriptor's `scale` (stored code * scale = value); other dtypes ignore `scale`.
+ *   Queries and outputs: PKV_F32 or PKV_BF16, the output in the query's dtype.
+ *   Supported head_dim: 64 and 128.  Supported block_size: 2, 4, 8, 16, 32.
+ * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream) of the
+ *   current device.  Every call is asynchronous and stream-ordered; nothing
+ *   synchronises unless the debug-sync option is on.
+ * Errors.  No call throws or aborts.  Argument problems found on the host return
+ *   PKV_ERR_INVALID_ARG or PKV_ERR_UNSUPPORTED before anything is queued; CUDA
+ *   launch/runtime failures return PKV_ERR_CUDA.  pkv_last_error() gives the calling
+ *   thread's message for its last non-OK status.  Data-dependent checks run on the
+ *   device in every call: a block-table entry outside [0, num_blocks), a slot past the
+ *   cache, a copy pair outside the pool or a context length past the table never
+ *   touch memory out of bounds — the offending access is skipped (or redirected to
+ *   block 0) and a bit is set in a per-device error word that pkv_read_device_errors()
+ *   returns.  With the debug-sync option on, each call synchronises its stream and
+ *   returns PKV_ERR_DEVICE_CHECK if that word is non-zero.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_ABI_VERSION 1
+
+typedef enum pkv_dtype {
+  PKV_F32 = 0,
+  PKV_BF16 = 1,
+  PKV_FP8_E4M3 = 2,
+  PKV_I32 = 3,
+  PKV_I64 = 4
+} pkv_dtype;
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,
+  PKV_ERR_UNSUPPORTED = 2,
+  PKV_ERR_CUDA = 3,
+  PKV_ERR_DEVICE_CHECK = 4
+} pkv_status;
+
+/* Bits of the per-device error word. */
+#define PKV_DEVERR_TABLE_ENTRY 0x1u  /* block-table entry outside [0, num_blocks) */
+#define PKV_DEVERR_SLOT 0x2u         /* slot >= num_blocks * block_size */
+#define PKV_DEVERR_COPY_PAIR 0x4u    /* copy pair outside [0, num_blocks) */
+#define PKV_DEVERR_CONTEXT_LEN 0x8u  /* context_len < 0 or > max_blocks_per_seq * block_size */
+#define PKV_DEVERR_TIMEOUT 0x10u     /* a bounded wait for an async copy ran out */
+
+typedef struct pkv_tensor {
+  void* data;         /* device pointer */
+  int32_t dtype;      /* a pkv_dtype */
+  int32_t ndim;       /* 1..4 */
+  int64_t shape[4];
+  int64_t stride[4];  /* in elements */
+  float scale;        /* e4m3 caches: dequantisation scale; ignored otherwise */
+} pkv_tensor;
+
+typedef void* pkv_stream; /* a cudaStream_t */
+
+/*
+ * pkv_paged_attention_decode — single-token decode attention over a paged KV cache.
+ *
+ * Defined by: gufacode.com "PagedAttention:KV cache 的页表革命", section
+ * "PagedAttention CUDA Kernel" (per sequence, gather the K/V blocks named by the
+ * block table, then softmax(q K^T) V; the scale multiplies the scores), together with
+ * vasteelab.pages.dev "PagedAttentionとは？", section "tokenを固定長blockへ分ける"
+ * (the kernel walks the table in logical order) and ultralytics.com glossary
+ * "PagedAttention", section "관련 기법" (grouped-query attention: KV heads shared by
+ * groups of query heads).
+ *
+ * For sequence s, query head h, KV head k = h / (num_heads / num_kv_heads), and
+ * L = context_lens[s]:
+ *   K_s[j] = key_cache[block_tables[s][j / block_size], k, j % block_size, :]  (j < L)
+ *   out[s, h, :] = sum_j softmax_j(scale * q[s, h, :] . K_s[j]) * V_s[j]
+ * Only the first ceil(L / block_size) table entries and the first L slots are read;
+ * L == 0 gives a zero row.
+ *
+ * out           [num_seqs, num_heads, head_dim], query's dtype, last dim contiguous.
+ * query         [num_seqs, num_heads, head_dim], f32 or bf16, last dim contiguous.
+ * key_cache,
+ * value_cache   [num_blocks, num_kv_heads, block_size, head_dim], same dtype, shape
+ *               and strides; layout rules above.
+ * block_tables  [num_seqs, max_blocks_per_seq] int32, last dim contiguous.
+ * context_lens  [num_seqs] int32, contiguous; each counts the token just written.
+ * num_kv_heads  must equal key_cache.shape[1] and divide num_heads.
+ * scale         multiplies the scores (usually 1/sqrt(head_dim)).
+ * block_size    must equal key_cache.shape[2].
+ * max_blocks_per_seq  must equal block_tables.shape[1].
+ *
+ * Long contexts are split across thread blocks and merged by a log-sum-exp reduce;
+ * the partial results live in a per-device workspace the library allocates and grows
+ * on demand (growth synchronises the device; it is refused while the stream is being
+ * captured — size it beforehand with pkv_reserve_workspace).
+ */
+pkv_status pkv_paged_attention_decode(const pkv_tensor* out, const pkv_tensor* query,
+                                      const pkv_tensor* key_cache, const pkv_tensor* value_cache,
+                                      const pkv_tensor* block_tables,
+                                      const pkv_tensor* context_lens, int32_t num_kv_heads,
+                                      float scale, int32_t block_size,
+                                      int32_t max_blocks_per_seq, pkv_stream stream);
+
+/*
+ * pkv_reshape_and_cache — write new tokens' K and V into their cache slots.
+ *
+ * Defined by: vasteelab.pages.dev "PagedAttentionとは？", section
+ * "PagedAttentionはAttention kernelとmemory managerの組み合わせである" (K/V are written
+ * through the physical blocks and the slot mapping) and the ultralytics.com glossary's
+ * PyTorch example in section "페이징의 작동 방식" (token at position pos goes to
+ * pool[table[pos / block_size], pos % block_size]); the slot is that position
+ * flattened: slot = table[pos / bs] * bs + pos % bs.
+ *
+ * For token t with slot = slot_mapping[t]:
+ *   slot < 0   nothing is written (padding token);
+ *   otherwise  key_cache[slot / bs, h, slot % bs, :] = encode(key[t, h, :]), same for V.
+ * encode is a bit copy when key and cache dtypes agree.  For an e4m3 cache (key in f32
+ * or bf16) it is e4m3(x / scale), the division in IEEE binary32 and the conversion
+ * round-to-nearest-even with saturation to +-448, scale taken from the cache
+ * descriptor.
+ *
+ * key, value     [num_tokens, num_kv_heads, head_dim], last dim contiguous, same dtype.
+ * key_cache,
+ * value_cache    as for decode (written in place).
+ * slot_mapping   [num_tokens] int64, contiguous.
+ * Slots must be distinct (two tokens writing one slot race).
+ */
+pkv_status pkv_reshape_and_cache(const pkv_tensor* key, const pkv_tensor* value,
+                                 const pkv_tensor* key_cache, const pkv_tensor* value_cache,
+                                 const pkv_tensor* slot_mapping, pkv_stream stream);
+
+/*
+ * pkv_copy_blocks — copy whole physical blocks of one cache tensor.
+ *
+ * Defined by: vasteelab.pages.dev "PagedAttentionとは？", section
+ * "Copy-on-Writeで共通prefixを共有できる", and ultralytics.com glossary
+ * "PagedAttention", section "시퀀스 간 블록 공유": before a sequence writes into a
+ * block that another sequence still references, the engine copies that block.
+ *
+ * For each row (src, dst) of src_dst_pairs: cache[dst, :, :, :] = cache[src, :, :, :]
+ * (all KV heads, byte copy).  Call once for the key cache and once for the value cache.
+ *
+ * cache          [num_blocks, num_kv_heads, block_size, head_dim], layout rules above.
+ * src_dst_pairs  [num_pairs, 2] int64, contiguous; num_pairs may be 0.
+ * Pairs are copied in parallel: destinations must be distinct and no destination may
+ * also be a source (the host side cannot check device-resident pairs; breaking this
+ * gives an unspecified mix of old and new bytes, never an out-of-bounds access).
+ */
+pkv_status pkv_copy_blocks(const pkv_tensor* cache, const pkv_tensor* src_dst_pairs,
+                           pkv_stream stream);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char* pkv_last_error(void);
+
+/* PKV_ABI_VERSION of the loaded library. */
+int32_t pkv_abi_version(void);
+
+/*
+ * Options (process-wide).  PKV_OPT_PARTITION_TOKENS: tokens per context partition of
+ * the decode kernel (0 = chosen from the shape; otherwise a multiple of 64).
+ * PKV_OPT_DEBUG_SYNC: 1 = every call synchronises its stream and checks the device
+ * error word.  PKV_OPT_DRY_RUN: 1 = calls validate their arguments and return without
+ * touching the GPU (lets the host-side checks run on a machine with no GPU).
+ * PKV_OPT_DECODE_KERNEL: 0 = automatic, 1 = CUDA-core kernel, 2 = tensor-core kernel.
+ * pkv_set_option returns PKV_ERR_INVALID_ARG for an unknown option or a bad value.
+ */
+typedef enum pkv_option {
+  PKV_OPT_PARTITION_TOKENS = 0,
+  PKV_OPT_DEBUG_SYNC = 1,
+  PKV_OPT_DRY_RUN = 2,
+  PKV_OPT_DECODE_KERNEL = 3
+} pkv_option;
+
+pkv_status pkv_set_option(int32_t option, int64_t value);
+int64_t pkv_get_option(int32_t option);
+
+/* Make sure the current device's decode workspace holds at least `bytes` bytes
+ * (synchronises the device if it has to grow).  Call before capturing a stream. */
+pkv_status pkv_reserve_workspace(int64_t bytes);
+
+/* Workspace bytes a decode call with these sizes needs (0 if it needs none). */
+int64_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                                   int32_t block_size, int32_t max_blocks_per_seq);
+
+/* Synchronise the current device, return its error word in *flags and clear it. */
+pkv_status pkv_read_device_errors(uint32_t* flags);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t pkv_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

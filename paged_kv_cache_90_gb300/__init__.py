@@ -1,1 +1,10 @@
-"""GB300-native PagedAttention decode: paged K/V cache kernels behind a C ABI."""
+"""GB300-native PagedAttention decode: a paged K/V cache and its hot path
+(slot-mapped cache write, copy-on-write block copy, paged decode attention) as
+hand-written CUDA kernels behind a C ABI (include/pkv.h, libpkv.so).
+
+``binding`` holds the ctypes entry points; ``block_manager`` the host-side block
+pool and tables; ``workloads`` the seeded synthetic inputs.
+"""
+from .binding import (PkvError, copy_blocks, decode_workspace_bytes, launch_count,  # noqa: F401
+                      load_library, paged_attention_decode, read_device_errors,
+                      reserve_workspace, reshape_and_cache, set_option, get_option)

@@ -1,0 +1,175 @@
+"""ctypes binding of libpkv (include/pkv.h).
+
+Argument marshalling only: each function turns torch tensors into pkv_tensor
+descriptors (device pointer, dtype, shape, strides, fp8 scale), passes the current
+CUDA stream, and raises :class:`PkvError` on a non-OK status.  Every step of the work
+runs in the library's CUDA kernels; if the library is not built this module raises
+instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libpkv.so")
+
+PKV_OK = 0
+STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA",
+                4: "PKV_ERR_DEVICE_CHECK"}
+DEVERR = {"table_entry": 0x1, "slot": 0x2, "copy_pair": 0x4, "context_len": 0x8, "timeout": 0x10}
+OPTIONS = {"partition_tokens": 0, "debug_sync": 1, "dry_run": 2, "decode_kernel": 3}
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float8_e4m3fn: 2, torch.int32: 3, torch.int64: 4}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+        self.message = message
+
+
+class PkvTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4), ("scale", ctypes.c_float)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libpkv.so (built in-tree by paged_kv_cache_90_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it with `python -m paged_kv_cache_90_gb300.build` "
+                               "(or __graft_entry__.build()); there is no fallback path")
+        lib = ctypes.CDLL(p)
+        d = ctypes.POINTER(PkvTensor)
+        i32, i64, f32, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
+        lib.pkv_paged_attention_decode.argtypes = [d, d, d, d, d, d, i32, f32, i32, i32, vp]
+        lib.pkv_reshape_and_cache.argtypes = [d, d, d, d, d, vp]
+        lib.pkv_copy_blocks.argtypes = [d, d, vp]
+        for fn in ("pkv_paged_attention_decode", "pkv_reshape_and_cache", "pkv_copy_blocks",
+                   "pkv_set_option", "pkv_reserve_workspace", "pkv_read_device_errors"):
+            getattr(lib, fn).restype = ctypes.c_int
+        lib.pkv_last_error.restype = ctypes.c_char_p
+        lib.pkv_last_error.argtypes = []
+        lib.pkv_abi_version.restype = i32
+        lib.pkv_set_option.argtypes = [i32, i64]
+        lib.pkv_get_option.restype = i64
+        lib.pkv_get_option.argtypes = [i32]
+        lib.pkv_reserve_workspace.argtypes = [i64]
+        lib.pkv_decode_workspace_bytes.restype = i64
+        lib.pkv_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+        lib.pkv_read_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+        lib.pkv_launch_count.restype = ctypes.c_uint64
+        lib.pkv_launch_count.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _check(status: int) -> None:
+    if status != PKV_OK:
+        msg = load_library().pkv_last_error()
+        raise PkvError(status, msg.decode() if msg else "")
+
+
+def describe(t: torch.Tensor, scale: float = 1.0) -> PkvTensor:
+    """pkv_tensor descriptor of a tensor (pointer, dtype code, shape, strides)."""
+    if t.dim() > 4 or t.dim() < 1:
+        raise ValueError("descriptors cover 1 to 4 dimensions")
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"dtype {t.dtype} has no pkv code")
+    d = PkvTensor()
+    d.data = t.data_ptr() if t.numel() else None
+    d.dtype = _DTYPES[t.dtype]
+    d.ndim = t.dim()
+    for i in range(4):
+        d.shape[i] = t.shape[i] if i < t.dim() else 1
+        d.stride[i] = t.stride(i) if i < t.dim() else 1
+    d.scale = float(scale)
+    return d
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        if not torch.cuda.is_available():
+            return ctypes.c_void_p(0)
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def paged_attention_decode(out, query, key_cache, value_cache, block_tables, context_lens,
+                           num_kv_heads: int, scale: float, block_size: int,
+                           max_blocks_per_seq: int, k_scale: float = 1.0, v_scale: float = 1.0,
+                           stream=None) -> torch.Tensor:
+    """Single-token decode attention over the paged cache into ``out`` (returned)."""
+    lib = load_library()
+    descs = [describe(out), describe(query), describe(key_cache, k_scale),
+             describe(value_cache, v_scale), describe(block_tables), describe(context_lens)]
+    _check(lib.pkv_paged_attention_decode(*[ctypes.byref(x) for x in descs], int(num_kv_heads),
+                                          float(scale), int(block_size), int(max_blocks_per_seq),
+                                          _stream(stream)))
+    return out
+
+
+def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, k_scale: float = 1.0,
+                      v_scale: float = 1.0, stream=None) -> None:
+    """Write the new tokens' K/V into their cache slots (in place)."""
+    lib = load_library()
+    descs = [describe(key), describe(value), describe(key_cache, k_scale),
+             describe(value_cache, v_scale), describe(slot_mapping)]
+    _check(lib.pkv_reshape_and_cache(*[ctypes.byref(x) for x in descs], _stream(stream)))
+
+
+def copy_blocks(cache, src_dst_pairs, stream=None) -> None:
+    """cache[dst] = cache[src] for every (src, dst) row of ``src_dst_pairs``."""
+    lib = load_library()
+    pairs = src_dst_pairs
+    if pairs.numel() == 0:
+        pairs = pairs.reshape(0, 2)
+    descs = [describe(cache), describe(pairs)]
+    _check(lib.pkv_copy_blocks(*[ctypes.byref(x) for x in descs], _stream(stream)))
+
+
+def set_option(name: str, value: int) -> None:
+    _check(load_library().pkv_set_option(OPTIONS[name], int(value)))
+
+
+def get_option(name: str) -> int:
+    return int(load_library().pkv_get_option(OPTIONS[name]))
+
+
+def reserve_workspace(nbytes: int) -> None:
+    _check(load_library().pkv_reserve_workspace(int(nbytes)))
+
+
+def decode_workspace_bytes(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq) -> int:
+    return int(load_library().pkv_decode_workspace_bytes(num_seqs, num_heads, head_dim, block_size,
+                                                         max_blocks_per_seq))
+
+
+def read_device_errors() -> int:
+    """Synchronise the current device, return and clear its error word."""
+    flags = ctypes.c_uint32(0)
+    _check(load_library().pkv_read_device_errors(ctypes.byref(flags)))
+    return int(flags.value)
+
+
+def launch_count() -> int:
+    return int(load_library().pkv_launch_count())
+
+
+def abi_version() -> int:
+    return int(load_library().pkv_abi_version())

@@ -1,0 +1,139 @@
+// cache_ops.cu — the slot-mapped cache write (reshape_and_cache) and the whole-block
+// copy used for copy-on-write (copy_blocks).
+//
+// Both are plain HBM streams: 16-byte vector loads and stores, one thread block per
+// token (cache write) or per (pair, KV head) tile (block copy).  Indices taken from
+// device memory are checked before use; a bad one sets a bit in the error word and
+// the access is skipped.
+#include "device_common.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kWriteThreads = 128;
+constexpr int kCopyThreads = 256;
+
+// Same dtype in and out: bit copy of each token's Hk x D row, 16 bytes at a time.
+__global__ void __launch_bounds__(kWriteThreads) cache_write_copy_kernel(const CacheWriteParams p,
+                                                                         int elt_bytes) {
+  const int64_t t = blockIdx.x;
+  const int64_t slot = p.slot_mapping[t];
+  if (slot < 0) return;  // padding token: nothing to write
+  if (slot >= p.num_blocks * p.block_size) {
+    if (threadIdx.x == 0) raise_device_error(p.err, kErrSlot);
+    return;
+  }
+  const int64_t blk = slot / p.block_size;
+  const int64_t off = slot % p.block_size;
+  const int vec_per_head = p.head_dim * elt_bytes / 16;
+  const int nvec = p.num_kv_heads * vec_per_head;
+  for (int i = threadIdx.x; i < nvec; i += kWriteThreads) {
+    const int h = i / vec_per_head;
+    const int v = i % vec_per_head;
+    const int64_t src = (t * p.src_stride_t + h * p.src_stride_h) * elt_bytes + v * 16;
+    const int64_t dst = (blk * p.cs_block + h * p.cs_head + off * p.head_dim) * elt_bytes + v * 16;
+    const uint4 kv = *reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(p.key) + src);
+    const uint4 vv = *reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(p.value) + src);
+    *reinterpret_cast<uint4*>(static_cast<unsigned char*>(p.key_cache) + dst) = kv;
+    *reinterpret_cast<uint4*>(static_cast<unsigned char*>(p.value_cache) + dst) = vv;
+  }
+}
+
+// Eight source values -> eight e4m3 codes: x / scale in IEEE binary32 (correctly
+// rounded division), then round-to-nearest-even with saturation to +-448.
+__device__ __forceinline__ uint2 quantize8(const float* x, float scale) {
+  uint32_t w[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float2 a = make_float2(__fdiv_rn(x[4 * i + 0], scale), __fdiv_rn(x[4 * i + 1], scale));
+    const float2 b = make_float2(__fdiv_rn(x[4 * i + 2], scale), __fdiv_rn(x[4 * i + 3], scale));
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E4M3);
+    w[i] = (lo & 0xffffu) | (hi << 16);
+  }
+  return make_uint2(w[0], w[1]);
+}
+
+template <typename Src>
+__device__ __forceinline__ void load8(const unsigned char* p, float* f);
+template <>
+__device__ __forceinline__ void load8<BF16>(const unsigned char* p, float* f) {
+  Chunk<BF16>::expand(*reinterpret_cast<const uint4*>(p), f);
+}
+template <>
+__device__ __forceinline__ void load8<F32>(const unsigned char* p, float* f) {
+  Chunk<F32>::expand(*reinterpret_cast<const uint4*>(p), f);
+  Chunk<F32>::expand(*reinterpret_cast<const uint4*>(p + 16), f + 4);
+}
+
+// bf16 / f32 source -> e4m3 cache, 8 elements per step.
+template <typename Src>
+__global__ void __launch_bounds__(kWriteThreads) cache_write_e4m3_kernel(const CacheWriteParams p) {
+  const int64_t t = blockIdx.x;
+  const int64_t slot = p.slot_mapping[t];
+  if (slot < 0) return;
+  if (slot >= p.num_blocks * p.block_size) {
+    if (threadIdx.x == 0) raise_device_error(p.err, kErrSlot);
+    return;
+  }
+  const int64_t blk = slot / p.block_size;
+  const int64_t off = slot % p.block_size;
+  const int units_per_head = p.head_dim / 8;
+  const int nunits = p.num_kv_heads * units_per_head;
+  for (int i = threadIdx.x; i < nunits; i += kWriteThreads) {
+    const int h = i / units_per_head;
+    const int u = i % units_per_head;
+    const int64_t src = (t * p.src_stride_t + h * p.src_stride_h + u * 8) * Src::bytes;
+    const int64_t dst = blk * p.cs_block + h * p.cs_head + off * p.head_dim + u * 8;
+    float xk[8], xv[8];
+    load8<Src>(static_cast<const unsigned char*>(p.key) + src, xk);
+    load8<Src>(static_cast<const unsigned char*>(p.value) + src, xv);
+    *reinterpret_cast<uint2*>(static_cast<unsigned char*>(p.key_cache) + dst) = quantize8(xk, p.k_scale);
+    *reinterpret_cast<uint2*>(static_cast<unsigned char*>(p.value_cache) + dst) = quantize8(xv, p.v_scale);
+  }
+}
+
+// One thread block per (pair, KV head): copy the contiguous bs x D tile.
+__global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(const CopyBlocksParams p) {
+  const int64_t pair = blockIdx.x;
+  const int h = blockIdx.y;
+  const int64_t src = p.pairs[2 * pair];
+  const int64_t dst = p.pairs[2 * pair + 1];
+  if (src < 0 || src >= p.num_blocks || dst < 0 || dst >= p.num_blocks) {
+    if (threadIdx.x == 0 && h == 0) raise_device_error(p.err, kErrCopyPair);
+    return;
+  }
+  const uint4* s = reinterpret_cast<const uint4*>(p.cache + src * p.block_stride_bytes + h * p.head_stride_bytes);
+  uint4* d = reinterpret_cast<uint4*>(p.cache + dst * p.block_stride_bytes + h * p.head_stride_bytes);
+  const int64_t nvec = p.chunk_bytes / 16;
+  for (int64_t i = threadIdx.x; i < nvec; i += kCopyThreads) d[i] = s[i];
+}
+
+}  // namespace
+
+cudaError_t launch_reshape_and_cache(const CacheWriteParams& p, cudaStream_t stream) {
+  if (p.num_tokens == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(p.num_tokens));
+  if (p.cache_dtype == p.src_dtype) {
+    const int elt = p.cache_dtype == kF32 ? 4 : p.cache_dtype == kBF16 ? 2 : 1;
+    cache_write_copy_kernel<<<grid, kWriteThreads, 0, stream>>>(p, elt);
+  } else if (p.src_dtype == kBF16) {
+    cache_write_e4m3_kernel<BF16><<<grid, kWriteThreads, 0, stream>>>(p);
+  } else {
+    cache_write_e4m3_kernel<F32><<<grid, kWriteThreads, 0, stream>>>(p);
+  }
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(const CopyBlocksParams& p, cudaStream_t stream) {
+  if (p.num_pairs == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(p.num_pairs), static_cast<unsigned>(p.num_kv_heads));
+  copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,485 @@
+// pkv_api.cu — the C ABI of libpkv (declared in include/pkv.h): argument checks,
+// kernel selection, the per-device decode workspace, options and error reporting.
+// All GPU work is queued on the caller's stream; nothing here blocks unless the
+// debug-sync option is on or the decode workspace has to grow.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "../../include/pkv.h"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+// The per-device error word the kernels OR their PKV_DEVERR_* bits into.
+__device__ unsigned int g_error_word;
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+std::atomic<int64_t> g_opt_partition_tokens{0};
+std::atomic<int64_t> g_opt_debug_sync{0};
+std::atomic<int64_t> g_opt_dry_run{0};
+std::atomic<int64_t> g_opt_decode_kernel{0};
+
+thread_local std::string t_last_error;
+
+pkv_status fail(pkv_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return st;
+}
+
+pkv_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  unsigned int* err = nullptr;  // address of g_error_word on this device
+  int num_sms = 0;
+  void* ws = nullptr;           // decode workspace
+  size_t ws_bytes = 0;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+pkv_status device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&s.err), g_error_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    s.ready = true;
+  }
+  *out = &s;
+  return PKV_OK;
+}
+
+// Grow the current device's workspace to `bytes` (synchronises the device first so no
+// queued kernel still uses the old buffer; refused during stream capture).
+pkv_status ensure_workspace(DeviceState* s, size_t bytes, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (bytes <= s->ws_bytes) return PKV_OK;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t ce = cudaStreamIsCapturing(stream, &cs);
+  if (ce != cudaSuccess) return cuda_fail(ce, "cudaStreamIsCapturing");
+  if (cs != cudaStreamCaptureStatusNone)
+    return fail(PKV_ERR_INVALID_ARG,
+                "decode needs %zu workspace bytes but only %zu are reserved and the stream is "
+                "being captured; call pkv_reserve_workspace before capture",
+                bytes, s->ws_bytes);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize (workspace growth)");
+  if (s->ws) {
+    e = cudaFree(s->ws);
+    s->ws = nullptr;
+    s->ws_bytes = 0;
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFree (workspace)");
+  }
+  const size_t rounded = (bytes + (1u << 20) - 1) & ~size_t((1u << 20) - 1);
+  e = cudaMalloc(&s->ws, rounded);
+  if (e != cudaSuccess) {
+    s->ws = nullptr;
+    return cuda_fail(e, "cudaMalloc (workspace)");
+  }
+  s->ws_bytes = rounded;
+  return PKV_OK;
+}
+
+pkv_status finish_call(DeviceState* s, cudaError_t launch_err, cudaStream_t stream, const char* what) {
+  if (launch_err != cudaSuccess) return cuda_fail(launch_err, what);
+  if (g_opt_debug_sync.load()) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    unsigned int word = 0;
+    e = cudaMemcpy(&word, s->err, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (word) {
+      const unsigned int zero = 0;
+      cudaMemcpy(s->err, &zero, sizeof zero, cudaMemcpyHostToDevice);
+      return fail(PKV_ERR_DEVICE_CHECK, "%s: device-side check failed (error word 0x%x)", what, word);
+    }
+  }
+  t_last_error.clear();
+  return PKV_OK;
+}
+
+// ---- descriptor checks -------------------------------------------------------------
+int elt_bytes(int dtype) {
+  switch (dtype) {
+    case PKV_F32: return 4;
+    case PKV_BF16: return 2;
+    case PKV_FP8_E4M3: return 1;
+    case PKV_I32: return 4;
+    case PKV_I64: return 8;
+    default: return 0;
+  }
+}
+
+const char* dtype_name(int dtype) {
+  switch (dtype) {
+    case PKV_F32: return "f32";
+    case PKV_BF16: return "bf16";
+    case PKV_FP8_E4M3: return "fp8_e4m3";
+    case PKV_I32: return "i32";
+    case PKV_I64: return "i64";
+    default: return "?";
+  }
+}
+
+int64_t numel(const pkv_tensor* t) {
+  int64_t n = 1;
+  for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
+  return n;
+}
+
+pkv_status check_basic(const pkv_tensor* t, const char* name, int ndim) {
+  if (!t) return fail(PKV_ERR_INVALID_ARG, "%s: null descriptor", name);
+  if (t->ndim != ndim) return fail(PKV_ERR_INVALID_ARG, "%s: expected %d dimensions, got %d", name, ndim, t->ndim);
+  if (elt_bytes(t->dtype) == 0) return fail(PKV_ERR_INVALID_ARG, "%s: unknown dtype %d", name, t->dtype);
+  for (int i = 0; i < ndim; ++i) {
+    if (t->shape[i] < 0) return fail(PKV_ERR_INVALID_ARG, "%s: negative size in dimension %d", name, i);
+    if (t->stride[i] < 0) return fail(PKV_ERR_INVALID_ARG, "%s: negative stride in dimension %d", name, i);
+  }
+  if (numel(t) > 0 && t->data == nullptr) return fail(PKV_ERR_INVALID_ARG, "%s: null data pointer", name);
+  if (t->stride[ndim - 1] != 1 && t->shape[ndim - 1] > 1)
+    return fail(PKV_ERR_INVALID_ARG, "%s: last dimension must be contiguous (stride 1)", name);
+  return PKV_OK;
+}
+
+pkv_status check_dtype(const pkv_tensor* t, const char* name, int a, int b = -1, int c = -1) {
+  if (t->dtype == a || t->dtype == b || t->dtype == c) return PKV_OK;
+  return fail(PKV_ERR_UNSUPPORTED, "%s: dtype %s is not supported here", name, dtype_name(t->dtype));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pkv_status check_cache(const pkv_tensor* c, const char* name) {
+  pkv_status st = check_basic(c, name, 4);
+  if (st) return st;
+  if ((st = check_dtype(c, name, PKV_F32, PKV_BF16, PKV_FP8_E4M3))) return st;
+  const int64_t D = c->shape[3];
+  if (c->shape[2] > 1 && c->stride[2] != D)
+    return fail(PKV_ERR_INVALID_ARG, "%s: the (block_size, head_dim) tile must be contiguous (stride[2] == head_dim)", name);
+  const int eb = elt_bytes(c->dtype);
+  if (!aligned16(c->data) || (c->stride[0] * eb) % 16 || (c->stride[1] * eb) % 16)
+    return fail(PKV_ERR_INVALID_ARG, "%s: base pointer and block/head strides must be multiples of 16 bytes", name);
+  if (c->dtype == PKV_FP8_E4M3 && !(std::isfinite(c->scale) && c->scale > 0.f))
+    return fail(PKV_ERR_INVALID_ARG, "%s: an e4m3 cache needs a finite positive scale", name);
+  return PKV_OK;
+}
+
+bool same_layout(const pkv_tensor* a, const pkv_tensor* b) {
+  if (a->dtype != b->dtype || a->ndim != b->ndim) return false;
+  for (int i = 0; i < a->ndim; ++i)
+    if (a->shape[i] != b->shape[i] || a->stride[i] != b->stride[i]) return false;
+  return true;
+}
+
+bool supported_head_dim(int64_t d) { return d == 64 || d == 128; }
+bool supported_block_size(int64_t bs) { return bs == 2 || bs == 4 || bs == 8 || bs == 16 || bs == 32; }
+
+int choose_partition_tokens(int64_t max_ctx) {
+  const int64_t opt = g_opt_partition_tokens.load();
+  if (opt > 0) return int(opt);
+  if (max_ctx <= 512) return int(((max_ctx > 0 ? max_ctx : 1) + 255) / 256 * 256);
+  return 512;
+}
+
+}  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char* pkv_last_error(void) { return t_last_error.c_str(); }
+
+int32_t pkv_abi_version(void) { return PKV_ABI_VERSION; }
+
+uint64_t pkv_launch_count(void) { return g_launches.load(); }
+
+pkv_status pkv_set_option(int32_t option, int64_t value) {
+  switch (option) {
+    case PKV_OPT_PARTITION_TOKENS:
+      if (value < 0 || value % 256 || value > (1 << 20))
+        return fail(PKV_ERR_INVALID_ARG, "partition tokens must be 0 or a positive multiple of 256 up to 2^20");
+      g_opt_partition_tokens = value;
+      return PKV_OK;
+    case PKV_OPT_DEBUG_SYNC:
+      if (value != 0 && value != 1) return fail(PKV_ERR_INVALID_ARG, "debug sync is 0 or 1");
+      g_opt_debug_sync = value;
+      return PKV_OK;
+    case PKV_OPT_DRY_RUN:
+      if (value != 0 && value != 1) return fail(PKV_ERR_INVALID_ARG, "dry run is 0 or 1");
+      g_opt_dry_run = value;
+      return PKV_OK;
+    case PKV_OPT_DECODE_KERNEL:
+      if (value < 0 || value > 2) return fail(PKV_ERR_INVALID_ARG, "decode kernel is 0, 1 or 2");
+      g_opt_decode_kernel = value;
+      return PKV_OK;
+    default:
+      return fail(PKV_ERR_INVALID_ARG, "unknown option %d", option);
+  }
+}
+
+int64_t pkv_get_option(int32_t option) {
+  switch (option) {
+    case PKV_OPT_PARTITION_TOKENS: return g_opt_partition_tokens.load();
+    case PKV_OPT_DEBUG_SYNC: return g_opt_debug_sync.load();
+    case PKV_OPT_DRY_RUN: return g_opt_dry_run.load();
+    case PKV_OPT_DECODE_KERNEL: return g_opt_decode_kernel.load();
+    default: return -1;
+  }
+}
+
+int64_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                                   int32_t block_size, int32_t max_blocks_per_seq) {
+  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || block_size <= 0 || max_blocks_per_seq <= 0)
+    return 0;
+  const int64_t max_ctx = int64_t(max_blocks_per_seq) * block_size;
+  const int pt = choose_partition_tokens(max_ctx);
+  const int64_t parts = (max_ctx + pt - 1) / pt;
+  if (parts <= 1) return 0;
+  return int64_t(num_seqs) * num_heads * parts * (head_dim + 2) * 4;
+}
+
+pkv_status pkv_reserve_workspace(int64_t bytes) {
+  if (bytes < 0) return fail(PKV_ERR_INVALID_ARG, "negative workspace size");
+  if (g_opt_dry_run.load()) return PKV_OK;
+  DeviceState* s;
+  pkv_status st = device_state(&s);
+  if (st) return st;
+  return ensure_workspace(s, size_t(bytes), nullptr);
+}
+
+pkv_status pkv_read_device_errors(uint32_t* flags) {
+  if (!flags) return fail(PKV_ERR_INVALID_ARG, "null flags pointer");
+  *flags = 0;
+  if (g_opt_dry_run.load()) return PKV_OK;
+  DeviceState* s;
+  pkv_status st = device_state(&s);
+  if (st) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  unsigned int word = 0;
+  e = cudaMemcpy(&word, s->err, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  const unsigned int zero = 0;
+  e = cudaMemcpy(s->err, &zero, sizeof zero, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+  *flags = word;
+  t_last_error.clear();
+  return PKV_OK;
+}
+
+pkv_status pkv_paged_attention_decode(const pkv_tensor* out, const pkv_tensor* query,
+                                      const pkv_tensor* key_cache, const pkv_tensor* value_cache,
+                                      const pkv_tensor* block_tables,
+                                      const pkv_tensor* context_lens, int32_t num_kv_heads,
+                                      float scale, int32_t block_size,
+                                      int32_t max_blocks_per_seq, pkv_stream stream) {
+  pkv_status st;
+  if ((st = check_basic(out, "out", 3)) || (st = check_basic(query, "query", 3)) ||
+      (st = check_cache(key_cache, "key_cache")) || (st = check_cache(value_cache, "value_cache")) ||
+      (st = check_basic(block_tables, "block_tables", 2)) ||
+      (st = check_basic(context_lens, "context_lens", 1)))
+    return st;
+  if ((st = check_dtype(query, "query", PKV_F32, PKV_BF16))) return st;
+  if ((st = check_dtype(block_tables, "block_tables", PKV_I32))) return st;
+  if ((st = check_dtype(context_lens, "context_lens", PKV_I32))) return st;
+  if (out->dtype != query->dtype) return fail(PKV_ERR_INVALID_ARG, "out must have the query's dtype");
+  const int64_t S = query->shape[0], Hq = query->shape[1], D = query->shape[2];
+  if (out->shape[0] != S || out->shape[1] != Hq || out->shape[2] != D)
+    return fail(PKV_ERR_INVALID_ARG, "out shape must equal query shape [%lld, %lld, %lld]",
+                (long long)S, (long long)Hq, (long long)D);
+  if (!same_layout(key_cache, value_cache))
+    return fail(PKV_ERR_INVALID_ARG, "key_cache and value_cache must share dtype, shape and strides");
+  const int64_t NB = key_cache->shape[0];
+  if (num_kv_heads <= 0 || key_cache->shape[1] != num_kv_heads)
+    return fail(PKV_ERR_INVALID_ARG, "num_kv_heads (%d) must equal key_cache.shape[1] (%lld)", num_kv_heads,
+                (long long)key_cache->shape[1]);
+  if (Hq % num_kv_heads != 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_heads (%lld) must be a multiple of num_kv_heads (%d)", (long long)Hq,
+                num_kv_heads);
+  if (key_cache->shape[2] != block_size)
+    return fail(PKV_ERR_INVALID_ARG, "block_size (%d) must equal key_cache.shape[2] (%lld)", block_size,
+                (long long)key_cache->shape[2]);
+  if (key_cache->shape[3] != D)
+    return fail(PKV_ERR_INVALID_ARG, "key_cache head_dim (%lld) must equal query head_dim (%lld)",
+                (long long)key_cache->shape[3], (long long)D);
+  if (!supported_head_dim(D)) return fail(PKV_ERR_UNSUPPORTED, "head_dim %lld (supported: 64, 128)", (long long)D);
+  if (!supported_block_size(block_size))
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 2, 4, 8, 16, 32)", block_size);
+  if (block_tables->shape[0] != S || block_tables->shape[1] != max_blocks_per_seq)
+    return fail(PKV_ERR_INVALID_ARG, "block_tables must be [num_seqs=%lld, max_blocks_per_seq=%d]", (long long)S,
+                max_blocks_per_seq);
+  if (context_lens->shape[0] != S) return fail(PKV_ERR_INVALID_ARG, "context_lens must be [num_seqs]");
+  if (max_blocks_per_seq < 1) return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq must be >= 1");
+  const int64_t max_ctx = int64_t(max_blocks_per_seq) * block_size;
+  if (max_ctx > (int64_t(1) << 30)) return fail(PKV_ERR_UNSUPPORTED, "max context above 2^30 tokens");
+  if (S > 65535 || Hq > 65535)
+    return fail(PKV_ERR_UNSUPPORTED, "num_seqs and num_heads must be <= 65535");
+  if (!(std::isfinite(scale))) return fail(PKV_ERR_INVALID_ARG, "scale must be finite");
+  if (NB < 1) return fail(PKV_ERR_INVALID_ARG, "the cache holds no block");
+  if (g_opt_decode_kernel.load() == 2) return fail(PKV_ERR_UNSUPPORTED, "the tensor-core decode kernel is not built");
+
+  const int pt = choose_partition_tokens(max_ctx);
+  const int64_t parts = (max_ctx + pt - 1) / pt;
+  if (parts > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many context partitions; raise the partition size");
+  if (g_opt_dry_run.load() || S == 0) return PKV_OK;
+
+  DeviceState* s;
+  if ((st = device_state(&s))) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+
+  DecodeParams p{};
+  p.out = out->data;
+  p.out_dtype = out->dtype;
+  p.out_stride_s = out->stride[0];
+  p.out_stride_h = out->stride[1];
+  p.query = query->data;
+  p.q_dtype = query->dtype;
+  p.q_stride_s = query->stride[0];
+  p.q_stride_h = query->stride[1];
+  p.key_cache = key_cache->data;
+  p.value_cache = value_cache->data;
+  p.kv_dtype = key_cache->dtype;
+  p.cs_block = key_cache->stride[0];
+  p.cs_head = key_cache->stride[1];
+  p.block_tables = static_cast<const int32_t*>(block_tables->data);
+  p.bt_stride = block_tables->stride[0];
+  p.context_lens = static_cast<const int32_t*>(context_lens->data);
+  p.num_seqs = int(S);
+  p.num_heads = int(Hq);
+  p.num_kv_heads = num_kv_heads;
+  p.head_dim = int(D);
+  p.block_size = block_size;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_blocks = NB;
+  p.group = int(Hq / num_kv_heads);
+  const float kscale = key_cache->dtype == PKV_FP8_E4M3 ? key_cache->scale : 1.0f;
+  p.qk_scale_log2 = float(double(scale) * 1.4426950408889634 * double(kscale));
+  p.v_scale = value_cache->dtype == PKV_FP8_E4M3 ? value_cache->scale : 1.0f;
+  p.partition_tokens = pt;
+  p.max_partitions = int(parts);
+  p.err = s->err;
+  if (parts > 1) {
+    const size_t rows = size_t(S) * size_t(Hq) * size_t(parts);
+    if ((st = ensure_workspace(s, rows * (size_t(D) + 2) * 4, cs))) return st;
+    p.part_o = static_cast<float*>(s->ws);
+    p.part_m = p.part_o + rows * size_t(D);
+    p.part_l = p.part_m + rows;
+  }
+  return finish_call(s, launch_decode(p, cs), cs, "paged_attention_decode");
+}
+
+pkv_status pkv_reshape_and_cache(const pkv_tensor* key, const pkv_tensor* value,
+                                 const pkv_tensor* key_cache, const pkv_tensor* value_cache,
+                                 const pkv_tensor* slot_mapping, pkv_stream stream) {
+  pkv_status st;
+  if ((st = check_basic(key, "key", 3)) || (st = check_basic(value, "value", 3)) ||
+      (st = check_cache(key_cache, "key_cache")) || (st = check_cache(value_cache, "value_cache")) ||
+      (st = check_basic(slot_mapping, "slot_mapping", 1)))
+    return st;
+  if ((st = check_dtype(key, "key", PKV_F32, PKV_BF16, PKV_FP8_E4M3))) return st;
+  if ((st = check_dtype(slot_mapping, "slot_mapping", PKV_I64))) return st;
+  if (!same_layout(key, value)) return fail(PKV_ERR_INVALID_ARG, "key and value must share dtype, shape and strides");
+  if (!same_layout(key_cache, value_cache))
+    return fail(PKV_ERR_INVALID_ARG, "key_cache and value_cache must share dtype, shape and strides");
+  const int64_t T = key->shape[0], Hk = key->shape[1], D = key->shape[2];
+  if (key_cache->shape[1] != Hk || key_cache->shape[3] != D)
+    return fail(PKV_ERR_INVALID_ARG, "key [T, %lld, %lld] does not match the cache's [.., %lld, .., %lld]",
+                (long long)Hk, (long long)D, (long long)key_cache->shape[1], (long long)key_cache->shape[3]);
+  if (slot_mapping->shape[0] != T) return fail(PKV_ERR_INVALID_ARG, "slot_mapping must be [num_tokens]");
+  if (!supported_head_dim(D)) return fail(PKV_ERR_UNSUPPORTED, "head_dim %lld (supported: 64, 128)", (long long)D);
+  if (!supported_block_size(key_cache->shape[2]))
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %lld (supported: 2, 4, 8, 16, 32)", (long long)key_cache->shape[2]);
+  const bool same = key->dtype == key_cache->dtype;
+  const bool quant = key_cache->dtype == PKV_FP8_E4M3 && (key->dtype == PKV_F32 || key->dtype == PKV_BF16);
+  if (!same && !quant)
+    return fail(PKV_ERR_UNSUPPORTED, "writing %s tokens into a %s cache", dtype_name(key->dtype),
+                dtype_name(key_cache->dtype));
+  const int eb = elt_bytes(key->dtype);
+  if (!aligned16(key->data) || !aligned16(value->data) || (key->stride[0] * eb) % 16 || (key->stride[1] * eb) % 16)
+    return fail(PKV_ERR_INVALID_ARG, "key/value base pointers and strides must be multiples of 16 bytes");
+  if (T > 0x7fffffff) return fail(PKV_ERR_UNSUPPORTED, "too many tokens in one call");
+  if (g_opt_dry_run.load() || T == 0) return PKV_OK;
+
+  DeviceState* s;
+  if ((st = device_state(&s))) return st;
+  CacheWriteParams p{};
+  p.key = key->data;
+  p.value = value->data;
+  p.src_stride_t = key->stride[0];
+  p.src_stride_h = key->stride[1];
+  p.src_dtype = key->dtype;
+  p.key_cache = key_cache->data;
+  p.value_cache = value_cache->data;
+  p.cs_block = key_cache->stride[0];
+  p.cs_head = key_cache->stride[1];
+  p.cache_dtype = key_cache->dtype;
+  p.k_scale = key_cache->scale;
+  p.v_scale = value_cache->scale;
+  p.slot_mapping = static_cast<const int64_t*>(slot_mapping->data);
+  p.num_tokens = T;
+  p.num_kv_heads = int(Hk);
+  p.head_dim = int(D);
+  p.block_size = int(key_cache->shape[2]);
+  p.num_blocks = key_cache->shape[0];
+  p.err = s->err;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  return finish_call(s, launch_reshape_and_cache(p, cs), cs, "reshape_and_cache");
+}
+
+pkv_status pkv_copy_blocks(const pkv_tensor* cache, const pkv_tensor* src_dst_pairs, pkv_stream stream) {
+  pkv_status st;
+  if ((st = check_cache(cache, "cache")) || (st = check_basic(src_dst_pairs, "src_dst_pairs", 2))) return st;
+  if ((st = check_dtype(src_dst_pairs, "src_dst_pairs", PKV_I64))) return st;
+  if (src_dst_pairs->shape[1] != 2 || (src_dst_pairs->shape[0] > 1 && src_dst_pairs->stride[0] != 2))
+    return fail(PKV_ERR_INVALID_ARG, "src_dst_pairs must be a contiguous [num_pairs, 2] array");
+  if (!supported_head_dim(cache->shape[3]))
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %lld (supported: 64, 128)", (long long)cache->shape[3]);
+  if (!supported_block_size(cache->shape[2]))
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %lld (supported: 2, 4, 8, 16, 32)", (long long)cache->shape[2]);
+  const int64_t n = src_dst_pairs->shape[0];
+  if (n > 0x7fffffff || cache->shape[1] > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many pairs or heads");
+  if (g_opt_dry_run.load() || n == 0) return PKV_OK;
+
+  DeviceState* s;
+  if ((st = device_state(&s))) return st;
+  const int eb = elt_bytes(cache->dtype);
+  CopyBlocksParams p{};
+  p.cache = static_cast<unsigned char*>(cache->data);
+  p.block_stride_bytes = cache->stride[0] * eb;
+  p.head_stride_bytes = cache->stride[1] * eb;
+  p.chunk_bytes = cache->shape[2] * cache->shape[3] * eb;
+  p.num_kv_heads = int(cache->shape[1]);
+  p.pairs = static_cast<const int64_t*>(src_dst_pairs->data);
+  p.num_pairs = n;
+  p.num_blocks = cache->shape[0];
+  p.err = s->err;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  return finish_call(s, launch_copy_blocks(p, cs), cs, "copy_blocks");
+}
+
+}  // extern "C"

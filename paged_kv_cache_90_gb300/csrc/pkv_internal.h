@@ -1,0 +1,94 @@
+// pkv_internal.h — launch parameters and launchers shared between the C-ABI host
+// layer (pkv_api.cu) and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pkv {
+
+enum DType { kF32 = 0, kBF16 = 1, kE4M3 = 2, kI32 = 3, kI64 = 4 };
+
+// Counts kernel launches made by the library (pkv_launch_count()).
+void note_launch();
+
+// ---- reshape_and_cache --------------------------------------------------------------
+struct CacheWriteParams {
+  const void* key;           // [T, Hk, D]
+  const void* value;
+  int64_t src_stride_t;      // elements
+  int64_t src_stride_h;
+  int src_dtype;             // kF32 / kBF16
+  void* key_cache;           // [NB, Hk, bs, D], token stride = D
+  void* value_cache;
+  int64_t cs_block;          // elements
+  int64_t cs_head;
+  int cache_dtype;           // kF32 / kBF16 / kE4M3
+  float k_scale;             // e4m3 cache: value = code * scale
+  float v_scale;
+  const int64_t* slot_mapping;
+  int64_t num_tokens;
+  int num_kv_heads;
+  int head_dim;
+  int block_size;
+  int64_t num_blocks;
+  unsigned int* err;         // per-device error word
+};
+cudaError_t launch_reshape_and_cache(const CacheWriteParams& p, cudaStream_t stream);
+
+// ---- copy_blocks ------------------------------------------------------------------
+struct CopyBlocksParams {
+  unsigned char* cache;      // base of block 0
+  int64_t block_stride_bytes;
+  int64_t head_stride_bytes;
+  int64_t chunk_bytes;       // bs * D * elt: one (block, head) tile, contiguous
+  int num_kv_heads;
+  const int64_t* pairs;      // [n, 2]
+  int64_t num_pairs;
+  int64_t num_blocks;
+  unsigned int* err;
+};
+cudaError_t launch_copy_blocks(const CopyBlocksParams& p, cudaStream_t stream);
+
+// ---- paged decode attention ------------------------------------------------------
+struct DecodeParams {
+  void* out;                 // [S, Hq, D]
+  int out_dtype;
+  int64_t out_stride_s, out_stride_h;
+  const void* query;         // [S, Hq, D]
+  int q_dtype;
+  int64_t q_stride_s, q_stride_h;
+  const void* key_cache;     // [NB, Hk, bs, D]
+  const void* value_cache;
+  int kv_dtype;
+  int64_t cs_block, cs_head; // elements
+  const int32_t* block_tables;
+  int64_t bt_stride;
+  const int32_t* context_lens;
+  int num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq;
+  int64_t num_blocks;
+  int group;                 // num_heads / num_kv_heads
+  float qk_scale_log2;       // scale * log2(e) * k_scale
+  float v_scale;
+  int partition_tokens;      // multiple of 256
+  int max_partitions;        // ceil(max_blocks_per_seq * block_size / partition_tokens)
+  float* part_o;             // [S, Hq, P, D]   (P = max_partitions; unused when P == 1)
+  float* part_m;             // [S, Hq, P]
+  float* part_l;             // [S, Hq, P]
+  unsigned int* err;
+};
+
+// Heads of one KV-head group handled by one thread block (divides p.group).
+int decode_heads_per_cta(int group);
+// Dynamic shared memory the CUDA-core decode kernel needs.
+size_t decode_smem_bytes(int kv_dtype, int head_dim, int heads_per_cta, int partition_tokens,
+                         int block_size);
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+
+// Per-dtype launchers (one translation unit each).
+cudaError_t launch_decode_f32(const DecodeParams& p, int g, cudaStream_t stream);
+cudaError_t launch_decode_bf16(const DecodeParams& p, int g, cudaStream_t stream);
+cudaError_t launch_decode_e4m3(const DecodeParams& p, int g, cudaStream_t stream);
+cudaError_t launch_decode_reduce(const DecodeParams& p, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,70 @@
+"""One decode step of a serving engine, on the device, through the C ABI.
+
+A step is the whole hot path for one batch: copy-on-write block copies (if any
+sequence writes into a shared block), the new tokens' cache write, then decode
+attention over every sequence's paged context (vasteelab.pages.dev
+"PagedAttentionとは？", section "PagedAttentionはAttention kernelとmemory managerの
+組み合わせである": the scheduler reserves blocks, the runner hands the mapping to the
+kernels).  This module only moves tensors and calls :mod:`binding`; every step runs in
+the library's kernels.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import List, Optional
+
+import torch
+
+from . import binding
+from .workloads import DecodeStep, Workload
+
+
+@dataclass
+class DeviceStep:
+    query: torch.Tensor
+    new_key: torch.Tensor
+    new_value: torch.Tensor
+    slot_mapping: torch.Tensor
+    block_tables: torch.Tensor
+    context_lens: torch.Tensor
+    cow_pairs: torch.Tensor
+
+    @staticmethod
+    def from_host(st: DecodeStep, device, pin: bool = False) -> "DeviceStep":
+        def mv(t):
+            return t.to(device, non_blocking=pin)
+        return DeviceStep(*(mv(getattr(st, f)) for f in DeviceStep.__dataclass_fields__))
+
+
+class DeviceWorkload:
+    """A workload's caches and step inputs resident on one GPU."""
+
+    def __init__(self, w: Workload, device: str = "cuda"):
+        self.w = w
+        self.device = torch.device(device)
+        self.key_cache = w.key_cache.to(self.device)
+        self.value_cache = w.value_cache.to(self.device)
+        self.steps: List[DeviceStep] = [DeviceStep.from_host(st, self.device) for st in w.steps]
+        s, hq, d = w.steps[0].query.shape
+        self.out = torch.empty(s, hq, d, dtype=w.q_dtype, device=self.device)
+
+    def run_step(self, i: int, out: Optional[torch.Tensor] = None, stream=None,
+                 step: Optional[DeviceStep] = None) -> torch.Tensor:
+        """Run step ``i`` (or the given device-resident inputs) on the current
+        stream; returns the decode output tensor."""
+        st = step if step is not None else self.steps[i]
+        out = self.out if out is None else out
+        run_decode_step(self.w, self.key_cache, self.value_cache, st, out, stream)
+        return out
+
+
+def run_decode_step(w: Workload, key_cache, value_cache, st: DeviceStep, out, stream=None) -> None:
+    if st.cow_pairs.numel():
+        binding.copy_blocks(key_cache, st.cow_pairs, stream)
+        binding.copy_blocks(value_cache, st.cow_pairs, stream)
+    if st.slot_mapping.numel():
+        binding.reshape_and_cache(st.new_key, st.new_value, key_cache, value_cache, st.slot_mapping,
+                                  w.k_scale, w.v_scale, stream)
+    binding.paged_attention_decode(out, st.query, key_cache, value_cache, st.block_tables,
+                                   st.context_lens, w.num_kv_heads, w.scale, w.block_size,
+                                   w.max_blocks_per_seq, w.k_scale, w.v_scale, stream)

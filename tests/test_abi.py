@@ -1,0 +1,142 @@
+"""The C ABI without a GPU: the library builds and loads, exports every function
+include/pkv.h declares, and its host-side argument checks accept good descriptors
+and reject bad ones (dry-run mode: validation only, nothing touches the GPU)."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+import torch
+
+from paged_kv_cache_90_gb300 import binding
+from paged_kv_cache_90_gb300 import build as pkv_build
+
+HEADER = Path(__file__).resolve().parent.parent / "include" / "pkv.h"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkv_build.build()
+    return binding.load_library()
+
+
+@pytest.fixture
+def dry(lib):
+    binding.set_option("dry_run", 1)
+    yield lib
+    binding.set_option("dry_run", 0)
+    binding.set_option("partition_tokens", 0)
+
+
+def declared_functions():
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert {"pkv_paged_attention_decode", "pkv_reshape_and_cache", "pkv_copy_blocks"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} is declared in pkv.h but not exported"
+    assert binding.abi_version() == 1
+
+
+def _decode_args(S=3, Hq=8, Hk=2, D=128, bs=16, NB=20, MB=4, dtype=torch.bfloat16, kv=torch.bfloat16):
+    q = torch.zeros(S, Hq, D, dtype=dtype)
+    return dict(out=torch.empty_like(q), query=q,
+                key_cache=torch.zeros(NB, Hk, bs, D, dtype=kv), value_cache=torch.zeros(NB, Hk, bs, D, dtype=kv),
+                block_tables=torch.zeros(S, MB, dtype=torch.int32), context_lens=torch.ones(S, dtype=torch.int32),
+                num_kv_heads=Hk, scale=D ** -0.5, block_size=bs, max_blocks_per_seq=MB)
+
+
+def _status(fn, **kw):
+    try:
+        fn(**kw)
+        return 0
+    except binding.PkvError as e:
+        assert e.message, "a failing call must leave a message"
+        return e.status
+
+
+def test_decode_validation(dry):
+    ok = _decode_args()
+    assert _status(binding.paged_attention_decode, **ok) == 0
+    assert _status(binding.paged_attention_decode, **_decode_args(kv=torch.float8_e4m3fn),
+                   k_scale=0.01, v_scale=0.02) == 0
+    assert _status(binding.paged_attention_decode, **_decode_args(dtype=torch.float32, kv=torch.float32, D=64)) == 0
+    bad = []
+    a = _decode_args(); a["num_kv_heads"] = 3; bad.append((a, 1))                 # != cache heads
+    a = _decode_args(Hq=6, Hk=4); bad.append((a, 1))                              # Hq % Hk
+    a = _decode_args(); a["block_size"] = 8; bad.append((a, 1))                   # != cache bs
+    a = _decode_args(); a["max_blocks_per_seq"] = 5; bad.append((a, 1))           # != table width
+    a = _decode_args(D=96); bad.append((a, 2))                                    # head_dim
+    a = _decode_args(bs=64); bad.append((a, 2))                                   # block size
+    a = _decode_args(); a["out"] = torch.empty(3, 8, 128, dtype=torch.float32); bad.append((a, 1))
+    a = _decode_args(); a["block_tables"] = a["block_tables"].long(); bad.append((a, 2))
+    a = _decode_args(); a["context_lens"] = torch.ones(2, dtype=torch.int32); bad.append((a, 1))
+    a = _decode_args(); a["value_cache"] = torch.zeros(20, 2, 16, 128, dtype=torch.float32); bad.append((a, 1))
+    a = _decode_args(); a["query"] = a["query"].transpose(1, 2).contiguous().transpose(1, 2); bad.append((a, 1))
+    a = _decode_args(kv=torch.float8_e4m3fn); bad.append((dict(a, k_scale=0.0), 1))  # fp8 scale
+    a = _decode_args(); a["scale"] = float("inf"); bad.append((a, 1))
+    for args, want in bad:
+        extra = {}
+        if "k_scale" in args:
+            extra["k_scale"] = args.pop("k_scale")
+        assert _status(binding.paged_attention_decode, **args, **extra) == want, args
+
+
+def test_decode_rejects_misaligned_cache(dry):
+    a = _decode_args()
+    big = torch.zeros(20 * 2 * 16 * 128 + 4, dtype=torch.bfloat16)
+    a["key_cache"] = big[1:1 + 20 * 2 * 16 * 128].view(20, 2, 16, 128)   # 2-byte offset
+    a["value_cache"] = big[1:1 + 20 * 2 * 16 * 128].view(20, 2, 16, 128)
+    assert _status(binding.paged_attention_decode, **a) == 1
+
+
+def test_cache_views_with_block_stride(dry):
+    """K and V as views of one [NB, 2, Hk, bs, D] tensor: strided blocks are fine."""
+    a = _decode_args()
+    both = torch.zeros(20, 2, 2, 16, 128, dtype=torch.bfloat16)
+    a["key_cache"], a["value_cache"] = both[:, 0], both[:, 1]
+    assert _status(binding.paged_attention_decode, **a) == 0
+
+
+def test_reshape_and_cache_validation(dry):
+    kc = torch.zeros(10, 2, 16, 128, dtype=torch.bfloat16)
+    k = torch.zeros(4, 2, 128, dtype=torch.bfloat16)
+    sm = torch.zeros(4, dtype=torch.int64)
+    assert _status(binding.reshape_and_cache, key=k, value=k, key_cache=kc, value_cache=kc, slot_mapping=sm) == 0
+    f8 = torch.zeros(10, 2, 16, 128, dtype=torch.float8_e4m3fn)
+    assert _status(binding.reshape_and_cache, key=k, value=k, key_cache=f8, value_cache=f8,
+                   slot_mapping=sm, k_scale=0.5, v_scale=0.5) == 0
+    assert _status(binding.reshape_and_cache, key=k.float(), value=k.float(), key_cache=kc, value_cache=kc,
+                   slot_mapping=sm) == 2                                            # f32 -> bf16
+    assert _status(binding.reshape_and_cache, key=k, value=k, key_cache=kc, value_cache=kc,
+                   slot_mapping=sm.int()) == 2                                      # slot dtype
+    assert _status(binding.reshape_and_cache, key=k, value=k, key_cache=kc, value_cache=kc,
+                   slot_mapping=sm[:3]) == 1                                        # count
+    assert _status(binding.reshape_and_cache, key=k[:, :1], value=k[:, :1], key_cache=kc, value_cache=kc,
+                   slot_mapping=sm) == 1                                            # heads
+
+
+def test_copy_blocks_validation(dry):
+    c = torch.zeros(10, 2, 16, 128, dtype=torch.bfloat16)
+    assert _status(binding.copy_blocks, cache=c, src_dst_pairs=torch.zeros(3, 2, dtype=torch.int64)) == 0
+    assert _status(binding.copy_blocks, cache=c, src_dst_pairs=torch.zeros(0, 2, dtype=torch.int64)) == 0
+    assert _status(binding.copy_blocks, cache=c, src_dst_pairs=torch.zeros(3, 3, dtype=torch.int64)) == 1
+    assert _status(binding.copy_blocks, cache=c, src_dst_pairs=torch.zeros(3, 2, dtype=torch.int32)) == 2
+
+
+def test_options_and_workspace_size(lib):
+    with pytest.raises(binding.PkvError):
+        binding.set_option("partition_tokens", 100)
+    binding.set_option("partition_tokens", 1024)
+    assert binding.get_option("partition_tokens") == 1024
+    binding.set_option("partition_tokens", 0)
+    # 8 sequences of up to 2048 blocks of 16 tokens: 64 partitions of 512 tokens
+    assert binding.decode_workspace_bytes(8, 32, 128, 16, 2048) == 8 * 32 * 64 * 130 * 4
+    assert binding.decode_workspace_bytes(3, 4, 64, 16, 3) == 0
+    with pytest.raises(KeyError):
+        binding.set_option("nope", 1)
+    assert lib.pkv_set_option(99, 0) == 1

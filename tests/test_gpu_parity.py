@@ -1,0 +1,312 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, on the same
+seeded inputs.  Cache writes and block copies must match bit for bit; decode outputs
+within the stated max-abs tolerances (f32 1e-5, bf16 2e-2, fp8 K/V 5e-2) and, more
+tightly, within the final output rounding (2^-8 relative for a bf16 output)."""
+import os
+
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_90_gb300 import binding
+from paged_kv_cache_90_gb300 import build as pkv_build
+from paged_kv_cache_90_gb300 import workloads as wl
+from paged_kv_cache_90_gb300.decode_step import DeviceWorkload
+
+pytestmark = pytest.mark.gpu
+
+THREADS = max(1, min(16, len(os.sched_getaffinity(0))))
+MAX_ABS = {torch.float32: 1e-5, torch.bfloat16: 2e-2, torch.float8_e4m3fn: 5e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pkv_build.build()
+    oracle.build()
+    binding.load_library()
+    yield
+    binding.set_option("partition_tokens", 0)
+    binding.set_option("debug_sync", 0)
+
+
+@pytest.fixture
+def partition_tokens():
+    def set_(n):
+        binding.set_option("partition_tokens", n)
+    yield set_
+    binding.set_option("partition_tokens", 0)
+
+
+def run_device(w):
+    dw = DeviceWorkload(w)
+    outs = []
+    for i in range(len(w.steps)):
+        outs.append(dw.run_step(i, out=torch.empty_like(dw.out)).clone())
+    torch.cuda.synchronize()
+    assert binding.read_device_errors() == 0
+    return [o.double().cpu() for o in outs], dw.key_cache.cpu(), dw.value_cache.cpu()
+
+
+def run_oracle(w):
+    kc, vc = w.key_cache.clone(), w.value_cache.clone()
+    outs = [oracle.run_workload_step(w, i, kc, vc, THREADS) for i in range(len(w.steps))]
+    return outs, kc, vc
+
+
+def raw(t):
+    return t.view(torch.uint8) if t.element_size() == 1 else t.view(torch.int16 if t.element_size() == 2 else torch.int32)
+
+
+def assert_decode_close(got, ref, w):
+    err = (got - ref).abs()
+    assert torch.isfinite(got).all()
+    worst = MAX_ABS[w.kv_dtype] if w.kv_dtype == torch.float8_e4m3fn else MAX_ABS[w.q_dtype]
+    assert err.max().item() <= worst, f"max abs err {err.max().item()} > {worst}"
+    if w.q_dtype == torch.bfloat16:
+        tight = 2.0 ** -8 * ref.abs() + 2e-5
+    else:
+        tight = 2e-6 * ref.abs() + 2e-6
+    bad = (err > tight).sum().item()
+    assert bad == 0, f"{bad} outputs beyond the rounding bound (max err {err.max().item():.3e})"
+
+
+def check_workload(w):
+    outs, kc, vc = run_device(w)
+    routs, rkc, rvc = run_oracle(w)
+    assert torch.equal(raw(kc), raw(rkc)), "key cache differs from the oracle's"
+    assert torch.equal(raw(vc), raw(rvc)), "value cache differs from the oracle's"
+    for got, ref in zip(outs, routs):
+        assert_decode_close(got, ref, w)
+    return outs, routs
+
+
+# --- the five workloads, scaled to seconds of oracle time and at full size ----------
+
+def test_tiny_f32():
+    check_workload(wl.tiny())
+
+
+@pytest.mark.parametrize("layout", [(0, 1), (4, 1), (5, 2)])
+def test_scalar_example_padded(layout):
+    """keys 0, query 1, values 1..5 at block size 4: 3 for every layout (head padded
+    with zeros to 64 dims, which leaves q.k unchanged)."""
+    w = wl.scalar_example(physical=layout, num_blocks=8, head_dim=64)
+    outs, _, _ = run_device(w)
+    got = outs[0][0, 0]
+    assert abs(got[0].item() - 3.0) <= 1e-6
+    assert torch.all(got[1:] == 0)
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_llama3_shaped_small(bs):
+    check_workload(wl.llama3_8b_decode(seed=2, num_seqs=8, len_range=(128, 600), block_size=bs, poison=True))
+
+
+def test_llama3_shaped_peaked_queries():
+    """Queries scaled by 8: concentrated attention, |out| of order 1."""
+    w = wl.llama3_8b_decode(seed=21, num_seqs=6, len_range=(100, 900), poison=True)
+    w.steps[0].query.mul_(8)
+    outs, routs = check_workload(w)
+    assert routs[0].abs().max() > 0.5
+
+
+def test_llama3_shaped_full():
+    check_workload(wl.llama3_8b_decode())
+
+
+@pytest.mark.parametrize("bs", [16, 32])
+def test_long_context_small(bs):
+    check_workload(wl.long_context(block_size=bs, num_seqs=2, context_len=5000, poison=True))
+
+
+@pytest.mark.parametrize("bs", [16, 32])
+def test_long_context_full(bs):
+    check_workload(wl.long_context(block_size=bs))
+
+
+def test_shared_prefix_cow_small():
+    w = wl.shared_prefix_cow(num_groups=4, prefix_blocks=8, suffix_range=(16, 120), poison=True)
+    assert w.steps[0].cow_pairs.shape[0] == 12
+    check_workload(w)
+
+
+def test_shared_prefix_cow_full():
+    w = wl.shared_prefix_cow()
+    assert w.steps[0].cow_pairs.shape[0] == 96
+    check_workload(w)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_continuous_batching_small(bs, kv):
+    check_workload(wl.continuous_batching(block_size=bs, kv_dtype=kv, num_seqs=24, num_steps=3,
+                                          median=200, cap=2000, poison=True))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_continuous_batching_full(bs, kv):
+    check_workload(wl.continuous_batching(block_size=bs, kv_dtype=kv))
+
+
+# --- edge cases -----------------------------------------------------------------
+
+def test_partition_edges(partition_tokens):
+    """Lengths around partition and block boundaries with 256-token partitions, so the
+    log-sum-exp reduce merges 1..5 partitions."""
+    partition_tokens(256)
+    check_workload(wl.variable_length_decode("edges", 30, [1, 2, 255, 256, 257, 511, 512, 513, 1000, 1280],
+                                             8, 2, 128, 16, "bf16", poison=True))
+
+
+@pytest.mark.parametrize("hq,hk,d,bs,kv,q", [
+    (6, 2, 128, 16, "bf16", "bf16"),    # 3 query heads per KV head -> one head per block
+    (16, 2, 128, 16, "bf16", "bf16"),   # 8 per KV head
+    (4, 4, 128, 16, "bf16", "bf16"),    # no grouping
+    (8, 2, 64, 2, "bf16", "bf16"),      # head_dim 64, block size 2
+    (8, 4, 64, 4, "e4m3", "bf16"),
+    (8, 2, 128, 8, "bf16", "f32"),      # f32 queries over a bf16 cache
+    (4, 2, 128, 32, "f32", "f32"),
+    (16, 2, 64, 8, "e4m3", "f32"),
+])
+def test_shapes_and_dtypes(hq, hk, d, bs, kv, q):
+    check_workload(wl.variable_length_decode("shapes", 40 + hq + d + bs, [1, 7, bs, 3 * bs + 1, 300, 777],
+                                             hq, hk, d, bs, kv, q_dtype=q, poison=True, num_steps=2))
+
+
+def test_zero_length_and_empty_batch():
+    w = wl.variable_length_decode("z", 50, [5, 40], 8, 2, 128, 16, "bf16", poison=True)
+    dw = DeviceWorkload(w)
+    st = dw.steps[0]
+    dw.run_step(0)
+    cl = st.context_lens.clone()
+    cl[0] = 0
+    out = torch.full_like(dw.out, 7.0)
+    binding.paged_attention_decode(out, st.query, dw.key_cache, dw.value_cache, st.block_tables, cl,
+                                   w.num_kv_heads, w.scale, w.block_size, w.max_blocks_per_seq)
+    torch.cuda.synchronize()
+    assert torch.all(out[0] == 0)
+    # an empty batch is a no-op
+    e = torch.empty(0, 8, 128, dtype=torch.bfloat16, device="cuda")
+    binding.paged_attention_decode(e, e, dw.key_cache, dw.value_cache,
+                                   torch.empty(0, w.max_blocks_per_seq, dtype=torch.int32, device="cuda"),
+                                   torch.empty(0, dtype=torch.int32, device="cuda"),
+                                   w.num_kv_heads, w.scale, w.block_size, w.max_blocks_per_seq)
+    assert binding.read_device_errors() == 0
+
+
+def test_strided_cache_views_and_side_stream():
+    """K and V as views of one [NB, 2, Hk, bs, D] tensor, work on a non-default stream."""
+    w = wl.variable_length_decode("views", 60, [3, 90, 400], 8, 2, 128, 16, "bf16", poison=True)
+    nb = w.num_blocks
+    both = torch.empty(nb, 2, 2, 16, 128, dtype=torch.bfloat16, device="cuda")
+    both[:, 0] = w.key_cache.cuda()
+    both[:, 1] = w.value_cache.cuda()
+    kc, vc = both[:, 0], both[:, 1]
+    st = DeviceWorkload(w).steps[0]
+    out = torch.empty(3, 8, 128, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        binding.reshape_and_cache(st.new_key, st.new_value, kc, vc, st.slot_mapping)
+        binding.paged_attention_decode(out, st.query, kc, vc, st.block_tables, st.context_lens, 2, w.scale,
+                                       16, w.max_blocks_per_seq)
+        pairs = torch.tensor([[int(st.block_tables[0, 0]), nb - 1]], dtype=torch.int64, device="cuda")
+    s.synchronize()
+    routs, rkc, rvc = run_oracle(w)
+    assert_decode_close(out.double().cpu(), routs[0], w)
+    assert torch.equal(raw(kc.cpu()), raw(rkc))
+    with torch.cuda.stream(s):
+        binding.copy_blocks(kc, pairs)
+    s.synchronize()
+    assert torch.equal(raw(kc[nb - 1].cpu()), raw(rkc[int(st.block_tables[0, 0])]))
+    assert torch.equal(raw(vc.cpu()), raw(rvc))       # V untouched by the K copy
+
+
+@pytest.mark.parametrize("src,dst", [("f32", "f32"), ("bf16", "bf16"), ("bf16", "e4m3"), ("f32", "e4m3")])
+def test_cache_write_bit_exact(src, dst):
+    """Every slot kind: regular, padding (-1), first/last slot of the pool; e4m3 with
+    values beyond the saturation point."""
+    g = torch.Generator().manual_seed(70)
+    nb, hk, bs, d, t = 12, 4, 16, 128, 40
+    dt = wl.DTYPES
+    kc = torch.randn(nb, hk, bs, d, generator=g).to(dt[dst] if dst != "e4m3" else torch.float32)
+    if dst == "e4m3":
+        kc = (kc / 0.02).clamp(-448, 448).to(torch.float8_e4m3fn)
+    vc = kc.clone()
+    key = (torch.randn(t, hk, d, generator=g) * 3).to(dt[src])
+    value = (torch.randn(t, hk, d, generator=g) * 50).to(dt[src])
+    slots = torch.randperm(nb * bs, generator=g)[:t]
+    slots[3] = -1
+    slots[7] = 0
+    slots[8] = nb * bs - 1
+    ks, vs = (0.02, 0.05) if dst == "e4m3" else (1.0, 1.0)
+    dk, dv = kc.cuda(), vc.cuda()
+    binding.reshape_and_cache(key.cuda(), value.cuda(), dk, dv, slots.cuda(), ks, vs)
+    torch.cuda.synchronize()
+    rk, rv = kc.clone(), vc.clone()
+    oracle.reshape_and_cache(key, value, rk, rv, slots, ks, vs)
+    assert torch.equal(raw(dk.cpu()), raw(rk))
+    assert torch.equal(raw(dv.cpu()), raw(rv))
+    assert binding.read_device_errors() == 0
+
+
+def test_copy_blocks_bit_exact():
+    g = torch.Generator().manual_seed(80)
+    cache = torch.randn(40, 8, 16, 128, generator=g).to(torch.bfloat16)
+    pairs = torch.tensor([[1, 30], [5, 31], [5, 32], [39, 0], [17, 18]], dtype=torch.int64)
+    d = cache.cuda()
+    binding.copy_blocks(d, pairs.cuda())
+    torch.cuda.synchronize()
+    ref = cache.clone()
+    oracle.copy_blocks(ref, pairs)
+    assert torch.equal(raw(d.cpu()), raw(ref))
+
+
+def test_device_checks_flag_bad_indices():
+    """Out-of-range table entries, slots, copy pairs and context lengths are caught
+    on the device: the access is skipped or redirected in bounds and a bit is set."""
+    w = wl.variable_length_decode("bad", 90, [20, 40], 8, 2, 128, 16, "bf16")
+    dw = DeviceWorkload(w)
+    st = dw.steps[0]
+    assert binding.read_device_errors() == 0
+    bt = st.block_tables.clone()
+    bt[1, 1] = w.num_blocks + 3
+    binding.paged_attention_decode(dw.out, st.query, dw.key_cache, dw.value_cache, bt, st.context_lens,
+                                   2, w.scale, 16, w.max_blocks_per_seq)
+    assert binding.read_device_errors() == binding.DEVERR["table_entry"]
+    sm = st.slot_mapping.clone()
+    sm[0] = w.num_blocks * 16
+    before = dw.key_cache.clone()
+    binding.reshape_and_cache(st.new_key[:1], st.new_value[:1], dw.key_cache, dw.value_cache, sm[:1])
+    assert binding.read_device_errors() == binding.DEVERR["slot"]
+    assert torch.equal(raw(dw.key_cache), raw(before))
+    binding.copy_blocks(dw.key_cache, torch.tensor([[0, w.num_blocks]], dtype=torch.int64, device="cuda"))
+    assert binding.read_device_errors() == binding.DEVERR["copy_pair"]
+    cl = st.context_lens.clone()
+    cl[0] = w.max_blocks_per_seq * 16 + 1
+    binding.paged_attention_decode(dw.out, st.query, dw.key_cache, dw.value_cache, st.block_tables, cl,
+                                   2, w.scale, 16, w.max_blocks_per_seq)
+    assert binding.read_device_errors() & binding.DEVERR["context_len"]
+    binding.set_option("debug_sync", 1)
+    try:
+        with pytest.raises(binding.PkvError) as ei:
+            binding.paged_attention_decode(dw.out, st.query, dw.key_cache, dw.value_cache, bt,
+                                           st.context_lens, 2, w.scale, 16, w.max_blocks_per_seq)
+        assert ei.value.status == 4
+    finally:
+        binding.set_option("debug_sync", 0)
+    assert binding.read_device_errors() == 0
+
+
+def test_launch_count_and_determinism():
+    w = wl.llama3_8b_decode(seed=99, num_seqs=4, len_range=(600, 1500))
+    dw = DeviceWorkload(w)
+    n0 = binding.launch_count()
+    a = dw.run_step(0, out=torch.empty_like(dw.out)).clone()
+    b = dw.run_step(0, out=torch.empty_like(dw.out)).clone()   # same slot rewritten with the same data
+    torch.cuda.synchronize()
+    assert binding.launch_count() - n0 == 2 * 3                 # write, decode, reduce
+    assert torch.equal(a, b)
