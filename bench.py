@@ -1,0 +1,422 @@
+"""Benchmark of the paged decode hot path on GB300.
+
+A step is one pass of the whole path over one batch: copy-on-write block copies (when
+the workload has shared blocks), the new tokens' cache write, and paged decode
+attention for every sequence.  Inputs are synthetic and seeded
+(paged_kv_cache_90_gb300.workloads); the default workload is the Llama-3-8B-shaped
+decode layer (64 sequences, contexts uniform in [128, 2048] plus the new token,
+32/8 heads, head_dim 128, bf16, block size 16).
+
+Metric: effective GB/s = algorithmic bytes of a step / step time, where the bytes are
+those the step must move: every context token's K and V (for its KV head), the
+queries, the outputs, the block-table entries and lengths, the new tokens read and
+written, and the copied blocks.  Timing: CUDA events on the launching stream around
+each step, the L2 flushed (a 256 MiB write) between steps outside the events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_90_gb300 import binding, workloads as wl  # noqa: E402
+from paged_kv_cache_90_gb300.decode_step import DeviceStep, DeviceWorkload, run_decode_step  # noqa: E402
+
+METRIC = "paged decode attention: effective KV-read GB/s (% of HBM peak), µs/step"
+UNIT = "GB/s"
+L2_FLUSH_BYTES = 256 << 20
+DECODE_SOURCES = ["decode_core.cuh", "decode_mma.cuh", "decode_dispatch.cu", "device_common.cuh"]
+
+
+# ---- workloads -----------------------------------------------------------------------
+
+def make_workload(name: str, rank: int = 0) -> wl.Workload:
+    seed_off = 1000 * rank
+    if name == "llama3_8b_decode":
+        return wl.llama3_8b_decode(seed=2 + seed_off)
+    if name.startswith("long_context"):
+        bs = 32 if name.endswith("bs32") else 16
+        return wl.long_context(seed=3 + seed_off, block_size=bs)
+    if name == "shared_prefix_cow":
+        return wl.shared_prefix_cow(seed=4 + seed_off)
+    m = re.fullmatch(r"continuous_batching_bs(\d+)_(bf16|e4m3)", name)
+    if m:
+        return wl.continuous_batching(seed=5 + seed_off, block_size=int(m.group(1)), kv_dtype=m.group(2))
+    if name == "tiny":
+        return wl.tiny(seed=1 + seed_off)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def describe_workload(w: wl.Workload, name: str) -> str:
+    L = torch.cat([st.context_lens for st in w.steps]).float()
+    return (f"{name}: {w.num_seqs} seqs, {w.num_heads}/{w.num_kv_heads} heads, head_dim {w.head_dim}, "
+            f"{wl.DTYPE_NAMES[w.kv_dtype]} KV, block {w.block_size}, ctx mean {L.mean():.0f} "
+            f"[{int(L.min())}, {int(L.max())}], {len(w.steps)} distinct step(s)")
+
+
+def decode_bytes(w: wl.Workload, st) -> int:
+    """Bytes paged decode must move for one step: K and V of every context token of
+    every KV head, queries in, outputs out, table entries and lengths."""
+    elt = w.key_cache.element_size()
+    L = st.context_lens.long()
+    kv = int(L.sum()) * w.num_kv_heads * w.head_dim * elt * 2
+    q = st.query.numel() * st.query.element_size()
+    tbl = int(((L + w.block_size - 1) // w.block_size).sum()) * 4 + 4 * L.numel()
+    return kv + 2 * q + tbl
+
+
+def step_bytes(w: wl.Workload, st) -> int:
+    """Decode bytes plus the cache write (new K/V read, slots read, cache written)
+    and the copy-on-write block copies (read + write, K and V)."""
+    elt = w.key_cache.element_size()
+    t = st.slot_mapping.numel()
+    write = 2 * st.new_key.numel() * st.new_key.element_size() + 8 * t + 2 * t * w.num_kv_heads * w.head_dim * elt
+    blk = w.num_kv_heads * w.block_size * w.head_dim * elt
+    cow = st.cow_pairs.shape[0] * blk * 2 * 2 + st.cow_pairs.numel() * 8
+    return decode_bytes(w, st) + write + cow
+
+
+# ---- helpers -------------------------------------------------------------------------
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        p = os.path.join(ROOT, "paged_kv_cache_90_gb300", "csrc", name)
+        if os.path.exists(p):
+            with open(p, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """dram read+write bytes per decode launch from the committed ncu summary for this
+    workload, if it was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", f"paged_decode_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    text = open(p).read()
+    m_src = re.search(r"kernel sources digest:\s*`?([0-9a-f]+)`?", text)
+    m_tr = re.search(r"dram bytes per launch \(read \+ write\):\s*([0-9]+)", text)
+    if not m_src or not m_tr or m_src.group(1) != source_digest():
+        return None
+    return int(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except Exception:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        inside = [r for r in rows if t0 - 1.0 <= r[0] <= t1 + 1.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+def oracle_throughput(w: wl.Workload, budget_s: float, max_seqs=None):
+    """Time the CPU oracle on whole sequences of the first step until ~budget_s of CPU
+    work is done; returns (GB/s of needed bytes, threads, description)."""
+    import oracle
+    oracle.build()
+    threads = len(os.sched_getaffinity(0))
+    st = w.steps[0]
+    kc, vc = w.key_cache.clone(), w.value_cache.clone()
+    if st.cow_pairs.numel():
+        oracle.copy_blocks(kc, st.cow_pairs)
+        oracle.copy_blocks(vc, st.cow_pairs)
+    oracle.reshape_and_cache(st.new_key, st.new_value, kc, vc, st.slot_mapping, w.k_scale, w.v_scale)
+    s_total = st.query.shape[0]
+    n = s_total if max_seqs is None else max(1, min(s_total, max_seqs))
+    done_bytes, elapsed, reps = 0, 0.0, 0
+    while True:
+        sub = wl.DecodeStep(st.query[:n], st.new_key[:n], st.new_value[:n], st.slot_mapping[:n],
+                            st.block_tables[:n], st.context_lens[:n], st.cow_pairs[:0])
+        t = time.perf_counter()
+        oracle.paged_attention_decode(sub.query, kc, vc, sub.block_tables, sub.context_lens, w.scale,
+                                      w.k_scale, w.v_scale, threads)
+        elapsed += time.perf_counter() - t
+        done_bytes += decode_bytes(w, sub)
+        reps += 1
+        if elapsed >= budget_s or reps >= 50:
+            break
+    desc = f"fp64 C oracle decode of the first {n} of {s_total} sequences x {reps} repetition(s), {elapsed:.1f} s"
+    return done_bytes / elapsed / 1e9, threads, desc
+
+
+# ---- the two arms --------------------------------------------------------------------
+
+def init_dist(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl != "reference" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    w = make_workload(args.workload)
+    steps = args.warmup + args.steps
+    # calibrate: one sequence, then size the per-step sample to fit ~2 minutes overall
+    gbs1, threads, _ = oracle_throughput(w, 0.0, max_seqs=1)
+    per_seq = decode_bytes(w, w.steps[0]) / w.num_seqs / (gbs1 * 1e9)
+    target = max(0.05, min(2.0, 120.0 / steps))
+    n = max(1, min(w.num_seqs, int(target / max(per_seq, 1e-9))))
+    vals, total = [], 0.0
+    for i in range(steps):
+        g, threads, desc = oracle_throughput(w, 0.0, max_seqs=n)
+        if i >= args.warmup:
+            vals.append(g)
+    value = statistics.median(vals)
+    sample = f"each step: fp64 C oracle decode of the first {n} of {w.num_seqs} sequences ({args.workload})"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe_workload(w, args.workload), "l2": "n/a (host)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args, world, rank, local):
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the reference arm is --impl reference)")
+    dev = torch.device("cuda", local)
+    binding.load_library()
+    w = make_workload(args.workload, rank)
+    dw = DeviceWorkload(w, dev)
+    nsteps = len(w.steps)
+    if binding.decode_workspace_bytes(w.num_seqs, w.num_heads, w.head_dim, w.block_size, w.max_blocks_per_seq):
+        binding.reserve_workspace(binding.decode_workspace_bytes(
+            w.num_seqs, w.num_heads, w.head_dim, w.block_size, w.max_blocks_per_seq))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- device-resident timing (value) ----
+    for i in range(args.warmup):
+        flush.zero_()
+        dw.run_step(i % nsteps)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
+                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    n0 = binding.launch_count()
+    t0 = time.time()
+    for k in range(args.steps):
+        flush.zero_()
+        st = dw.steps[k % nsteps]
+        a, b, c = ev[k]
+        a.record(stream)
+        if st.cow_pairs.numel():
+            binding.copy_blocks(dw.key_cache, st.cow_pairs)
+            binding.copy_blocks(dw.value_cache, st.cow_pairs)
+        if st.slot_mapping.numel():
+            binding.reshape_and_cache(st.new_key, st.new_value, dw.key_cache, dw.value_cache, st.slot_mapping,
+                                      w.k_scale, w.v_scale)
+        b.record(stream)
+        binding.paged_attention_decode(dw.out, st.query, dw.key_cache, dw.value_cache, st.block_tables,
+                                       st.context_lens, w.num_kv_heads, w.scale, w.block_size,
+                                       w.max_blocks_per_seq, w.k_scale, w.v_scale)
+        c.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    launches = binding.launch_count() - n0
+    barrier()
+    time.sleep(0.2)
+    clocks.stop()
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    dec_ms = [b.elapsed_time(c) for _, b, c in ev]
+    total_ms = sum(step_ms)
+    flags = binding.read_device_errors()
+    if flags:
+        raise SystemExit(f"device error word 0x{flags:x} during the bench")
+
+    bytes_steps = [step_bytes(w, w.steps[k % nsteps]) for k in range(args.steps)]
+    dec_bytes = [decode_bytes(w, w.steps[k % nsteps]) for k in range(args.steps)]
+    my_time = torch.tensor([total_ms], dtype=torch.float64)
+    my_bytes = torch.tensor([float(sum(bytes_steps))], dtype=torch.float64)
+    if world > 1:
+        import torch.distributed as dist
+        t_ = my_time.to(dev)
+        b_ = my_bytes.to(dev)
+        dist.all_reduce(t_, op=dist.ReduceOp.MAX)
+        dist.all_reduce(b_, op=dist.ReduceOp.SUM)
+        my_time, my_bytes = t_.cpu(), b_.cpu()
+    max_ms = float(my_time[0])
+    value = float(my_bytes[0]) / (max_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API from pinned host buffers (e2e) ----
+    fields = ("query", "new_key", "new_value", "slot_mapping", "block_tables", "context_lens", "cow_pairs")
+    host_steps = [DeviceStep(*(getattr(st, f).pin_memory() for f in fields)) for st in w.steps]
+    dev_in = [DeviceStep(*(torch.empty_like(getattr(st, f), device=dev) for f in fields)) for st in w.steps]
+    out_host = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
+    h2d = sum(getattr(host_steps[0], f).numel() * getattr(host_steps[0], f).element_size() for f in fields)
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_steps = max(10, min(args.steps, 200))
+    for k in range(3):
+        i = k % nsteps
+        for f in fields:
+            getattr(dev_in[i], f).copy_(getattr(host_steps[i], f), non_blocking=True)
+        run_decode_step(w, dw.key_cache, dw.value_cache, dev_in[i], dw.out)
+        out_host.copy_(dw.out, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e_ms = 0.0
+    for k in range(e2e_steps):
+        flush.zero_()
+        i = k % nsteps
+        a, _, c = ev[k % len(ev)]
+        a.record(stream)
+        for f in fields:
+            getattr(dev_in[i], f).copy_(getattr(host_steps[i], f), non_blocking=True)
+        run_decode_step(w, dw.key_cache, dw.value_cache, dev_in[i], dw.out)
+        out_host.copy_(dw.out, non_blocking=True)
+        c.record(stream)
+        c.synchronize()
+        e_ms += a.elapsed_time(c)
+    e2e_bytes = sum(step_bytes(w, w.steps[k % nsteps]) for k in range(e2e_steps))
+    e2e_value = e2e_bytes / (e_ms * 1e-3) / 1e9
+
+    if rank != 0:
+        return 0
+    peak, peak_kind = load_peaks()
+    dec_avg_s = sum(dec_ms) / len(dec_ms) * 1e-3
+    achieved = (sum(dec_bytes) / len(dec_bytes)) / dec_avg_s / 1e9
+    traffic = profiled_traffic(args.workload)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "kernel": "paged_attention_decode (main + log-sum-exp reduce)", "peak_kind": peak_kind}
+    cpu_base = None
+    if world == 1 and not args.no_cpu_baseline:
+        g, threads, desc = oracle_throughput(w, args.cpu_budget)
+        cpu_base = {"value": round(g, 4), "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.DTYPE_NAMES[w.kv_dtype], "data": "synthetic",
+        "config": {"workload": describe_workload(w, args.workload), "l2": "flushed between steps (256 MiB write)",
+                   "accumulate": "f32", "us_per_step": round(max_ms / args.steps * 1e3, 2),
+                   "decode_us": round(dec_avg_s * 1e6, 2),
+                   "tokens_per_s": round(w.num_seqs * world / (max_ms / args.steps * 1e-3), 1),
+                   "pct_of_8TBps": round(value / 8000 * 100, 2), "parallelism": f"replicas x{world}"},
+        "roofline": roofline,
+        "cpu_baseline": cpu_base,
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(launches),
+        "clocks": clocks.summary(t0, t1),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
+    ap.add_argument("--workload", default="llama3_8b_decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle CPU time")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("at least 3 warm-up steps")
+    world, rank, local = init_dist(args)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_gpu(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())
