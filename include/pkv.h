@@ -176,6 +176,40 @@ pkv_status pkv_reshape_and_cache(const pkv_tensor* key, const pkv_tensor* value,
 pkv_status pkv_copy_blocks(const pkv_tensor* cache, const pkv_tensor* src_dst_pairs,
                            pkv_stream stream);
 
+/*
+ * pkv_paged_attention_decode_noalloc — the same decode as pkv_paged_attention_decode,
+ * for callers that must not allocate device memory.  (No counterpart on the pages: it
+ * exists for embedding, not for the method.)
+ *
+ * Who needs it: a serving engine that reserves almost all device memory up front for
+ * its KV-cache pool and its own caching allocator, where a library's cudaMalloc can
+ * fail or take memory the engine cannot account for; and latency-critical decode loops,
+ * where cudaMalloc / cudaFree may synchronise the device.  This entry point calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Arguments, results and errors are those of pkv_paged_attention_decode, except that
+ * the partial results of split contexts go to a fixed scratch array compiled into the
+ * library (pkv_noalloc_scratch_bytes(), 16 MiB), which every GPU that loads the library
+ * holds until the process exits.  A call that would need more scratch than that
+ * (num_seqs * num_heads * partitions * (head_dim + 2) * 4 bytes) returns
+ * PKV_ERR_INVALID_ARG with a message and queues nothing.
+ * The first call on each device looks up the array's device address (and may load the
+ * library's device code there): make it before any stream capture.  All calls on a
+ * device share the array, so calls whose GPU work overlaps (unordered streams) race on
+ * it; calls ordered on one stream are safe.
+ */
+pkv_status pkv_paged_attention_decode_noalloc(const pkv_tensor* out, const pkv_tensor* query,
+                                              const pkv_tensor* key_cache,
+                                              const pkv_tensor* value_cache,
+                                              const pkv_tensor* block_tables,
+                                              const pkv_tensor* context_lens,
+                                              int32_t num_kv_heads, float scale,
+                                              int32_t block_size, int32_t max_blocks_per_seq,
+                                              pkv_stream stream);
+
+/* Size in bytes of the static scratch used by pkv_paged_attention_decode_noalloc. */
+int64_t pkv_noalloc_scratch_bytes(void);
+
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char* pkv_last_error(void);
 

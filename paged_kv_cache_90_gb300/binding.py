@@ -58,7 +58,11 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.pkv_paged_attention_decode.argtypes = [d, d, d, d, d, d, i32, f32, i32, i32, vp]
         lib.pkv_reshape_and_cache.argtypes = [d, d, d, d, d, vp]
         lib.pkv_copy_blocks.argtypes = [d, d, vp]
-        for fn in ("pkv_paged_attention_decode", "pkv_reshape_and_cache", "pkv_copy_blocks",
+        lib.pkv_paged_attention_decode_noalloc.argtypes = [d, d, d, d, d, d, i32, f32, i32, i32, vp]
+        lib.pkv_noalloc_scratch_bytes.restype = i64
+        lib.pkv_noalloc_scratch_bytes.argtypes = []
+        for fn in ("pkv_paged_attention_decode", "pkv_paged_attention_decode_noalloc",
+                   "pkv_reshape_and_cache", "pkv_copy_blocks",
                    "pkv_set_option", "pkv_reserve_workspace", "pkv_read_device_errors"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.pkv_last_error.restype = ctypes.c_char_p
@@ -122,6 +126,28 @@ def paged_attention_decode(out, query, key_cache, value_cache, block_tables, con
                                           float(scale), int(block_size), int(max_blocks_per_seq),
                                           _stream(stream)))
     return out
+
+
+def paged_attention_decode_noalloc(out, query, key_cache, value_cache, block_tables, context_lens,
+                                   num_kv_heads: int, scale: float, block_size: int,
+                                   max_blocks_per_seq: int, k_scale: float = 1.0,
+                                   v_scale: float = 1.0, stream=None) -> torch.Tensor:
+    """Decode attention that allocates no device memory: partial results of split
+    contexts go to the library's fixed 16 MiB scratch array instead of a workspace
+    grown with cudaMalloc (for callers that own all device memory, or must not let
+    an allocation synchronise the device).  Calls on one device share that scratch,
+    so calls on unordered streams must not overlap."""
+    lib = load_library()
+    descs = [describe(out), describe(query), describe(key_cache, k_scale),
+             describe(value_cache, v_scale), describe(block_tables), describe(context_lens)]
+    _check(lib.pkv_paged_attention_decode_noalloc(*[ctypes.byref(x) for x in descs],
+                                                  int(num_kv_heads), float(scale), int(block_size),
+                                                  int(max_blocks_per_seq), _stream(stream)))
+    return out
+
+
+def noalloc_scratch_bytes() -> int:
+    return int(load_library().pkv_noalloc_scratch_bytes())
 
 
 def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, k_scale: float = 1.0,

@@ -206,6 +206,127 @@ int choose_partition_tokens(int64_t max_ctx) {
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+// Checks a decode call's arguments and fills the kernel parameters (everything but
+// the workspace pointers).  *ws_bytes is the workspace the call needs (0 if none);
+// *nothing_to_do is set for a dry run or an empty batch.
+pkv_status decode_prepare(const pkv_tensor* out, const pkv_tensor* query, const pkv_tensor* key_cache,
+                          const pkv_tensor* value_cache, const pkv_tensor* block_tables,
+                          const pkv_tensor* context_lens, int32_t num_kv_heads, float scale,
+                          int32_t block_size, int32_t max_blocks_per_seq, DecodeParams* pp,
+                          size_t* ws_bytes, bool* nothing_to_do) {
+  *ws_bytes = 0;
+  *nothing_to_do = false;
+  pkv_status st;
+  if ((st = check_basic(out, "out", 3)) || (st = check_basic(query, "query", 3)) ||
+      (st = check_cache(key_cache, "key_cache")) || (st = check_cache(value_cache, "value_cache")) ||
+      (st = check_basic(block_tables, "block_tables", 2)) ||
+      (st = check_basic(context_lens, "context_lens", 1)))
+    return st;
+  if ((st = check_dtype(query, "query", PKV_F32, PKV_BF16))) return st;
+  if ((st = check_dtype(block_tables, "block_tables", PKV_I32))) return st;
+  if ((st = check_dtype(context_lens, "context_lens", PKV_I32))) return st;
+  if (out->dtype != query->dtype) return fail(PKV_ERR_INVALID_ARG, "out must have the query's dtype");
+  const int64_t S = query->shape[0], Hq = query->shape[1], D = query->shape[2];
+  if (out->shape[0] != S || out->shape[1] != Hq || out->shape[2] != D)
+    return fail(PKV_ERR_INVALID_ARG, "out shape must equal query shape [%lld, %lld, %lld]",
+                (long long)S, (long long)Hq, (long long)D);
+  if (!same_layout(key_cache, value_cache))
+    return fail(PKV_ERR_INVALID_ARG, "key_cache and value_cache must share dtype, shape and strides");
+  const int64_t NB = key_cache->shape[0];
+  if (num_kv_heads <= 0 || key_cache->shape[1] != num_kv_heads)
+    return fail(PKV_ERR_INVALID_ARG, "num_kv_heads (%d) must equal key_cache.shape[1] (%lld)", num_kv_heads,
+                (long long)key_cache->shape[1]);
+  if (Hq % num_kv_heads != 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_heads (%lld) must be a multiple of num_kv_heads (%d)", (long long)Hq,
+                num_kv_heads);
+  if (key_cache->shape[2] != block_size)
+    return fail(PKV_ERR_INVALID_ARG, "block_size (%d) must equal key_cache.shape[2] (%lld)", block_size,
+                (long long)key_cache->shape[2]);
+  if (key_cache->shape[3] != D)
+    return fail(PKV_ERR_INVALID_ARG, "key_cache head_dim (%lld) must equal query head_dim (%lld)",
+                (long long)key_cache->shape[3], (long long)D);
+  if (!supported_head_dim(D)) return fail(PKV_ERR_UNSUPPORTED, "head_dim %lld (supported: 64, 128)", (long long)D);
+  if (!supported_block_size(block_size))
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 2, 4, 8, 16, 32)", block_size);
+  if (block_tables->shape[0] != S || block_tables->shape[1] != max_blocks_per_seq)
+    return fail(PKV_ERR_INVALID_ARG, "block_tables must be [num_seqs=%lld, max_blocks_per_seq=%d]", (long long)S,
+                max_blocks_per_seq);
+  if (context_lens->shape[0] != S) return fail(PKV_ERR_INVALID_ARG, "context_lens must be [num_seqs]");
+  if (max_blocks_per_seq < 1) return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq must be >= 1");
+  const int64_t max_ctx = int64_t(max_blocks_per_seq) * block_size;
+  if (max_ctx > (int64_t(1) << 30)) return fail(PKV_ERR_UNSUPPORTED, "max context above 2^30 tokens");
+  if (S > 65535 || Hq > 65535)
+    return fail(PKV_ERR_UNSUPPORTED, "num_seqs and num_heads must be <= 65535");
+  if (!(std::isfinite(scale))) return fail(PKV_ERR_INVALID_ARG, "scale must be finite");
+  if (NB < 1) return fail(PKV_ERR_INVALID_ARG, "the cache holds no block");
+  if (g_opt_decode_kernel.load() == 2) return fail(PKV_ERR_UNSUPPORTED, "the tensor-core decode kernel is not built");
+
+  const int pt = choose_partition_tokens(max_ctx);
+  const int64_t parts = (max_ctx + pt - 1) / pt;
+  if (parts > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many context partitions; raise the partition size");
+  if (g_opt_dry_run.load() || S == 0) {
+    *nothing_to_do = true;
+    return PKV_OK;
+  }
+
+  DeviceState* s;
+  if ((st = device_state(&s))) return st;
+
+  DecodeParams& p = *pp;
+  p = DecodeParams{};
+  p.out = out->data;
+  p.out_dtype = out->dtype;
+  p.out_stride_s = out->stride[0];
+  p.out_stride_h = out->stride[1];
+  p.query = query->data;
+  p.q_dtype = query->dtype;
+  p.q_stride_s = query->stride[0];
+  p.q_stride_h = query->stride[1];
+  p.key_cache = key_cache->data;
+  p.value_cache = value_cache->data;
+  p.kv_dtype = key_cache->dtype;
+  p.cs_block = key_cache->stride[0];
+  p.cs_head = key_cache->stride[1];
+  p.block_tables = static_cast<const int32_t*>(block_tables->data);
+  p.bt_stride = block_tables->stride[0];
+  p.context_lens = static_cast<const int32_t*>(context_lens->data);
+  p.num_seqs = int(S);
+  p.num_heads = int(Hq);
+  p.num_kv_heads = num_kv_heads;
+  p.head_dim = int(D);
+  p.block_size = block_size;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_blocks = NB;
+  p.group = int(Hq / num_kv_heads);
+  const float kscale = key_cache->dtype == PKV_FP8_E4M3 ? key_cache->scale : 1.0f;
+  p.qk_scale_log2 = float(double(scale) * 1.4426950408889634 * double(kscale));
+  p.v_scale = value_cache->dtype == PKV_FP8_E4M3 ? value_cache->scale : 1.0f;
+  p.partition_tokens = pt;
+  p.max_partitions = int(parts);
+  p.err = s->err;
+  if (parts > 1) *ws_bytes = size_t(S) * size_t(Hq) * size_t(parts) * (size_t(D) + 2) * 4;
+  return PKV_OK;
+}
+
+pkv_status set_error(pkv_status st, const char* msg) { return fail(st, "%s", msg); }
+
+pkv_status finish_launch(cudaError_t launch_err, cudaStream_t stream, const char* what) {
+  DeviceState* s;
+  pkv_status st = device_state(&s);
+  if (st) return st;
+  return finish_call(s, launch_err, stream, what);
+}
+
+// Points the kernel parameters' partial-result arrays into `ws`.
+void decode_set_workspace(DecodeParams* p, void* ws) {
+  const size_t rows = size_t(p->num_seqs) * size_t(p->num_heads) * size_t(p->max_partitions);
+  p->part_o = static_cast<float*>(ws);
+  p->part_m = p->part_o + rows * size_t(p->head_dim);
+  p->part_l = p->part_m + rows;
+}
+
+
+
 }  // namespace pkv
 
 using namespace pkv;
@@ -298,97 +419,18 @@ pkv_status pkv_paged_attention_decode(const pkv_tensor* out, const pkv_tensor* q
                                       const pkv_tensor* context_lens, int32_t num_kv_heads,
                                       float scale, int32_t block_size,
                                       int32_t max_blocks_per_seq, pkv_stream stream) {
-  pkv_status st;
-  if ((st = check_basic(out, "out", 3)) || (st = check_basic(query, "query", 3)) ||
-      (st = check_cache(key_cache, "key_cache")) || (st = check_cache(value_cache, "value_cache")) ||
-      (st = check_basic(block_tables, "block_tables", 2)) ||
-      (st = check_basic(context_lens, "context_lens", 1)))
-    return st;
-  if ((st = check_dtype(query, "query", PKV_F32, PKV_BF16))) return st;
-  if ((st = check_dtype(block_tables, "block_tables", PKV_I32))) return st;
-  if ((st = check_dtype(context_lens, "context_lens", PKV_I32))) return st;
-  if (out->dtype != query->dtype) return fail(PKV_ERR_INVALID_ARG, "out must have the query's dtype");
-  const int64_t S = query->shape[0], Hq = query->shape[1], D = query->shape[2];
-  if (out->shape[0] != S || out->shape[1] != Hq || out->shape[2] != D)
-    return fail(PKV_ERR_INVALID_ARG, "out shape must equal query shape [%lld, %lld, %lld]",
-                (long long)S, (long long)Hq, (long long)D);
-  if (!same_layout(key_cache, value_cache))
-    return fail(PKV_ERR_INVALID_ARG, "key_cache and value_cache must share dtype, shape and strides");
-  const int64_t NB = key_cache->shape[0];
-  if (num_kv_heads <= 0 || key_cache->shape[1] != num_kv_heads)
-    return fail(PKV_ERR_INVALID_ARG, "num_kv_heads (%d) must equal key_cache.shape[1] (%lld)", num_kv_heads,
-                (long long)key_cache->shape[1]);
-  if (Hq % num_kv_heads != 0)
-    return fail(PKV_ERR_INVALID_ARG, "num_heads (%lld) must be a multiple of num_kv_heads (%d)", (long long)Hq,
-                num_kv_heads);
-  if (key_cache->shape[2] != block_size)
-    return fail(PKV_ERR_INVALID_ARG, "block_size (%d) must equal key_cache.shape[2] (%lld)", block_size,
-                (long long)key_cache->shape[2]);
-  if (key_cache->shape[3] != D)
-    return fail(PKV_ERR_INVALID_ARG, "key_cache head_dim (%lld) must equal query head_dim (%lld)",
-                (long long)key_cache->shape[3], (long long)D);
-  if (!supported_head_dim(D)) return fail(PKV_ERR_UNSUPPORTED, "head_dim %lld (supported: 64, 128)", (long long)D);
-  if (!supported_block_size(block_size))
-    return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 2, 4, 8, 16, 32)", block_size);
-  if (block_tables->shape[0] != S || block_tables->shape[1] != max_blocks_per_seq)
-    return fail(PKV_ERR_INVALID_ARG, "block_tables must be [num_seqs=%lld, max_blocks_per_seq=%d]", (long long)S,
-                max_blocks_per_seq);
-  if (context_lens->shape[0] != S) return fail(PKV_ERR_INVALID_ARG, "context_lens must be [num_seqs]");
-  if (max_blocks_per_seq < 1) return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq must be >= 1");
-  const int64_t max_ctx = int64_t(max_blocks_per_seq) * block_size;
-  if (max_ctx > (int64_t(1) << 30)) return fail(PKV_ERR_UNSUPPORTED, "max context above 2^30 tokens");
-  if (S > 65535 || Hq > 65535)
-    return fail(PKV_ERR_UNSUPPORTED, "num_seqs and num_heads must be <= 65535");
-  if (!(std::isfinite(scale))) return fail(PKV_ERR_INVALID_ARG, "scale must be finite");
-  if (NB < 1) return fail(PKV_ERR_INVALID_ARG, "the cache holds no block");
-  if (g_opt_decode_kernel.load() == 2) return fail(PKV_ERR_UNSUPPORTED, "the tensor-core decode kernel is not built");
-
-  const int pt = choose_partition_tokens(max_ctx);
-  const int64_t parts = (max_ctx + pt - 1) / pt;
-  if (parts > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many context partitions; raise the partition size");
-  if (g_opt_dry_run.load() || S == 0) return PKV_OK;
-
+  DecodeParams p;
+  size_t ws_bytes = 0;
+  bool nothing = false;
+  pkv_status st = decode_prepare(out, query, key_cache, value_cache, block_tables, context_lens, num_kv_heads,
+                                 scale, block_size, max_blocks_per_seq, &p, &ws_bytes, &nothing);
+  if (st || nothing) return st;
   DeviceState* s;
   if ((st = device_state(&s))) return st;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-
-  DecodeParams p{};
-  p.out = out->data;
-  p.out_dtype = out->dtype;
-  p.out_stride_s = out->stride[0];
-  p.out_stride_h = out->stride[1];
-  p.query = query->data;
-  p.q_dtype = query->dtype;
-  p.q_stride_s = query->stride[0];
-  p.q_stride_h = query->stride[1];
-  p.key_cache = key_cache->data;
-  p.value_cache = value_cache->data;
-  p.kv_dtype = key_cache->dtype;
-  p.cs_block = key_cache->stride[0];
-  p.cs_head = key_cache->stride[1];
-  p.block_tables = static_cast<const int32_t*>(block_tables->data);
-  p.bt_stride = block_tables->stride[0];
-  p.context_lens = static_cast<const int32_t*>(context_lens->data);
-  p.num_seqs = int(S);
-  p.num_heads = int(Hq);
-  p.num_kv_heads = num_kv_heads;
-  p.head_dim = int(D);
-  p.block_size = block_size;
-  p.max_blocks_per_seq = max_blocks_per_seq;
-  p.num_blocks = NB;
-  p.group = int(Hq / num_kv_heads);
-  const float kscale = key_cache->dtype == PKV_FP8_E4M3 ? key_cache->scale : 1.0f;
-  p.qk_scale_log2 = float(double(scale) * 1.4426950408889634 * double(kscale));
-  p.v_scale = value_cache->dtype == PKV_FP8_E4M3 ? value_cache->scale : 1.0f;
-  p.partition_tokens = pt;
-  p.max_partitions = int(parts);
-  p.err = s->err;
-  if (parts > 1) {
-    const size_t rows = size_t(S) * size_t(Hq) * size_t(parts);
-    if ((st = ensure_workspace(s, rows * (size_t(D) + 2) * 4, cs))) return st;
-    p.part_o = static_cast<float*>(s->ws);
-    p.part_m = p.part_o + rows * size_t(D);
-    p.part_l = p.part_m + rows;
+  if (ws_bytes) {
+    if ((st = ensure_workspace(s, ws_bytes, cs))) return st;
+    decode_set_workspace(&p, s->ws);
   }
   return finish_call(s, launch_decode(p, cs), cs, "paged_attention_decode");
 }

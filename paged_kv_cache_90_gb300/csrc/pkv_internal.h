@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/pkv.h"
+
 namespace pkv {
 
 enum DType { kF32 = 0, kBF16 = 1, kE4M3 = 2, kI32 = 3, kI64 = 4 };
@@ -84,6 +86,20 @@ int decode_heads_per_cta(int group);
 size_t decode_smem_bytes(int kv_dtype, int head_dim, int heads_per_cta, int partition_tokens,
                          int block_size);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+
+// Host-side helpers of the C ABI (pkv_api.cu).
+// Checks a decode call and fills `p` except the workspace pointers; *ws_bytes is the
+// workspace the call needs, *nothing_to_do is set for a dry run or an empty batch.
+pkv_status decode_prepare(const pkv_tensor* out, const pkv_tensor* query, const pkv_tensor* key_cache,
+                          const pkv_tensor* value_cache, const pkv_tensor* block_tables,
+                          const pkv_tensor* context_lens, int32_t num_kv_heads, float scale,
+                          int32_t block_size, int32_t max_blocks_per_seq, DecodeParams* p,
+                          size_t* ws_bytes, bool* nothing_to_do);
+void decode_set_workspace(DecodeParams* p, void* ws);
+// Maps a launch result to a status (and, with debug sync on, checks the device).
+pkv_status finish_launch(cudaError_t launch_err, cudaStream_t stream, const char* what);
+// Records `msg` as the calling thread's last error and returns `st`.
+pkv_status set_error(pkv_status st, const char* msg);
 
 // Per-dtype launchers (one translation unit each).
 cudaError_t launch_decode_f32(const DecodeParams& p, int g, cudaStream_t stream);
