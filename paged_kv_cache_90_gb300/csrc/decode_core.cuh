@@ -353,8 +353,14 @@ cudaError_t launch_decode_tpl(const DecodeParams& p, cudaStream_t stream) {
   const int table_entries = p.partition_tokens / p.block_size;
   const size_t smem = T::smem_bytes(table_entries);
   auto kern = paged_decode_kernel<KV, D, G>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-  if (e != cudaSuccess) return e;
+  static size_t smem_set[64] = {};  // per device: the limit raised so far
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || smem > smem_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) smem_set[dev] = smem;
+  }
   const dim3 grid(unsigned(p.max_partitions), unsigned(p.num_kv_heads * (p.group / G)), unsigned(p.num_seqs));
   kern<<<grid, T::kThreads, smem, stream>>>(p);
   note_launch();

@@ -73,8 +73,11 @@ cudaError_t launch_decode_reduce(const DecodeParams& p, cudaStream_t stream) {
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   if (p.num_seqs == 0) return cudaSuccess;
-  const int g = decode_heads_per_cta(p.group);
   cudaError_t e;
+  if (p.kernel == 1) {
+    return launch_decode_mma(p, stream);  // merges split rows itself
+  }
+  const int g = decode_heads_per_cta(p.group);
   switch (p.kv_dtype) {
     case kF32: e = launch_decode_f32(p, g, stream); break;
     case kBF16: e = launch_decode_bf16(p, g, stream); break;

@@ -1,0 +1,647 @@
+// decode_mma.cuh — paged decode attention on the tensor cores (mma.sync m16n8k16).
+//
+// Why tensor cores here: with grouped-query attention a KV head serves G query heads,
+// so each K tile meets a G x D query block and the score step S = Q K^T and the value
+// step O = P V are small matrix products.  As FMAs on CUDA cores they cost ~45 warp
+// instructions per token and KV head (the CUDA-core kernel is issue/latency bound at
+// about a third of HBM bandwidth); as 16x8x16 MMAs they cost a handful.  Query heads
+// are the MMA's M rows (padded to 16), tokens are N for the scores and K for the
+// values, so the score accumulators become the value step's A operand in registers.
+//
+// Work split ("stream-K"): the work is the flattened sequence of (sequence, head group,
+// 16-token stage) for all sequences, each row (sequence, head group) padded to whole
+// stages.  A persistent grid of one 8-warp block per SM gives every warp one equal
+// contiguous range of that sequence, so every warp streams the same number of bytes
+// whatever the mix of context lengths.  A row that spans several warps leaves one
+// partial (m, l, o/l) per warp, and a small second kernel merges them with the
+// log-sum-exp rule: the main kernel holds no cross-warp synchronisation at all (a
+// GPU-scope release while the SM streams hundreds of KB cost up to 25 us per warp).
+//
+// Per warp: lane 0 streams K and V tiles of its stages with TMA tensor copies (128-byte
+// swizzle, so ldmatrix reads are bank-conflict free) into a 3-deep ring of stages, one
+// mbarrier each; block-table entries are fetched a 32-stage window ahead and the
+// next row's queries one row ahead.  The softmax is online in base 2; the running reference max is
+// only moved (and the accumulators rescaled) when a row's max grows by more than 2^8,
+// so the rescale is skipped in the steady state.
+//
+// An 8-bit cache is read the same way; its codes become f16 exactly (e4m3 -> f16), the
+// scores use f16 MMAs, and each stage's values are converted to an f16 staging tile.
+#pragma once
+
+#include <cuda.h>
+#include <float.h>
+
+#include <type_traits>
+
+#include "device_common.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace mma {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kST = 16;               // tokens per pipeline stage
+constexpr float kRescaleGap = 8.f;    // log2 of the largest weight allowed before rescaling
+
+// ---- PTX wrappers --------------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+template <bool kF16>
+__device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  if constexpr (kF16) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
+__device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map, int x, int y, int z, int w,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6];"
+      ::"r"(smem_addr(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w),
+        "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool f16) {
+  if (f16) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// Two bf16 (a 32-bit word) -> the same two values as f16x2.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u), true);
+}
+
+// Two e4m3 codes (low 16 bits) -> f16x2, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
+  return (uint32_t(h.y) << 16) | uint32_t(h.x);
+}
+
+// ---- compile-time shape of one instance ----------------------------------------------
+template <typename KV, int D, int G>
+struct Cfg {
+  static constexpr bool kFp8 = std::is_same<KV, E4M3>::value;
+  static constexpr bool kF16 = kFp8;                       // f16 MMAs for an 8-bit cache
+  static constexpr int kHalves = D / 64;                   // 128-byte operand rows of 16-bit data
+  static constexpr int kRawRowBytes = D * KV::bytes;       // one token row as stored
+  static constexpr int kRawTile = kST * kRawRowBytes;      // K (or V) bytes of a stage, as stored
+  static constexpr int kStages = (kFp8 || D == 64) ? 4 : 3;
+  static constexpr int kStageBytes = 2 * kRawTile;         // K then V
+  static constexpr int kVConv = kFp8 ? kST * D * 2 : 0;    // per-warp f16 copy of a stage's V
+  static constexpr int kRows = G > 8 ? 2 : 1;              // real MMA rows per thread (g, g+8)
+  static constexpr int kNT = D / 8;                        // output n-tiles
+  static constexpr int kKS = D / 16;                       // k-steps of the score MMA
+  static_assert(kFp8 ? D == 128 : (D == 64 || D == 128), "head_dim");
+  static_assert(G == 4 || G == 8 || G == 16, "heads per item");
+  static_assert(kRawTile % 1024 == 0 || kRawRowBytes == 64, "tiles are whole swizzle atoms");
+  static constexpr size_t kWarpBytes = size_t(kStages) * kStageBytes + kVConv;
+  // from the 1024-aligned base: cum[S+1] ints | lens[S] ints | mbarriers | per-warp rings
+  __host__ __device__ static size_t bar_offset(int num_seqs) { return ((2 * size_t(num_seqs) + 1) * 4 + 7) / 8 * 8; }
+  __host__ __device__ static size_t ring_offset(int num_seqs) {
+    return (bar_offset(num_seqs) + size_t(kWarps) * kStages * 8 + 1023) / 1024 * 1024;
+  }
+  static size_t smem_bytes(int num_seqs) { return ring_offset(num_seqs) + kWarps * kWarpBytes + 1024; }
+};
+
+// Position in the flattened (sequence, head tile, stage) order.  cum[s] is the first
+// flattened token of sequence s; a sequence holds `tiles` rows of equal padded length.
+// Everything the per-stage code needs is carried, so advancing costs no division.
+struct Cursor {
+  int s, tile, kvh, sub;  // sequence, head tile, its KV head, tile within the KV head
+  int t0;                 // first token of the stage within the row
+  int rl, L;              // padded row length and context length of sequence s
+  int left;               // stages left in this warp's range, this one included
+};
+
+struct Geometry {
+  const int* cum;    // shared memory: flattened offset of each sequence (S + 1 entries)
+  const int* lens;   // shared memory: clamped context length of each sequence
+  int tiles, tiles_per_kv, max_ctx;
+};
+
+__device__ __forceinline__ int clamp_len(int L, int max_ctx) { return L < 0 ? 0 : (L > max_ctx ? max_ctx : L); }
+
+__device__ __forceinline__ void cursor_load_seq(Cursor& c, const Geometry& q) {
+  c.L = q.lens[c.s];
+  c.rl = (c.L + kST - 1) & ~(kST - 1);
+}
+
+__device__ __forceinline__ void cursor_next(Cursor& c, const Geometry& q) {
+  if (--c.left <= 0) return;
+  c.t0 += kST;
+  if (c.t0 >= c.rl) {
+    c.t0 = 0;
+    ++c.tile;
+    if (++c.sub == q.tiles_per_kv) {
+      c.sub = 0;
+      ++c.kvh;
+    }
+    if (c.tile == q.tiles) {
+      c.tile = c.sub = c.kvh = 0;
+      do { ++c.s; } while (q.cum[c.s + 1] == q.cum[c.s]);  // skip empty sequences
+      cursor_load_seq(c, q);
+    }
+  }
+}
+
+template <typename KV, int D, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                        const DecodeParams p) {
+  using C = Cfg<KV, D, G>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);  // swizzle atoms
+  const int S = p.num_seqs;
+  int* cum = reinterpret_cast<int*>(smem);
+  int* lens = cum + S + 1;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, c4 = lane & 3;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::bar_offset(S)) + warp * C::kStages;
+  unsigned char* wbase = smem + C::ring_offset(S) + size_t(warp) * C::kWarpBytes;
+  unsigned char* vconv = wbase + size_t(C::kStages) * C::kStageBytes;   // 8-bit caches only
+
+  const int max_ctx = p.max_blocks_per_seq * p.block_size;
+  const int tiles = p.num_heads / G;
+  const Geometry geo{cum, lens, tiles, p.group / G, max_ctx};
+
+  // the merge kernel behind this one may be scheduled now (it waits for our writes)
+  asm volatile("griddepcontrol.launch_dependents;");
+
+  // ---- prologue: flattened offsets of the sequences; zero rows for empty ones ------
+  {
+    __shared__ int warp_tot[kWarps];
+    const int per = (S + kThreads - 1) / kThreads;
+    const int s0 = tid * per;
+    int local = 0;
+    for (int s = s0; s < s0 + per && s < S; ++s) {
+      const int L = p.context_lens[s];
+      if (L < 0 || L > max_ctx) raise_device_error(p.err, kErrContextLen);
+      local += ((clamp_len(L, max_ctx) + kST - 1) & ~(kST - 1)) * tiles;
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    if (lane == 0) {
+      for (int s = 0; s < C::kStages; ++s) mbar_init(&bars[s], 1);
+      fence_barrier_init();
+    }
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += warp_tot[w];
+    int run = base + incl - local;
+    for (int s = s0; s < s0 + per && s < S; ++s) {
+      const int L = clamp_len(p.context_lens[s], max_ctx);
+      cum[s] = run;
+      lens[s] = L;
+      run += ((L + kST - 1) & ~(kST - 1)) * tiles;
+    }
+    if (tid == kThreads - 1) cum[S] = base + incl;
+    __syncthreads();
+    if (blockIdx.x == 0)  // the merge kernel needs the same offsets
+      for (int s = tid; s <= S; s += kThreads) p.seq_offsets[s] = cum[s];
+    // an empty context attends to nothing: its output rows are zero
+    for (int s = blockIdx.x; s < S; s += gridDim.x) {
+      if (cum[s + 1] != cum[s]) continue;
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + int64_t(s) * p.out_stride_s;
+      for (int i = tid; i < p.num_heads * D; i += kThreads)
+        out[int64_t(i / D) * p.out_stride_h + i % D] = __float2bfloat16_rn(0.f);
+    }
+  }
+  const int T = cum[S];
+  if (T == 0) return;
+  // stage ranges: q or q + 1 consecutive stages per warp
+  const int GW = gridDim.x * kWarps;
+  const int gw = blockIdx.x * kWarps + warp;
+  const int NS = T / kST;
+  const int q = NS / GW, rmd = NS % GW;
+  const int k_begin = gw * q + min(gw, rmd);
+  const int n_stages = q + (gw < rmd ? 1 : 0);
+  if (n_stages == 0) return;
+  const int r_begin = k_begin * kST;
+  // the warp whose range holds stage k
+  auto owner = [&](int k) { return k < (q + 1) * rmd ? k / (q + 1) : rmd + (k - (q + 1) * rmd) / q; };
+
+  Cursor start;
+  {
+    int lo = 0, hi = S - 1;  // last sequence whose offset is <= r_begin (skips empty ones)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cum[mid] <= r_begin) lo = mid; else hi = mid - 1;
+    }
+    start.s = lo;
+    cursor_load_seq(start, geo);
+    const int off = r_begin - cum[lo];
+    start.tile = off / start.rl;
+    start.t0 = off - start.tile * start.rl;
+    start.kvh = start.tile / geo.tiles_per_kv;
+    start.sub = start.tile - start.kvh * geo.tiles_per_kv;
+    start.left = n_stages;
+  }
+  const int bs = p.block_size;
+  const int bs_shift = 31 - __clz(bs);
+  const bool two_boxes = bs < kST;                 // block size 8: two boxes per stage
+  const int box_rows = two_boxes ? bs : kST;
+  const uint32_t box_bytes = uint32_t(box_rows) * 128u;
+  const int64_t bt_stride = p.bt_stride;
+
+  // ---- block-table entries, in windows of 32 stages: lane j holds the entries of
+  // stage (window base + j), found from the flattened position by one search; the next
+  // window is loaded while the current one is used, so no read of these registers
+  // waits on memory.
+  const int total_stages = n_stages;
+  const int mb = p.max_blocks_per_seq;
+  auto load_window = [&](int base, int& e0, int& e1) {
+    e0 = e1 = 0;
+    const int k = base + lane;
+    if (k < total_stages) {
+      const int pos = r_begin + k * kST;
+      int lo = 0, hi = S - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cum[mid] <= pos) lo = mid; else hi = mid - 1;
+      }
+      const int rl = (lens[lo] + kST - 1) & ~(kST - 1);
+      const int off = pos - cum[lo];
+      const int t0 = off - (off / rl) * rl;
+      const int b = t0 >> bs_shift;
+      const int32_t* row = p.block_tables + int64_t(lo) * bt_stride;
+      e0 = __ldg(row + b);
+      if (two_boxes && b + 1 < mb) e1 = __ldg(row + b + 1);
+    }
+  };
+  int wcur0, wcur1, wnext0, wnext1;
+  load_window(0, wcur0, wcur1);
+  load_window(32, wnext0, wnext1);
+
+  // ---- producer ------------------------------------------------------------------
+  Cursor icur = start;
+  uint32_t issued = 0, consumed = 0;
+  int islot = 0;
+  constexpr int kOpsPerBox = 2 * (C::kFp8 ? 1 : C::kHalves);     // K and V, per half
+  // this lane's copy within a stage: box, tensor (K/V), half
+  const int op_b = lane / kOpsPerBox;
+  const int op_tensor = (lane % kOpsPerBox) / (kOpsPerBox / 2);
+  const int op_h = (lane % kOpsPerBox) % (kOpsPerBox / 2);
+  const uint32_t op_off = uint32_t(op_tensor * C::kRawTile + op_h * kST * 128) + uint32_t(op_b) * box_bytes;
+  const CUtensorMap* op_map = op_tensor ? &tmv : &tmk;
+  auto issue_stage = [&]() {
+    const int wj = issued & 31;
+    const int e0 = __shfl_sync(0xffffffffu, wcur0, wj);
+    const int e1 = __shfl_sync(0xffffffffu, wcur1, wj);
+    if (wj == 31) {  // window used up: move on, fetch the one after
+      wcur0 = wnext0;
+      wcur1 = wnext1;
+      load_window(int(issued) + 33, wnext0, wnext1);
+    }
+    unsigned char* sb = wbase + size_t(islot) * C::kStageBytes;
+    const int nbox = (two_boxes && icur.t0 + 8 < icur.L) ? 2 : 1;
+    if (lane == 0) mbar_arrive_expect_tx(&bars[islot], uint32_t(kOpsPerBox * nbox) * box_bytes);
+    if (lane < kOpsPerBox * nbox) {  // one copy per lane
+      int blk = op_b == 0 ? e0 : e1;
+      if (blk < 0 || int64_t(blk) >= p.num_blocks) {
+        raise_device_error(p.err, kErrTableEntry);
+        blk = 0;
+      }
+      tma_load_4d(sb + op_off, op_map, 64 * op_h, icur.t0 & (bs - 1), icur.kvh, blk, &bars[islot]);
+    }
+    cursor_next(icur, geo);
+    ++issued;
+    if (++islot == C::kStages) islot = 0;
+  };
+
+  // queries of one row as MMA A fragments (rows g and g+8, this lane's k's)
+  auto load_q = [&](int s, int h0, uint32_t (&qa)[C::kKS][4]) {
+#pragma unroll
+    for (int kk = 0; kk < C::kKS; ++kk)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) qa[kk][r] = 0u;
+#pragma unroll
+    for (int rr = 0; rr < C::kRows; ++rr) {
+      const int row = g + 8 * rr;
+      if (row < G) {
+        const uint16_t* q = static_cast<const uint16_t*>(p.query) + int64_t(s) * p.q_stride_s +
+                            int64_t(h0 + row) * p.q_stride_h;
+#pragma unroll
+        for (int kk = 0; kk < C::kKS; ++kk) {
+          if constexpr (C::kFp8) {
+            // k index 2c, 2c+1, 2c+8, 2c+9 <-> d = 16kk + 4c + {0,1,2,3} (matches the K reads)
+            const uint2 w = __ldg(reinterpret_cast<const uint2*>(q + 16 * kk + 4 * c4));
+            qa[kk][0 + rr] = bf16x2_to_f16x2(w.x);
+            qa[kk][2 + rr] = bf16x2_to_f16x2(w.y);
+          } else {
+            qa[kk][0 + rr] = __ldg(reinterpret_cast<const uint32_t*>(q + 16 * kk + 2 * c4));
+            qa[kk][2 + rr] = __ldg(reinterpret_cast<const uint32_t*>(q + 16 * kk + 8 + 2 * c4));
+          }
+        }
+      }
+    }
+  };
+
+  // per-lane swizzled shared-memory offsets of the ldmatrix reads
+  uint32_t koff[C::kKS / 2];   // K: pair of k-steps i, n-tile 0 (n-tile 1 adds 1024)
+#pragma unroll
+  for (int i = 0; i < C::kKS / 2; ++i)
+    koff[i] = uint32_t((i / 2) * kST * 128 + (lane & 7) * 128 + ((((i % 2) * 4 + (lane >> 3)) ^ (lane & 7)) << 4));
+  constexpr int kVOff = C::kFp8 ? C::kNT / 2 : 4;
+  uint32_t voff[kVOff];        // V: pair of n-tiles (per half for an 8-bit cache)
+  {
+    const int vrow = ((lane >> 3) & 1) * 8 + (lane & 7);
+#pragma unroll
+    for (int i = 0; i < kVOff; ++i) {
+      const int h = C::kFp8 ? i / 4 : 0;
+      const int key = C::kFp8 ? ((lane & 7) ^ h) : (lane & 7);
+      voff[i] = uint32_t(h * kST * 128 + vrow * 128 + (((2 * (i % 4) + (lane >> 4)) ^ key) << 4));
+    }
+  }
+
+  // ---- consumer ----------------------------------------------------------------------
+  Cursor cc = start;
+  uint32_t qa[C::kKS][4], qa_next[C::kKS][4];
+  load_q(cc.s, cc.kvh * p.group + cc.sub * G, qa_next);
+  const float sl = p.qk_scale_log2;
+  float o[C::kNT][4];
+  float m_ref[C::kRows], l_run[C::kRows];
+  bool first = true, aborted = false;
+  int cslot = 0;
+  uint32_t cphase = 0;
+
+  while (cc.left > 0) {
+    const bool last = cc.left == 1 || cc.t0 + kST >= cc.rl;
+    if (first) {
+#pragma unroll
+      for (int kk = 0; kk < C::kKS; ++kk)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) qa[kk][r] = qa_next[kk][r];
+      if (cc.left > (cc.rl - cc.t0) / kST) {  // this warp reaches the next row: prefetch its queries
+        int s2 = cc.s, kvh2 = cc.kvh, sub2 = cc.sub + 1;
+        if (sub2 == geo.tiles_per_kv) {
+          sub2 = 0;
+          ++kvh2;
+        }
+        if (cc.tile + 1 == tiles) {
+          kvh2 = sub2 = 0;
+          do { ++s2; } while (cum[s2 + 1] == cum[s2]);
+        }
+        load_q(s2, kvh2 * p.group + sub2 * G, qa_next);
+      }
+#pragma unroll
+      for (int n = 0; n < C::kNT; ++n)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) o[n][r] = 0.f;
+#pragma unroll
+      for (int rr = 0; rr < C::kRows; ++rr) {
+        m_ref[rr] = -INFINITY;
+        l_run[rr] = 0.f;
+      }
+    }
+
+    while (icur.left > 0 && issued - consumed < uint32_t(C::kStages)) issue_stage();
+    const int slot = cslot;
+    const bool ok = mbar_wait_bounded(&bars[slot], cphase);
+    if (!__all_sync(0xffffffffu, ok)) {
+      aborted = true;
+      break;
+    }
+    unsigned char* sb = wbase + size_t(slot) * C::kStageBytes;
+    const unsigned char* kt = sb;
+    unsigned char* vt = sb + C::kRawTile;
+    const int nvalid = cc.L - cc.t0 < kST ? cc.L - cc.t0 : kST;
+
+    // values as 16-bit operand rows (8-bit cache: convert; rows past the context: zero)
+    const unsigned char* vop = vt;
+    if constexpr (C::kFp8) {
+      // 16 rows x 8 chunks of 16 codes; lanes 0-7 take one row, so reads are conflict
+      // free; the second half uses a different XOR key so the stores are too
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = i * 4 + (lane >> 3), j = lane & 7;
+        uint4 raw = make_uint4(0, 0, 0, 0);
+        if (r < nvalid) raw = *reinterpret_cast<const uint4*>(vt + r * 128 + ((j ^ (r & 7)) << 4));
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t h16[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          h16[2 * q] = e4m3x2_to_f16x2(w[q]);
+          h16[2 * q + 1] = e4m3x2_to_f16x2(w[q] >> 16);
+        }
+        const int hf = j >> 2, key = (r & 7) ^ hf;
+        unsigned char* rowp = vconv + size_t(hf) * kST * 128 + r * 128;
+        const int c0 = 2 * (j & 3);
+        *reinterpret_cast<uint4*>(rowp + ((c0 ^ key) << 4)) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
+        *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ key) << 4)) = make_uint4(h16[4], h16[5], h16[6], h16[7]);
+      }
+      __syncwarp();
+      vop = vconv;
+    } else if (nvalid < kST) {
+      const int per_half = (kST - nvalid) * 8;  // 16-byte pieces per half
+      for (int i = lane; i < per_half * C::kHalves; i += 32) {
+        const int h = i / per_half, rem = i - h * per_half;
+        *reinterpret_cast<uint4*>(vt + size_t(h) * kST * 128 + (nvalid + (rem >> 3)) * 128 + (rem & 7) * 16) =
+            make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
+
+    // scores S = Q K^T for the stage's 16 tokens (2 n-tiles of 8), two chains per tile
+    float s[2][4];
+    {
+      float s2[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) s[nt][r] = s2[nt][r] = 0.f;
+      if constexpr (C::kFp8) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int row = nt * 8 + g;
+#pragma unroll
+          for (int kk = 0; kk < C::kKS; ++kk) {
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(kt + row * 128 + ((kk ^ (row & 7)) << 4) + 4 * c4);
+            mma16816<true>(kk & 1 ? s2[nt] : s[nt], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3],
+                           e4m3x2_to_f16x2(w), e4m3x2_to_f16x2(w >> 16));
+          }
+        }
+      } else {
+        const uint32_t kbase = smem_addr(kt);
+#pragma unroll
+        for (int i = 0; i < C::kKS / 2; ++i)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kbase + koff[i] + nt * 1024, b0, b1, b2, b3);
+            mma16816<false>(s[nt], qa[2 * i][0], qa[2 * i][1], qa[2 * i][2], qa[2 * i][3], b0, b1);
+            mma16816<false>(s2[nt], qa[2 * i + 1][0], qa[2 * i + 1][1], qa[2 * i + 1][2], qa[2 * i + 1][3], b2, b3);
+          }
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) s[nt][r] += s2[nt][r];
+    }
+
+    // online softmax in base 2 against a lazily moved reference max
+    bool need = false;
+    float m_new[C::kRows];
+#pragma unroll
+    for (int rr = 0; rr < C::kRows; ++rr) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) s[nt][2 * rr + e] *= sl;
+      if (nvalid < kST) {  // the row's last, partly filled stage
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            if (nt * 8 + 2 * c4 + e >= nvalid) s[nt][2 * rr + e] = -INFINITY;
+      }
+      float mx = fmaxf(fmaxf(s[0][2 * rr], s[0][2 * rr + 1]), fmaxf(s[1][2 * rr], s[1][2 * rr + 1]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      m_new[rr] = m_ref[rr];
+      if (mx > m_ref[rr] + kRescaleGap || m_ref[rr] == -INFINITY) {
+        m_new[rr] = mx;
+        need = true;
+      }
+    }
+    if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+      for (int rr = 0; rr < C::kRows; ++rr) {
+        const float alpha = m_new[rr] == m_ref[rr] ? 1.f : fast_exp2(m_ref[rr] - m_new[rr]);
+        l_run[rr] *= alpha;
+#pragma unroll
+        for (int n = 0; n < C::kNT; ++n) {
+          o[n][2 * rr] *= alpha;
+          o[n][2 * rr + 1] *= alpha;
+        }
+        m_ref[rr] = m_new[rr];
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < C::kRows; ++rr) {
+      const float mu = m_ref[rr] == -INFINITY ? 0.f : m_ref[rr];
+      float psum = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float pv = fast_exp2(s[nt][2 * rr + e] - mu);
+          s[nt][2 * rr + e] = pv;
+          psum += pv;
+        }
+      l_run[rr] += psum;
+    }
+
+    // O += P V over the stage's 16 tokens
+    {
+      const uint32_t a0 = pack2(s[0][0], s[0][1], C::kF16);
+      const uint32_t a2 = pack2(s[1][0], s[1][1], C::kF16);
+      const uint32_t a1 = C::kRows > 1 ? pack2(s[0][2], s[0][3], C::kF16) : 0u;
+      const uint32_t a3 = C::kRows > 1 ? pack2(s[1][2], s[1][3], C::kF16) : 0u;
+      const uint32_t vbase = smem_addr(vop);
+#pragma unroll
+      for (int n = 0; n < C::kNT; n += 2) {
+        const int i = n / 2;
+        const uint32_t addr = C::kFp8 ? vbase + voff[i] : vbase + voff[i % 4] + (i / 4) * kST * 128;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(addr, b0, b1, b2, b3);
+        mma16816<C::kF16>(o[n], a0, a1, a2, a3, b0, b1);
+        mma16816<C::kF16>(o[n + 1], a0, a1, a2, a3, b2, b3);
+      }
+    }
+    __syncwarp();
+    ++consumed;  // the slot may be refilled
+    if (++cslot == C::kStages) {
+      cslot = 0;
+      cphase ^= 1u;
+    }
+
+    // ---- end of this warp's part of a row -----------------------------------------
+    if (last) {
+#pragma unroll
+      for (int rr = 0; rr < C::kRows; ++rr) {
+        l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 1);
+        l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 2);
+      }
+      const int row_id = cc.s * tiles + cc.tile;
+      const int row_start = cum[cc.s] + cc.tile * cc.rl;
+      const int wf = owner(row_start / kST), wl = owner((row_start + cc.rl) / kST - 1);
+      const int h0 = cc.kvh * p.group + cc.sub * G;
+      __nv_bfloat16* outs = static_cast<__nv_bfloat16*>(p.out) + int64_t(cc.s) * p.out_stride_s;
+      if (wf == wl) {  // the whole row was this warp's: write the output
+#pragma unroll
+        for (int rr = 0; rr < C::kRows; ++rr) {
+          const int hr = g + 8 * rr;
+          if (hr < G) {
+            const float inv = l_run[rr] > 0.f ? p.v_scale / l_run[rr] : 0.f;
+            __nv_bfloat16* out = outs + int64_t(h0 + hr) * p.out_stride_h;
+#pragma unroll
+            for (int n = 0; n < C::kNT; ++n)
+              *reinterpret_cast<__nv_bfloat162*>(out + n * 8 + 2 * c4) =
+                  __floats2bfloat162_rn(o[n][2 * rr] * inv, o[n][2 * rr + 1] * inv);
+          }
+        }
+      } else {
+        const int slot_id = gw + row_id;  // distinct for every (row, warp) pair: < GW + rows
+#pragma unroll
+        for (int rr = 0; rr < C::kRows; ++rr) {
+          const int hr = g + 8 * rr;
+          if (hr < G) {
+            const int64_t pr = int64_t(slot_id) * G + hr;
+            const float inv = l_run[rr] > 0.f ? p.v_scale / l_run[rr] : 0.f;
+            float* po = p.part_o + pr * D;
+#pragma unroll
+            for (int n = 0; n < C::kNT; ++n)
+              *reinterpret_cast<float2*>(po + n * 8 + 2 * c4) =
+                  make_float2(o[n][2 * rr] * inv, o[n][2 * rr + 1] * inv);
+            if (c4 == 0) {
+              p.part_m[pr] = m_ref[rr];
+              p.part_l[pr] = l_run[rr];
+            }
+          }
+        }
+      }
+    }
+    first = last;
+    cursor_next(cc, geo);
+  }
+
+  if (aborted) {
+    // a copy never landed: record it, let every queued copy of this warp land, stop
+    if (lane == 0) raise_device_error(p.err, kErrTimeout);
+    for (uint32_t j = consumed; j < issued; ++j)
+      (void)mbar_wait_bounded(&bars[j % C::kStages], (j / C::kStages) & 1u);
+    __syncwarp();
+  }
+}
+
+}  // namespace mma
+}  // namespace pkv

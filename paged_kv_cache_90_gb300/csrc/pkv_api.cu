@@ -9,7 +9,7 @@
 #include <mutex>
 #include <string>
 
-#include "../../include/pkv.h"
+#include "pkv.h"
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -98,6 +98,8 @@ pkv_status ensure_workspace(DeviceState* s, size_t bytes, cudaStream_t stream) {
     s->ws = nullptr;
     return cuda_fail(e, "cudaMalloc (workspace)");
   }
+  e = cudaMemset(s->ws, 0, rounded);  // deterministic contents before first use
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemset (workspace)");
   s->ws_bytes = rounded;
   return PKV_OK;
 }
@@ -259,7 +261,6 @@ pkv_status decode_prepare(const pkv_tensor* out, const pkv_tensor* query, const 
     return fail(PKV_ERR_UNSUPPORTED, "num_seqs and num_heads must be <= 65535");
   if (!(std::isfinite(scale))) return fail(PKV_ERR_INVALID_ARG, "scale must be finite");
   if (NB < 1) return fail(PKV_ERR_INVALID_ARG, "the cache holds no block");
-  if (g_opt_decode_kernel.load() == 2) return fail(PKV_ERR_UNSUPPORTED, "the tensor-core decode kernel is not built");
 
   const int pt = choose_partition_tokens(max_ctx);
   const int64_t parts = (max_ctx + pt - 1) / pt;
@@ -304,7 +305,26 @@ pkv_status decode_prepare(const pkv_tensor* out, const pkv_tensor* query, const 
   p.partition_tokens = pt;
   p.max_partitions = int(parts);
   p.err = s->err;
-  if (parts > 1) *ws_bytes = size_t(S) * size_t(Hq) * size_t(parts) * (size_t(D) + 2) * 4;
+  p.kernel = 0;
+  // tensor-core kernel when it supports the call (or when forced)
+  const int64_t want = g_opt_decode_kernel.load();
+  const bool mma_ok = want != 1 && mma_decode_supported(p);
+  if (want == 2 && !mma_ok)
+    return fail(PKV_ERR_UNSUPPORTED, "the tensor-core decode kernel does not support this call "
+                "(needs bf16 queries, a bf16 cache with head_dim 64/128 or an e4m3 cache with head_dim 128, "
+                "query heads per KV head a multiple of 4, block size 8/16/32, at most 4096 sequences)");
+  p.partial_rows = parts > 1 ? int64_t(S) * Hq * parts : 0;
+  size_t extra = 0;
+  if (mma_ok) {
+    // one partial per (row, warp) pair a row spans: fewer than warps + rows of them
+    p.kernel = 1;
+    p.heads_per_item = mma_heads_per_item(p.group);
+    p.grid = s->num_sms;
+    const int64_t rows = int64_t(S) * (Hq / p.heads_per_item);
+    p.partial_rows = (int64_t(p.grid) * kMmaWarps + rows) * p.heads_per_item;
+    extra = (size_t(S) + 1) * 4;
+  }
+  if (p.partial_rows) *ws_bytes = size_t(p.partial_rows) * (size_t(D) + 2) * 4 + extra;
   return PKV_OK;
 }
 
@@ -319,10 +339,11 @@ pkv_status finish_launch(cudaError_t launch_err, cudaStream_t stream, const char
 
 // Points the kernel parameters' partial-result arrays into `ws`.
 void decode_set_workspace(DecodeParams* p, void* ws) {
-  const size_t rows = size_t(p->num_seqs) * size_t(p->num_heads) * size_t(p->max_partitions);
+  const size_t rows = size_t(p->partial_rows);
   p->part_o = static_cast<float*>(ws);
   p->part_m = p->part_o + rows * size_t(p->head_dim);
   p->part_l = p->part_m + rows;
+  p->seq_offsets = reinterpret_cast<int*>(p->part_l + rows);
 }
 
 
@@ -377,11 +398,18 @@ int64_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t 
                                    int32_t block_size, int32_t max_blocks_per_seq) {
   if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || block_size <= 0 || max_blocks_per_seq <= 0)
     return 0;
+  // the larger of the two kernels' needs (this call cannot tell which one will run)
   const int64_t max_ctx = int64_t(max_blocks_per_seq) * block_size;
   const int pt = choose_partition_tokens(max_ctx);
   const int64_t parts = (max_ctx + pt - 1) / pt;
-  if (parts <= 1) return 0;
-  return int64_t(num_seqs) * num_heads * parts * (head_dim + 2) * 4;
+  const int64_t core = parts > 1 ? int64_t(num_seqs) * num_heads * parts * (head_dim + 2) * 4 : 0;
+  // tensor-core kernel: (warps + rows) partials of up to 16 heads, plus the sequence offsets
+  int num_sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    num_sms = 256;
+  const int64_t tc = (int64_t(num_sms) * kMmaWarps * 16 + int64_t(num_seqs) * num_heads) * (head_dim + 2) * 4 +
+                     (int64_t(num_seqs) + 1) * 4;
+  return core > tc ? core : tc;
 }
 
 pkv_status pkv_reserve_workspace(int64_t bytes) {

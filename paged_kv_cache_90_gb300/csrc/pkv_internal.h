@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/pkv.h"
+#include "pkv.h"
 
 namespace pkv {
 
@@ -74,10 +74,16 @@ struct DecodeParams {
   float v_scale;
   int partition_tokens;      // multiple of 256
   int max_partitions;        // ceil(max_blocks_per_seq * block_size / partition_tokens)
-  float* part_o;             // [S, Hq, P, D]   (P = max_partitions; unused when P == 1)
-  float* part_m;             // [S, Hq, P]
-  float* part_l;             // [S, Hq, P]
+  int64_t partial_rows;      // rows of the partial arrays (0: none)
+  float* part_o;             // [partial_rows, D]: CUDA-core kernel rows are (S, Hq, P)
+  float* part_m;             // [partial_rows]
+  float* part_l;             // [partial_rows]
   unsigned int* err;
+  // tensor-core kernel only
+  int kernel;                // 0: CUDA-core kernel, 1: tensor-core kernel
+  int heads_per_item;        // query heads per row of work (4, 8 or 16)
+  int grid;                  // persistent thread blocks
+  int* seq_offsets;          // [S + 1] flattened offsets, published for the merge kernel
 };
 
 // Heads of one KV-head group handled by one thread block (divides p.group).
@@ -100,6 +106,13 @@ void decode_set_workspace(DecodeParams* p, void* ws);
 pkv_status finish_launch(cudaError_t launch_err, cudaStream_t stream, const char* what);
 // Records `msg` as the calling thread's last error and returns `st`.
 pkv_status set_error(pkv_status st, const char* msg);
+
+// Tensor-core decode (decode_mma.cu): query heads per work item it would use for this
+// group size (0 = unsupported), whether it handles a call, and its launch.
+int mma_heads_per_item(int group);
+bool mma_decode_supported(const DecodeParams& p);
+constexpr int kMmaWarps = 8;  // warps per thread block of the tensor-core kernel
+cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream);
 
 // Per-dtype launchers (one translation unit each).
 cudaError_t launch_decode_f32(const DecodeParams& p, int g, cudaStream_t stream);

@@ -134,9 +134,13 @@ def test_options_and_workspace_size(lib):
     binding.set_option("partition_tokens", 1024)
     assert binding.get_option("partition_tokens") == 1024
     binding.set_option("partition_tokens", 0)
-    # 8 sequences of up to 2048 blocks of 16 tokens: 64 partitions of 512 tokens
-    assert binding.decode_workspace_bytes(8, 32, 128, 16, 2048) == 8 * 32 * 64 * 130 * 4
-    assert binding.decode_workspace_bytes(3, 4, 64, 16, 3) == 0
+    # an upper bound over both decode kernels: at least the CUDA-core kernel's partials
+    # (8 sequences x 32 heads x 64 partitions of 512 tokens) and the tensor-core kernel's
+    # (one per (warp, row) pair, up to 16 heads each, plus a counter per row)
+    big = binding.decode_workspace_bytes(8, 32, 128, 16, 2048)
+    assert big >= 8 * 32 * 64 * 130 * 4
+    assert big >= (8 * 32) * 130 * 4
+    assert binding.decode_workspace_bytes(0, 32, 128, 16, 2048) == 0
     with pytest.raises(KeyError):
         binding.set_option("nope", 1)
     assert lib.pkv_set_option(99, 0) == 1

@@ -31,6 +31,14 @@ def _setup():
     binding.set_option("debug_sync", 0)
 
 
+@pytest.fixture(params=["tensor", "core"])
+def kernel(request):
+    """Run the test with the tensor-core kernel forced, then with the CUDA-core one."""
+    binding.set_option("decode_kernel", 2 if request.param == "tensor" else 1)
+    yield request.param
+    binding.set_option("decode_kernel", 0)
+
+
 @pytest.fixture
 def partition_tokens():
     def set_(n):
@@ -59,26 +67,62 @@ def raw(t):
     return t.view(torch.uint8) if t.element_size() == 1 else t.view(torch.int16 if t.element_size() == 2 else torch.int32)
 
 
-def assert_decode_close(got, ref, w):
+def gather_blocks(cache, blocks):
+    if cache.dtype == torch.float8_e4m3fn:   # torch cannot index fp8 tensors on the CPU
+        return cache.view(torch.uint8)[blocks].view(torch.float8_e4m3fn)
+    return cache[blocks]
+
+
+def weighted_abs_values(w, st, kc, vc):
+    """sum_j p_j |V_j| for every output (softmax weights p), in fp64 with torch on the
+    gathered context: the scale of the error that rounding the weights to a 16-bit
+    format before the P.V product can cause (at most 2^-9 of it for bf16)."""
+    S, hq, d = st.query.shape
+    hk, bs = w.num_kv_heads, w.block_size
+    g = hq // hk
+    out = torch.zeros(S, hq, d, dtype=torch.float64)
+    for s in range(S):
+        L = int(st.context_lens[s])
+        if L == 0:
+            continue
+        n = -(-L // bs)
+        blocks = st.block_tables[s, :n].long()
+        K = gather_blocks(kc, blocks).double().permute(1, 0, 2, 3).reshape(hk, n * bs, d)[:, :L] * w.k_scale
+        V = gather_blocks(vc, blocks).double().permute(1, 0, 2, 3).reshape(hk, n * bs, d)[:, :L].abs() * w.v_scale
+        q = st.query[s].double().view(hk, g, d)
+        p = torch.softmax(w.scale * q @ K.transpose(1, 2), dim=-1)
+        out[s] = (p @ V).reshape(hq, d)
+    return out
+
+
+def assert_decode_close(got, ref, w, wabs=None):
     err = (got - ref).abs()
     assert torch.isfinite(got).all()
     worst = MAX_ABS[w.kv_dtype] if w.kv_dtype == torch.float8_e4m3fn else MAX_ABS[w.q_dtype]
     assert err.max().item() <= worst, f"max abs err {err.max().item()} > {worst}"
+    # rounding bound: the output's own rounding plus (tensor-core path) the 16-bit
+    # weights of the P.V product, with a factor-2 margin
     if w.q_dtype == torch.bfloat16:
         tight = 2.0 ** -8 * ref.abs() + 2e-5
     else:
         tight = 2e-6 * ref.abs() + 2e-6
+    if wabs is not None:
+        tight = tight + 2.0 ** -8 * wabs
     bad = (err > tight).sum().item()
     assert bad == 0, f"{bad} outputs beyond the rounding bound (max err {err.max().item():.3e})"
 
 
 def check_workload(w):
     outs, kc, vc = run_device(w)
-    routs, rkc, rvc = run_oracle(w)
-    assert torch.equal(raw(kc), raw(rkc)), "key cache differs from the oracle's"
-    assert torch.equal(raw(vc), raw(rvc)), "value cache differs from the oracle's"
-    for got, ref in zip(outs, routs):
-        assert_decode_close(got, ref, w)
+    kc0, vc0 = w.key_cache.clone(), w.value_cache.clone()
+    routs, wabs = [], []
+    for i in range(len(w.steps)):
+        routs.append(oracle.run_workload_step(w, i, kc0, vc0, THREADS))
+        wabs.append(weighted_abs_values(w, w.steps[i], kc0, vc0) if w.q_dtype == torch.bfloat16 else None)
+    assert torch.equal(raw(kc), raw(kc0)), "key cache differs from the oracle's"
+    assert torch.equal(raw(vc), raw(vc0)), "value cache differs from the oracle's"
+    for got, ref, wa in zip(outs, routs, wabs):
+        assert_decode_close(got, ref, w, wa)
     return outs, routs
 
 
@@ -100,11 +144,11 @@ def test_scalar_example_padded(layout):
 
 
 @pytest.mark.parametrize("bs", [8, 16, 32])
-def test_llama3_shaped_small(bs):
+def test_llama3_shaped_small(bs, kernel):
     check_workload(wl.llama3_8b_decode(seed=2, num_seqs=8, len_range=(128, 600), block_size=bs, poison=True))
 
 
-def test_llama3_shaped_peaked_queries():
+def test_llama3_shaped_peaked_queries(kernel):
     """Queries scaled by 8: concentrated attention, |out| of order 1."""
     w = wl.llama3_8b_decode(seed=21, num_seqs=6, len_range=(100, 900), poison=True)
     w.steps[0].query.mul_(8)
@@ -112,27 +156,27 @@ def test_llama3_shaped_peaked_queries():
     assert routs[0].abs().max() > 0.5
 
 
-def test_llama3_shaped_full():
+def test_llama3_shaped_full(kernel):
     check_workload(wl.llama3_8b_decode())
 
 
 @pytest.mark.parametrize("bs", [16, 32])
-def test_long_context_small(bs):
+def test_long_context_small(bs, kernel):
     check_workload(wl.long_context(block_size=bs, num_seqs=2, context_len=5000, poison=True))
 
 
 @pytest.mark.parametrize("bs", [16, 32])
-def test_long_context_full(bs):
+def test_long_context_full(bs, kernel):
     check_workload(wl.long_context(block_size=bs))
 
 
-def test_shared_prefix_cow_small():
+def test_shared_prefix_cow_small(kernel):
     w = wl.shared_prefix_cow(num_groups=4, prefix_blocks=8, suffix_range=(16, 120), poison=True)
     assert w.steps[0].cow_pairs.shape[0] == 12
     check_workload(w)
 
 
-def test_shared_prefix_cow_full():
+def test_shared_prefix_cow_full(kernel):
     w = wl.shared_prefix_cow()
     assert w.steps[0].cow_pairs.shape[0] == 96
     check_workload(w)
@@ -140,20 +184,20 @@ def test_shared_prefix_cow_full():
 
 @pytest.mark.parametrize("kv", ["bf16", "e4m3"])
 @pytest.mark.parametrize("bs", [8, 16, 32])
-def test_continuous_batching_small(bs, kv):
+def test_continuous_batching_small(bs, kv, kernel):
     check_workload(wl.continuous_batching(block_size=bs, kv_dtype=kv, num_seqs=24, num_steps=3,
                                           median=200, cap=2000, poison=True))
 
 
 @pytest.mark.parametrize("kv", ["bf16", "e4m3"])
 @pytest.mark.parametrize("bs", [8, 16, 32])
-def test_continuous_batching_full(bs, kv):
+def test_continuous_batching_full(bs, kv, kernel):
     check_workload(wl.continuous_batching(block_size=bs, kv_dtype=kv))
 
 
 # --- edge cases -----------------------------------------------------------------
 
-def test_partition_edges(partition_tokens):
+def test_partition_edges(partition_tokens, kernel):
     """Lengths around partition and block boundaries with 256-token partitions, so the
     log-sum-exp reduce merges 1..5 partitions."""
     partition_tokens(256)
@@ -164,6 +208,9 @@ def test_partition_edges(partition_tokens):
 @pytest.mark.parametrize("hq,hk,d,bs,kv,q", [
     (6, 2, 128, 16, "bf16", "bf16"),    # 3 query heads per KV head -> one head per block
     (16, 2, 128, 16, "bf16", "bf16"),   # 8 per KV head
+    (32, 2, 128, 16, "bf16", "bf16"),   # 16 per KV head: both MMA row halves hold heads
+    (16, 1, 64, 8, "bf16", "bf16"),     # 16 per KV head, head_dim 64
+    (32, 2, 128, 32, "e4m3", "bf16"),   # 16 per KV head, 8-bit cache
     (4, 4, 128, 16, "bf16", "bf16"),    # no grouping
     (8, 2, 64, 2, "bf16", "bf16"),      # head_dim 64, block size 2
     (8, 4, 64, 4, "e4m3", "bf16"),
@@ -216,7 +263,7 @@ def test_strided_cache_views_and_side_stream():
         pairs = torch.tensor([[int(st.block_tables[0, 0]), nb - 1]], dtype=torch.int64, device="cuda")
     s.synchronize()
     routs, rkc, rvc = run_oracle(w)
-    assert_decode_close(out.double().cpu(), routs[0], w)
+    assert_decode_close(out.double().cpu(), routs[0], w, weighted_abs_values(w, w.steps[0], rkc, rvc))
     assert torch.equal(raw(kc.cpu()), raw(rkc))
     with torch.cuda.stream(s):
         binding.copy_blocks(kc, pairs)
@@ -301,12 +348,42 @@ def test_device_checks_flag_bad_indices():
     assert binding.read_device_errors() == 0
 
 
-def test_launch_count_and_determinism():
+def test_launch_count_and_determinism(kernel):
     w = wl.llama3_8b_decode(seed=99, num_seqs=4, len_range=(600, 1500))
     dw = DeviceWorkload(w)
     n0 = binding.launch_count()
     a = dw.run_step(0, out=torch.empty_like(dw.out)).clone()
     b = dw.run_step(0, out=torch.empty_like(dw.out)).clone()   # same slot rewritten with the same data
     torch.cuda.synchronize()
-    assert binding.launch_count() - n0 == 2 * 3                 # write, decode, reduce
+    # write + decode main kernel + merge of split contexts
+    assert binding.launch_count() - n0 == 2 * 3
     assert torch.equal(a, b)
+
+
+def test_auto_selects_tensor_core_kernel_for_gqa_bf16():
+    """With no override the library runs the tensor-core kernel for GQA bf16 calls:
+    its output is bit-identical to the forced tensor-core run (the CUDA-core kernel
+    rounds differently)."""
+    w = wl.llama3_8b_decode(seed=98, num_seqs=4, len_range=(600, 1500))
+    dw = DeviceWorkload(w)
+    dw.run_step(0)
+    outs = {}
+    for k in (0, 2, 1):
+        binding.set_option("decode_kernel", k)
+        outs[k] = dw.run_step(0, out=torch.empty_like(dw.out)).clone()
+    binding.set_option("decode_kernel", 0)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[2])
+    assert not torch.equal(outs[0], outs[1])
+
+
+def test_tensor_core_kernel_rejects_what_it_cannot_run():
+    w = wl.variable_length_decode("nt", 97, [10, 20], 6, 2, 128, 16, "bf16")   # 3 heads per KV head
+    dw = DeviceWorkload(w)
+    binding.set_option("decode_kernel", 2)
+    try:
+        with pytest.raises(binding.PkvError) as ei:
+            dw.run_step(0)
+        assert ei.value.status == 2
+    finally:
+        binding.set_option("decode_kernel", 0)

@@ -32,8 +32,10 @@ def _args(dw, st):
             w.scale, w.block_size, w.max_blocks_per_seq, w.k_scale, w.v_scale)
 
 
-def test_noalloc_matches_regular_entry_point_twice_in_a_row():
+@pytest.mark.parametrize("kernel", ["tensor", "core"])
+def test_noalloc_matches_regular_entry_point_twice_in_a_row(kernel):
     binding.set_option("partition_tokens", 256)   # split contexts, so the scratch is used
+    binding.set_option("decode_kernel", 2 if kernel == "tensor" else 1)
     cases = [wl.llama3_8b_decode(seed=12, num_seqs=12, len_range=(300, 1800), poison=True),
              wl.continuous_batching(seed=15, block_size=32, kv_dtype="e4m3", num_seqs=20, num_steps=1,
                                     median=400, cap=3000, poison=True)]
@@ -54,21 +56,27 @@ def test_noalloc_matches_regular_entry_point_twice_in_a_row():
             err = (got.double() - ref.double()).abs().max().item()
             assert err <= tol, f"max abs difference {err}"
         assert binding.read_device_errors() == 0
+    binding.set_option("decode_kernel", 0)
 
 
-def test_noalloc_rejects_calls_beyond_its_scratch():
+@pytest.mark.parametrize("kernel,s,mb", [("core", 64, 4096), ("tensor", 4096, 2)])
+def test_noalloc_rejects_calls_beyond_its_scratch(kernel, s, mb):
+    """A call whose split contexts would need more than the static scratch is refused
+    with a message, and nothing is written."""
     binding.set_option("partition_tokens", 0)
-    w = wl.llama3_8b_decode(seed=13, num_seqs=4, len_range=(100, 200))
-    dw = DeviceWorkload(w)
-    st = dw.steps[0]
-    s, mb = 64, 4096                                  # 64 x 32 heads x 128 partitions: far over 16 MiB
-    bt = torch.zeros(s, mb, dtype=torch.int32, device="cuda")
-    cl = torch.ones(s, dtype=torch.int32, device="cuda")
-    q = torch.zeros(s, 32, 128, dtype=torch.bfloat16, device="cuda")
-    out = torch.zeros_like(q)
-    assert binding.decode_workspace_bytes(s, 32, 128, 16, mb) > binding.noalloc_scratch_bytes()
-    with pytest.raises(binding.PkvError) as ei:
-        binding.paged_attention_decode_noalloc(out, q, dw.key_cache, dw.value_cache, bt, cl, 8, w.scale,
-                                               16, mb)
-    assert ei.value.status == 1 and "scratch" in ei.value.message
-    assert torch.all(out == 0)
+    binding.set_option("decode_kernel", 1 if kernel == "core" else 2)
+    try:
+        w = wl.llama3_8b_decode(seed=13, num_seqs=4, len_range=(100, 200))
+        dw = DeviceWorkload(w)
+        bt = torch.zeros(s, mb, dtype=torch.int32, device="cuda")
+        cl = torch.ones(s, dtype=torch.int32, device="cuda")
+        q = torch.zeros(s, 32, 128, dtype=torch.bfloat16, device="cuda")
+        out = torch.zeros_like(q)
+        with pytest.raises(binding.PkvError) as ei:
+            binding.paged_attention_decode_noalloc(out, q, dw.key_cache, dw.value_cache, bt, cl, 8, w.scale,
+                                                   16, mb)
+        assert ei.value.status == 1 and "scratch" in ei.value.message
+        torch.cuda.synchronize()
+        assert torch.all(out == 0)
+    finally:
+        binding.set_option("decode_kernel", 0)
