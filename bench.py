@@ -264,9 +264,10 @@ def run_gpu(args, world, rank, local):
     w = make_workload(args.workload, rank)
     dw = DeviceWorkload(w, dev)
     nsteps = len(w.steps)
-    if binding.decode_workspace_bytes(w.num_seqs, w.num_heads, w.head_dim, w.block_size, w.max_blocks_per_seq):
-        binding.reserve_workspace(binding.decode_workspace_bytes(
-            w.num_seqs, w.num_heads, w.head_dim, w.block_size, w.max_blocks_per_seq))
+    ws_bytes = binding.decode_workspace_bytes(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                                              w.max_blocks_per_seq)
+    if ws_bytes:
+        binding.reserve_workspace(ws_bytes)
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_sink = torch.empty((), dtype=torch.float32, device=dev)

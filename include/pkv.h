@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 1
+#define PKV_ABI_VERSION 2
 
 typedef enum pkv_dtype {
   PKV_F32 = 0,
@@ -223,13 +223,23 @@ int32_t pkv_abi_version(void);
  * error word.  PKV_OPT_DRY_RUN: 1 = calls validate their arguments and return without
  * touching the GPU (lets the host-side checks run on a machine with no GPU).
  * PKV_OPT_DECODE_KERNEL: 0 = automatic, 1 = CUDA-core kernel, 2 = tensor-core kernel.
+ * PKV_OPT_DYNAMIC_SHARE (tensor-core kernel): the part of the work, in 1/1024 (0 to
+ * 1024), that warps claim at run time in small units instead of taking it in their even
+ * static share; it evens out SMs that stream at different rates.  -1 (the default)
+ * chooses: 256 for a 16-bit cache, 0 for an 8-bit one (whose kernel is not limited by
+ * memory, so every SM keeps the same pace).
+ * PKV_OPT_DYNAMIC_CHUNK (tensor-core kernel): fewest 16-token stages per run-time unit
+ * (1 to 64, default 4).  Neither option changes which values are computed, only which
+ * warp computes them (and so the rounding order of split rows).
  * pkv_set_option returns PKV_ERR_INVALID_ARG for an unknown option or a bad value.
  */
 typedef enum pkv_option {
   PKV_OPT_PARTITION_TOKENS = 0,
   PKV_OPT_DEBUG_SYNC = 1,
   PKV_OPT_DRY_RUN = 2,
-  PKV_OPT_DECODE_KERNEL = 3
+  PKV_OPT_DECODE_KERNEL = 3,
+  PKV_OPT_DYNAMIC_SHARE = 4,
+  PKV_OPT_DYNAMIC_CHUNK = 5
 } pkv_option;
 
 pkv_status pkv_set_option(int32_t option, int64_t value);
@@ -239,9 +249,12 @@ int64_t pkv_get_option(int32_t option);
  * (synchronises the device if it has to grow).  Call before capturing a stream. */
 pkv_status pkv_reserve_workspace(int64_t bytes);
 
-/* Workspace bytes a decode call with these sizes needs (0 if it needs none). */
-int64_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
-                                   int32_t block_size, int32_t max_blocks_per_seq);
+/* Workspace bytes a decode call with these sizes needs (0 if it needs none): the
+ * larger of the two decode kernels' needs, since the choice between them also depends
+ * on dtypes and options.  0 for non-positive sizes or num_heads not a multiple of
+ * num_kv_heads. */
+int64_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq);
 
 /* Synchronise the current device, return its error word in *flags and clear it. */
 pkv_status pkv_read_device_errors(uint32_t* flags);

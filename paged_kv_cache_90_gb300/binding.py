@@ -22,7 +22,8 @@ PKV_OK = 0
 STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA",
                 4: "PKV_ERR_DEVICE_CHECK"}
 DEVERR = {"table_entry": 0x1, "slot": 0x2, "copy_pair": 0x4, "context_len": 0x8, "timeout": 0x10}
-OPTIONS = {"partition_tokens": 0, "debug_sync": 1, "dry_run": 2, "decode_kernel": 3}
+OPTIONS = {"partition_tokens": 0, "debug_sync": 1, "dry_run": 2, "decode_kernel": 3,
+           "dynamic_share": 4, "dynamic_chunk": 5}
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float8_e4m3fn: 2, torch.int32: 3, torch.int64: 4}
 
 
@@ -73,7 +74,7 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.pkv_get_option.argtypes = [i32]
         lib.pkv_reserve_workspace.argtypes = [i64]
         lib.pkv_decode_workspace_bytes.restype = i64
-        lib.pkv_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+        lib.pkv_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.pkv_read_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
         lib.pkv_launch_count.restype = ctypes.c_uint64
         lib.pkv_launch_count.argtypes = []
@@ -181,8 +182,8 @@ def reserve_workspace(nbytes: int) -> None:
     _check(load_library().pkv_reserve_workspace(int(nbytes)))
 
 
-def decode_workspace_bytes(num_seqs, num_heads, head_dim, block_size, max_blocks_per_seq) -> int:
-    return int(load_library().pkv_decode_workspace_bytes(num_seqs, num_heads, head_dim, block_size,
+def decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq) -> int:
+    return int(load_library().pkv_decode_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
                                                          max_blocks_per_seq))
 
 

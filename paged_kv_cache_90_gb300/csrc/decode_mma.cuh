@@ -8,14 +8,19 @@
 // are the MMA's M rows (padded to 16), tokens are N for the scores and K for the
 // values, so the score accumulators become the value step's A operand in registers.
 //
-// Work split ("stream-K"): the work is the flattened sequence of (sequence, head group,
-// 16-token stage) for all sequences, each row (sequence, head group) padded to whole
-// stages.  A persistent grid of one 8-warp block per SM gives every warp one equal
-// contiguous range of that sequence, so every warp streams the same number of bytes
-// whatever the mix of context lengths.  A row that spans several warps leaves one
-// partial (m, l, o/l) per warp, and a small second kernel merges them with the
-// log-sum-exp rule: the main kernel holds no cross-warp synchronisation at all (a
-// GPU-scope release while the SM streams hundreds of KB cost up to 25 us per warp).
+// Work split ("stream-K" with a run-time tail): the work is the flattened sequence of
+// (sequence, head group, 16-token stage) for all sequences, each row (sequence, head
+// group) padded to whole stages.  A persistent grid of one 8-warp block per SM gives
+// every warp one equal contiguous range of the front of that sequence (its static
+// unit), so every warp streams the same number of bytes whatever the mix of context
+// lengths.  The back of the sequence is cut into small run-time units that warps claim
+// with one atomic counter once their static unit is issued: SMs do not stream at the
+// same rate (on this part some take ~20% longer for the same bytes), and the run-time
+// units let the faster ones take up the slack.  A row that spans several units leaves
+// one partial (m, l, o/l) per unit in a slot fixed by the unit's index, whichever warp
+// ran it, and a small second kernel merges them with the log-sum-exp rule; the main
+// kernel holds no cross-warp synchronisation beyond the claims (a GPU-scope release
+// while the SM streams hundreds of KB cost up to 25 us per warp).
 //
 // Per warp: lane 0 streams K and V tiles of its stages with TMA tensor copies (128-byte
 // swizzle, so ldmatrix reads are bank-conflict free) into a 3-deep ring of stages, one
@@ -70,13 +75,21 @@ __device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uin
   }
 }
 
+// L2 policy for data read once: its lines are the first to go, so the stream does not
+// push out what is read again soon (the partial results the merge kernel reads back).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map, int x, int y, int z, int w,
-                                            uint64_t* bar) {
+                                            uint64_t* bar, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5}], [%6];"
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
       ::"r"(smem_addr(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w),
-        "r"(smem_addr(bar))
+        "r"(smem_addr(bar)), "l"(policy)
       : "memory");
 }
 
@@ -118,10 +131,14 @@ struct Cfg {
   static_assert(G == 4 || G == 8 || G == 16, "heads per item");
   static_assert(kRawTile % 1024 == 0 || kRawRowBytes == 64, "tiles are whole swizzle atoms");
   static constexpr size_t kWarpBytes = size_t(kStages) * kStageBytes + kVConv;
-  // from the 1024-aligned base: cum[S+1] ints | lens[S] ints | mbarriers | per-warp rings
+  // from the 1024-aligned base: cum[S+1] ints | lens[S] ints | mbarriers | unit tags of
+  // the ring slots | per-warp rings
   __host__ __device__ static size_t bar_offset(int num_seqs) { return ((2 * size_t(num_seqs) + 1) * 4 + 7) / 8 * 8; }
+  __host__ __device__ static size_t tag_offset(int num_seqs) {
+    return bar_offset(num_seqs) + size_t(kWarps) * kStages * 8;
+  }
   __host__ __device__ static size_t ring_offset(int num_seqs) {
-    return (bar_offset(num_seqs) + size_t(kWarps) * kStages * 8 + 1023) / 1024 * 1024;
+    return (tag_offset(num_seqs) + size_t(kWarps) * kStages * 4 + 1023) / 1024 * 1024;
   }
   static size_t smem_bytes(int num_seqs) { return ring_offset(num_seqs) + kWarps * kWarpBytes + 1024; }
 };
@@ -140,6 +157,31 @@ struct Geometry {
   const int* cum;    // shared memory: flattened offset of each sequence (S + 1 entries)
   const int* lens;   // shared memory: clamped context length of each sequence
   int tiles, tiles_per_kv, max_ctx;
+};
+
+// Units of work over the NS flattened stages.  Units 0..GW-1 are the warps' static
+// units: stages [0, NSs) split evenly, q or q + 1 consecutive stages each (some empty
+// when NSs < GW).  Units GW..GW+ND-1 cover [NSs, NS) in runs of CH stages (the last may
+// be shorter).  `share` / 1024 of the stages go to the run-time units; CH grows beyond
+// `chunk` when that would make more than `nd_max` of them.  Unit indices grow with
+// position, so (unit + row) names a distinct partial slot for every (unit, row) pair.
+struct WorkSplit {
+  int GW, NS, NSs, q, rmd, CH, ND;
+  __device__ WorkSplit(int ns, int gw, int share, int chunk, int nd_max) : GW(gw), NS(ns) {
+    int64_t nsd = nd_max > 0 ? (int64_t(ns) * share) >> 10 : 0;
+    CH = chunk < 1 ? 1 : chunk;
+    if (nsd > int64_t(nd_max) * CH) CH = int((nsd + nd_max - 1) / nd_max);
+    NSs = ns - int(nsd);
+    q = NSs / gw;
+    rmd = NSs % gw;
+    ND = int((nsd + CH - 1) / CH);
+  }
+  __device__ int begin(int u) const { return u < GW ? u * q + min(u, rmd) : NSs + (u - GW) * CH; }
+  __device__ int len(int u) const { return u < GW ? q + (u < rmd ? 1 : 0) : min(CH, NS - begin(u)); }
+  __device__ int owner(int k) const {
+    if (k >= NSs) return GW + (k - NSs) / CH;
+    return k < (q + 1) * rmd ? k / (q + 1) : rmd + (k - (q + 1) * rmd) / q;
+  }
 };
 
 __device__ __forceinline__ int clamp_len(int L, int max_ctx) { return L < 0 ? 0 : (L > max_ctx ? max_ctx : L); }
@@ -224,8 +266,6 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
     }
     if (tid == kThreads - 1) cum[S] = base + incl;
     __syncthreads();
-    if (blockIdx.x == 0)  // the merge kernel needs the same offsets
-      for (int s = tid; s <= S; s += kThreads) p.seq_offsets[s] = cum[s];
     // an empty context attends to nothing: its output rows are zero
     for (int s = blockIdx.x; s < S; s += gridDim.x) {
       if (cum[s + 1] != cum[s]) continue;
@@ -236,34 +276,30 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
   }
   const int T = cum[S];
   if (T == 0) return;
-  // stage ranges: q or q + 1 consecutive stages per warp
   const int GW = gridDim.x * kWarps;
   const int gw = blockIdx.x * kWarps + warp;
-  const int NS = T / kST;
-  const int q = NS / GW, rmd = NS % GW;
-  const int k_begin = gw * q + min(gw, rmd);
-  const int n_stages = q + (gw < rmd ? 1 : 0);
-  if (n_stages == 0) return;
-  const int r_begin = k_begin * kST;
-  // the warp whose range holds stage k
-  auto owner = [&](int k) { return k < (q + 1) * rmd ? k / (q + 1) : rmd + (k - (q + 1) * rmd) / q; };
+  const WorkSplit split(T / kST, GW, p.dyn_share, p.dyn_chunk, p.dyn_units_max);
+  int* tags = reinterpret_cast<int*>(smem + C::tag_offset(S)) + warp * C::kStages;
 
-  Cursor start;
-  {
-    int lo = 0, hi = S - 1;  // last sequence whose offset is <= r_begin (skips empty ones)
+  // cursor at the first stage of unit u
+  auto unit_cursor = [&](int u) {
+    Cursor c;
+    const int r0 = split.begin(u) * kST;
+    int lo = 0, hi = S - 1;  // last sequence whose offset is <= r0 (skips empty ones)
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (cum[mid] <= r_begin) lo = mid; else hi = mid - 1;
+      if (cum[mid] <= r0) lo = mid; else hi = mid - 1;
     }
-    start.s = lo;
-    cursor_load_seq(start, geo);
-    const int off = r_begin - cum[lo];
-    start.tile = off / start.rl;
-    start.t0 = off - start.tile * start.rl;
-    start.kvh = start.tile / geo.tiles_per_kv;
-    start.sub = start.tile - start.kvh * geo.tiles_per_kv;
-    start.left = n_stages;
-  }
+    c.s = lo;
+    cursor_load_seq(c, geo);
+    const int off = r0 - cum[lo];
+    c.tile = off / c.rl;
+    c.t0 = off - c.tile * c.rl;
+    c.kvh = c.tile / geo.tiles_per_kv;
+    c.sub = c.tile - c.kvh * geo.tiles_per_kv;
+    c.left = split.len(u);
+    return c;
+  };
   const int bs = p.block_size;
   const int bs_shift = 31 - __clz(bs);
   const bool two_boxes = bs < kST;                 // block size 8: two boxes per stage
@@ -271,17 +307,16 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
   const uint32_t box_bytes = uint32_t(box_rows) * 128u;
   const int64_t bt_stride = p.bt_stride;
 
-  // ---- block-table entries, in windows of 32 stages: lane j holds the entries of
-  // stage (window base + j), found from the flattened position by one search; the next
-  // window is loaded while the current one is used, so no read of these registers
-  // waits on memory.
-  const int total_stages = n_stages;
+  // ---- block-table entries, in windows of 32 stages of the unit being issued: lane j
+  // holds the entries of stage (window base + j), found from the flattened position by
+  // one search; the next window is loaded while the current one is used.
   const int mb = p.max_blocks_per_seq;
+  int ubase = 0, ulen = 0;  // first stage and length of the unit being issued
   auto load_window = [&](int base, int& e0, int& e1) {
     e0 = e1 = 0;
     const int k = base + lane;
-    if (k < total_stages) {
-      const int pos = r_begin + k * kST;
+    if (k < ulen) {
+      const int pos = (ubase + k) * kST;
       int lo = 0, hi = S - 1;
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -296,14 +331,41 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
       if (two_boxes && b + 1 < mb) e1 = __ldg(row + b + 1);
     }
   };
-  int wcur0, wcur1, wnext0, wnext1;
-  load_window(0, wcur0, wcur1);
-  load_window(32, wnext0, wnext1);
+  int wcur0 = 0, wcur1 = 0, wnext0 = 0, wnext1 = 0;
 
   // ---- producer ------------------------------------------------------------------
-  Cursor icur = start;
+  // Units are issued in the order static unit, then claimed ones.  A claim is sent
+  // when the previous unit's last stage is issued and read when the next stage is
+  // due, so its round trip overlaps the ring's copies.
+  Cursor icur;
+  icur.left = 0;
+  int iu = -1, ui = 0;        // unit being issued; its stages issued so far
+  int claimed = 0;            // lane 0: result of the latest claim
+  bool no_more = false;       // a claim came back empty
   uint32_t issued = 0, consumed = 0;
   int islot = 0;
+  auto claim = [&]() {
+    if (lane == 0) claimed = atomicAdd(p.work_ctr, 1);
+  };
+  auto start_unit = [&](int u) {
+    iu = u;
+    ubase = split.begin(u);
+    ulen = split.len(u);
+    ui = 0;
+    icur = unit_cursor(u);
+    load_window(0, wcur0, wcur1);
+    load_window(32, wnext0, wnext1);
+  };
+  auto next_unit = [&]() -> bool {
+    if (no_more) return false;
+    const int c = __shfl_sync(0xffffffffu, claimed, 0);
+    if (c >= split.ND) {
+      no_more = true;
+      return false;
+    }
+    start_unit(GW + c);
+    return true;
+  };
   constexpr int kOpsPerBox = 2 * (C::kFp8 ? 1 : C::kHalves);     // K and V, per half
   // this lane's copy within a stage: box, tensor (K/V), half
   const int op_b = lane / kOpsPerBox;
@@ -311,15 +373,17 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
   const int op_h = (lane % kOpsPerBox) % (kOpsPerBox / 2);
   const uint32_t op_off = uint32_t(op_tensor * C::kRawTile + op_h * kST * 128) + uint32_t(op_b) * box_bytes;
   const CUtensorMap* op_map = op_tensor ? &tmv : &tmk;
+  const uint64_t stream_policy = l2_evict_first_policy();
   auto issue_stage = [&]() {
-    const int wj = issued & 31;
+    const int wj = ui & 31;
     const int e0 = __shfl_sync(0xffffffffu, wcur0, wj);
     const int e1 = __shfl_sync(0xffffffffu, wcur1, wj);
     if (wj == 31) {  // window used up: move on, fetch the one after
       wcur0 = wnext0;
       wcur1 = wnext1;
-      load_window(int(issued) + 33, wnext0, wnext1);
+      load_window(ui + 33, wnext0, wnext1);
     }
+    tags[islot] = iu;
     unsigned char* sb = wbase + size_t(islot) * C::kStageBytes;
     const int nbox = (two_boxes && icur.t0 + 8 < icur.L) ? 2 : 1;
     if (lane == 0) mbar_arrive_expect_tx(&bars[islot], uint32_t(kOpsPerBox * nbox) * box_bytes);
@@ -329,12 +393,15 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
         raise_device_error(p.err, kErrTableEntry);
         blk = 0;
       }
-      tma_load_4d(sb + op_off, op_map, 64 * op_h, icur.t0 & (bs - 1), icur.kvh, blk, &bars[islot]);
+      tma_load_4d(sb + op_off, op_map, 64 * op_h, icur.t0 & (bs - 1), icur.kvh, blk, &bars[islot], stream_policy);
     }
     cursor_next(icur, geo);
     ++issued;
+    ++ui;
     if (++islot == C::kStages) islot = 0;
+    if (icur.left == 0) claim();  // the unit is issued: ask for the next one
   };
+  if (split.len(gw) > 0) start_unit(gw); else claim();
 
   // queries of one row as MMA A fragments (rows g and g+8, this lane's k's)
   auto load_q = [&](int s, int h0, uint32_t (&qa)[C::kKS][4]) {
@@ -382,9 +449,10 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
   }
 
   // ---- consumer ----------------------------------------------------------------------
-  Cursor cc = start;
+  Cursor cc;
+  cc.left = 0;
+  int cu = 0;  // unit being consumed
   uint32_t qa[C::kKS][4], qa_next[C::kKS][4];
-  load_q(cc.s, cc.kvh * p.group + cc.sub * G, qa_next);
   const float sl = p.qk_scale_log2;
   float o[C::kNT][4];
   float m_ref[C::kRows], l_run[C::kRows];
@@ -392,14 +460,29 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
   int cslot = 0;
   uint32_t cphase = 0;
 
-  while (cc.left > 0) {
+  while (true) {
+    while (issued - consumed < uint32_t(C::kStages)) {  // keep the ring full
+      if (icur.left == 0 && !next_unit()) break;
+      issue_stage();
+    }
+    if (consumed == issued) break;  // nothing in flight and nothing left to claim
+    bool unit_start = false;
+    if (cc.left == 0) {  // the stage in this slot opens the next unit
+      cu = tags[cslot];
+      cc = unit_cursor(cu);
+      first = unit_start = true;
+    }
     const bool last = cc.left == 1 || cc.t0 + kST >= cc.rl;
     if (first) {
+      if (unit_start) {
+        load_q(cc.s, cc.kvh * p.group + cc.sub * G, qa);
+      } else {
 #pragma unroll
-      for (int kk = 0; kk < C::kKS; ++kk)
+        for (int kk = 0; kk < C::kKS; ++kk)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) qa[kk][r] = qa_next[kk][r];
-      if (cc.left > (cc.rl - cc.t0) / kST) {  // this warp reaches the next row: prefetch its queries
+          for (int r = 0; r < 4; ++r) qa[kk][r] = qa_next[kk][r];
+      }
+      if (cc.left > (cc.rl - cc.t0) / kST) {  // this unit reaches the next row: prefetch its queries
         int s2 = cc.s, kvh2 = cc.kvh, sub2 = cc.sub + 1;
         if (sub2 == geo.tiles_per_kv) {
           sub2 = 0;
@@ -422,7 +505,6 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
       }
     }
 
-    while (icur.left > 0 && issued - consumed < uint32_t(C::kStages)) issue_stage();
     const int slot = cslot;
     const bool ok = mbar_wait_bounded(&bars[slot], cphase);
     if (!__all_sync(0xffffffffu, ok)) {
@@ -593,10 +675,10 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
       }
       const int row_id = cc.s * tiles + cc.tile;
       const int row_start = cum[cc.s] + cc.tile * cc.rl;
-      const int wf = owner(row_start / kST), wl = owner((row_start + cc.rl) / kST - 1);
+      const int wf = split.owner(row_start / kST), wl = split.owner((row_start + cc.rl) / kST - 1);
       const int h0 = cc.kvh * p.group + cc.sub * G;
       __nv_bfloat16* outs = static_cast<__nv_bfloat16*>(p.out) + int64_t(cc.s) * p.out_stride_s;
-      if (wf == wl) {  // the whole row was this warp's: write the output
+      if (wf == wl) {  // the whole row is in this unit: write the output
 #pragma unroll
         for (int rr = 0; rr < C::kRows; ++rr) {
           const int hr = g + 8 * rr;
@@ -610,7 +692,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
           }
         }
       } else {
-        const int slot_id = gw + row_id;  // distinct for every (row, warp) pair: < GW + rows
+        const int slot_id = cu + row_id;  // distinct for every (row, unit) pair: < units + rows
 #pragma unroll
         for (int rr = 0; rr < C::kRows; ++rr) {
           const int hr = g + 8 * rr;
@@ -640,6 +722,16 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
     for (uint32_t j = consumed; j < issued; ++j)
       (void)mbar_wait_bounded(&bars[j % C::kStages], (j / C::kStages) & 1u);
     __syncwarp();
+  }
+  // The last warp to finish zeroes the counters for the next launch: every warp's
+  // claims precede its finish count, so none can claim after the reset.
+  if (lane == 0) {
+    __threadfence();
+    if (atomicAdd(p.work_ctr + 1, 1) == GW - 1) {
+      __threadfence();
+      atomicExch(p.work_ctr, 0);
+      atomicExch(p.work_ctr + 1, 0);
+    }
   }
 }
 

@@ -24,6 +24,8 @@ std::atomic<int64_t> g_opt_partition_tokens{0};
 std::atomic<int64_t> g_opt_debug_sync{0};
 std::atomic<int64_t> g_opt_dry_run{0};
 std::atomic<int64_t> g_opt_decode_kernel{0};
+std::atomic<int64_t> g_opt_dynamic_share{-1};
+std::atomic<int64_t> g_opt_dynamic_chunk{4};
 
 thread_local std::string t_last_error;
 
@@ -306,6 +308,7 @@ pkv_status decode_prepare(const pkv_tensor* out, const pkv_tensor* query, const 
   p.max_partitions = int(parts);
   p.err = s->err;
   p.kernel = 0;
+  p.grid = s->num_sms;
   // tensor-core kernel when it supports the call (or when forced)
   const int64_t want = g_opt_decode_kernel.load();
   const bool mma_ok = want != 1 && mma_decode_supported(p);
@@ -314,17 +317,21 @@ pkv_status decode_prepare(const pkv_tensor* out, const pkv_tensor* query, const 
                 "(needs bf16 queries, a bf16 cache with head_dim 64/128 or an e4m3 cache with head_dim 128, "
                 "query heads per KV head a multiple of 4, block size 8/16/32, at most 4096 sequences)");
   p.partial_rows = parts > 1 ? int64_t(S) * Hq * parts : 0;
-  size_t extra = 0;
   if (mma_ok) {
-    // one partial per (row, warp) pair a row spans: fewer than warps + rows of them
+    // one partial per (row, unit of work) pair a row spans: fewer than units + rows of
+    // them, with one static unit per warp and at most two run-time units per warp
     p.kernel = 1;
     p.heads_per_item = mma_heads_per_item(p.group);
-    p.grid = s->num_sms;
+    // run-time units even out SMs streaming at different rates; an 8-bit cache makes the
+    // kernel issue-bound, every SM runs at the same pace and the units only add parts
+    const int64_t share = g_opt_dynamic_share.load();
+    p.dyn_share = share >= 0 ? int(share) : (p.kv_dtype == kE4M3 ? 0 : 256);
+    p.dyn_chunk = int(g_opt_dynamic_chunk.load());
+    p.dyn_units_max = 2 * p.grid * kMmaWarps;
     const int64_t rows = int64_t(S) * (Hq / p.heads_per_item);
-    p.partial_rows = (int64_t(p.grid) * kMmaWarps + rows) * p.heads_per_item;
-    extra = (size_t(S) + 1) * 4;
+    p.partial_rows = (int64_t(p.grid) * kMmaWarps + p.dyn_units_max + rows) * p.heads_per_item;
   }
-  if (p.partial_rows) *ws_bytes = size_t(p.partial_rows) * (size_t(D) + 2) * 4 + extra;
+  if (p.partial_rows) *ws_bytes = kWorkspaceHeader + size_t(p.partial_rows) * (size_t(D) + 2) * 4;
   return PKV_OK;
 }
 
@@ -337,13 +344,13 @@ pkv_status finish_launch(cudaError_t launch_err, cudaStream_t stream, const char
   return finish_call(s, launch_err, stream, what);
 }
 
-// Points the kernel parameters' partial-result arrays into `ws`.
+// Points the kernel parameters' counters and partial-result arrays into `ws`.
 void decode_set_workspace(DecodeParams* p, void* ws) {
   const size_t rows = size_t(p->partial_rows);
-  p->part_o = static_cast<float*>(ws);
+  p->work_ctr = static_cast<int*>(ws);
+  p->part_o = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + kWorkspaceHeader);
   p->part_m = p->part_o + rows * size_t(p->head_dim);
   p->part_l = p->part_m + rows;
-  p->seq_offsets = reinterpret_cast<int*>(p->part_l + rows);
 }
 
 
@@ -379,6 +386,14 @@ pkv_status pkv_set_option(int32_t option, int64_t value) {
       if (value < 0 || value > 2) return fail(PKV_ERR_INVALID_ARG, "decode kernel is 0, 1 or 2");
       g_opt_decode_kernel = value;
       return PKV_OK;
+    case PKV_OPT_DYNAMIC_SHARE:
+      if (value < -1 || value > 1024) return fail(PKV_ERR_INVALID_ARG, "dynamic share is -1 (automatic) or 0 to 1024");
+      g_opt_dynamic_share = value;
+      return PKV_OK;
+    case PKV_OPT_DYNAMIC_CHUNK:
+      if (value < 1 || value > 64) return fail(PKV_ERR_INVALID_ARG, "dynamic chunk is 1 to 64 stages");
+      g_opt_dynamic_chunk = value;
+      return PKV_OK;
     default:
       return fail(PKV_ERR_INVALID_ARG, "unknown option %d", option);
   }
@@ -390,25 +405,35 @@ int64_t pkv_get_option(int32_t option) {
     case PKV_OPT_DEBUG_SYNC: return g_opt_debug_sync.load();
     case PKV_OPT_DRY_RUN: return g_opt_dry_run.load();
     case PKV_OPT_DECODE_KERNEL: return g_opt_decode_kernel.load();
+    case PKV_OPT_DYNAMIC_SHARE: return g_opt_dynamic_share.load();
+    case PKV_OPT_DYNAMIC_CHUNK: return g_opt_dynamic_chunk.load();
     default: return -1;
   }
 }
 
-int64_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
-                                   int32_t block_size, int32_t max_blocks_per_seq) {
-  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || block_size <= 0 || max_blocks_per_seq <= 0)
+int64_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq) {
+  if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      max_blocks_per_seq <= 0 || num_heads % num_kv_heads)
     return 0;
   // the larger of the two kernels' needs (this call cannot tell which one will run)
   const int64_t max_ctx = int64_t(max_blocks_per_seq) * block_size;
   const int pt = choose_partition_tokens(max_ctx);
   const int64_t parts = (max_ctx + pt - 1) / pt;
-  const int64_t core = parts > 1 ? int64_t(num_seqs) * num_heads * parts * (head_dim + 2) * 4 : 0;
-  // tensor-core kernel: (warps + rows) partials of up to 16 heads, plus the sequence offsets
-  int num_sms = 0, dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    num_sms = 256;
-  const int64_t tc = (int64_t(num_sms) * kMmaWarps * 16 + int64_t(num_seqs) * num_heads) * (head_dim + 2) * 4 +
-                     (int64_t(num_seqs) + 1) * 4;
+  const int64_t core =
+      parts > 1 ? int64_t(kWorkspaceHeader) + int64_t(num_seqs) * num_heads * parts * (head_dim + 2) * 4 : 0;
+  // tensor-core kernel: partials for (warps + run-time units + rows) slots of G heads
+  // (see decode_prepare)
+  const int G = mma_heads_per_item(num_heads / num_kv_heads);
+  int64_t tc = 0;
+  if (G > 0) {
+    int num_sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      num_sms = 256;
+    const int64_t units = 3 * int64_t(num_sms) * kMmaWarps;
+    tc = int64_t(kWorkspaceHeader) + (units * G + int64_t(num_seqs) * num_heads) * (head_dim + 2) * 4;
+  }
   return core > tc ? core : tc;
 }
 

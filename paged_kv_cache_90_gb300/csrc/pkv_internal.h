@@ -83,8 +83,15 @@ struct DecodeParams {
   int kernel;                // 0: CUDA-core kernel, 1: tensor-core kernel
   int heads_per_item;        // query heads per row of work (4, 8 or 16)
   int grid;                  // persistent thread blocks
-  int* seq_offsets;          // [S + 1] flattened offsets, published for the merge kernel
+  int dyn_share;             // stages handed out at run time, in 1/1024 of all stages
+  int dyn_chunk;             // fewest stages per run-time unit
+  int dyn_units_max;         // most run-time units (bounds the partial slots)
+  int* work_ctr;             // [2]: next run-time unit, warps finished; zero between launches
 };
+
+// The decode workspace starts with this many bytes of counters (zero while no launch
+// runs); the partial arrays follow.
+constexpr size_t kWorkspaceHeader = 256;
 
 // Heads of one KV-head group handled by one thread block (divides p.group).
 int decode_heads_per_cta(int group);

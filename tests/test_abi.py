@@ -39,7 +39,7 @@ def test_exports_every_declared_function(lib):
     assert {"pkv_paged_attention_decode", "pkv_reshape_and_cache", "pkv_copy_blocks"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} is declared in pkv.h but not exported"
-    assert binding.abi_version() == 1
+    assert binding.abi_version() == 2
 
 
 def _decode_args(S=3, Hq=8, Hk=2, D=128, bs=16, NB=20, MB=4, dtype=torch.bfloat16, kv=torch.bfloat16):
@@ -136,11 +136,24 @@ def test_options_and_workspace_size(lib):
     binding.set_option("partition_tokens", 0)
     # an upper bound over both decode kernels: at least the CUDA-core kernel's partials
     # (8 sequences x 32 heads x 64 partitions of 512 tokens) and the tensor-core kernel's
-    # (one per (warp, row) pair, up to 16 heads each, plus a counter per row)
-    big = binding.decode_workspace_bytes(8, 32, 128, 16, 2048)
+    # (one slot of 4 heads per warp, per run-time unit and per row)
+    big = binding.decode_workspace_bytes(8, 32, 8, 128, 16, 2048)
     assert big >= 8 * 32 * 64 * 130 * 4
     assert big >= (8 * 32) * 130 * 4
-    assert binding.decode_workspace_bytes(0, 32, 128, 16, 2048) == 0
+    # a short context: no CUDA-core partials, only the tensor-core kernel's slots
+    small = binding.decode_workspace_bytes(8, 32, 8, 128, 16, 16)
+    assert small >= (8 * 32) * 130 * 4 and small <= big
+    assert binding.decode_workspace_bytes(0, 32, 8, 128, 16, 2048) == 0
+    assert binding.decode_workspace_bytes(8, 32, 5, 128, 16, 2048) == 0
+    assert binding.decode_workspace_bytes(8, 6, 2, 128, 16, 16) == 0     # 3 heads per KV head: no tensor path
+    for name, bad in (("dynamic_share", 1025), ("dynamic_share", -2), ("dynamic_chunk", 0), ("dynamic_chunk", 65)):
+        with pytest.raises(binding.PkvError):
+            binding.set_option(name, bad)
+    assert binding.get_option("dynamic_share") == -1     # automatic
+    binding.set_option("dynamic_share", 512)
+    assert binding.get_option("dynamic_share") == 512
+    binding.set_option("dynamic_share", -1)
+    assert binding.get_option("dynamic_chunk") == 4
     with pytest.raises(KeyError):
         binding.set_option("nope", 1)
     assert lib.pkv_set_option(99, 0) == 1

@@ -360,6 +360,42 @@ def test_launch_count_and_determinism(kernel):
     assert torch.equal(a, b)
 
 
+@pytest.fixture
+def work_split():
+    def set_(share, chunk):
+        binding.set_option("dynamic_share", share)
+        binding.set_option("dynamic_chunk", chunk)
+    binding.set_option("decode_kernel", 2)
+    yield set_
+    binding.set_option("decode_kernel", 0)
+    binding.set_option("dynamic_share", -1)
+    binding.set_option("dynamic_chunk", 4)
+
+
+@pytest.mark.parametrize("share,chunk", [(0, 4), (256, 4), (384, 4), (512, 3), (1024, 1)])
+def test_tensor_kernel_work_split_settings(share, chunk, work_split):
+    """How much of the work warps claim at run time changes which warp runs which
+    stages, not the values: every setting matches the oracle, and launches in a row
+    (the kernel zeroes its claim counter for the next one) give identical bits."""
+    work_split(share, chunk)
+    check_workload(wl.llama3_8b_decode(seed=31, num_seqs=8, len_range=(1, 900), poison=True))
+    check_workload(wl.continuous_batching(block_size=8, kv_dtype="e4m3", num_seqs=24, num_steps=2,
+                                          median=200, cap=2000, poison=True))
+    w = wl.llama3_8b_decode(seed=32, num_seqs=64, len_range=(100, 2048))
+    dw = DeviceWorkload(w)
+    runs = [dw.run_step(0, out=torch.empty_like(dw.out)).clone() for _ in range(3)]
+    torch.cuda.synchronize()
+    assert binding.read_device_errors() == 0
+    assert torch.equal(runs[0], runs[1]) and torch.equal(runs[0], runs[2])
+
+
+def test_tensor_kernel_all_claimed_full_size(work_split):
+    """Every stage claimed at run time, more units than the cap allows at one stage
+    each (the kernel widens them): the full Llama-3-8B-shaped batch."""
+    work_split(1024, 1)
+    check_workload(wl.llama3_8b_decode())
+
+
 def test_auto_selects_tensor_core_kernel_for_gqa_bf16():
     """With no override the library runs the tensor-core kernel for GQA bf16 calls:
     its output is bit-identical to the forced tensor-core run (the CUDA-core kernel

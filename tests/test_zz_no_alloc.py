@@ -43,7 +43,7 @@ def test_noalloc_matches_regular_entry_point_twice_in_a_row(kernel):
         dw = DeviceWorkload(w)
         dw.run_step(0)                                # write the step's new tokens
         st = dw.steps[0]
-        need = binding.decode_workspace_bytes(w.num_seqs, w.num_heads, w.head_dim, w.block_size,
+        need = binding.decode_workspace_bytes(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size,
                                               w.max_blocks_per_seq)
         assert 0 < need <= binding.noalloc_scratch_bytes()
         ref = torch.empty_like(dw.out)
