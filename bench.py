@@ -13,6 +13,9 @@ queries, the outputs, the block-table entries and lengths, the new tokens read a
 written, and the copied blocks.  Timing: CUDA events on the launching stream around
 each step, the L2 flushed between steps outside the events (a 256 MiB write, then a
 256 MiB read so that the write's dirty lines are written back before the step starts).
+A step issues the cache write and the decode as one pkv_decode_step call.  The roofline
+entry times the decode kernels alone (main kernel + merge of split rows) in a second
+loop of decode calls on the same resident caches, bracketed the same way.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 """
@@ -300,35 +303,38 @@ def run_gpu(args, world, rank, local):
     t0 = time.time()
     for k in range(args.steps):
         flush_l2()
-        st = dw.steps[k % nsteps]
-        a, b, c = ev[k]
+        a, _, c = ev[k]
         a.record(stream)
-        if st.cow_pairs.numel():
-            binding.copy_blocks(dw.key_cache, st.cow_pairs)
-            binding.copy_blocks(dw.value_cache, st.cow_pairs)
-        if st.slot_mapping.numel():
-            binding.reshape_and_cache(st.new_key, st.new_value, dw.key_cache, dw.value_cache, st.slot_mapping,
-                                      w.k_scale, w.v_scale)
+        dw.run_step(k % nsteps)        # CoW copies, then the cache write and decode in one call
+        c.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    launches = binding.launch_count() - n0
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    total_ms = sum(step_ms)
+    # the decode kernels alone (main + merge), for the roofline: the same calls on the
+    # same resident caches, each bracketed by events on the launching stream
+    dec_steps = min(args.steps, 500)
+    for k in range(dec_steps):
+        flush_l2()
+        st = dw.steps[k % nsteps]
+        _, b, c = ev[k]
         b.record(stream)
         binding.paged_attention_decode(dw.out, st.query, dw.key_cache, dw.value_cache, st.block_tables,
                                        st.context_lens, w.num_kv_heads, w.scale, w.block_size,
                                        w.max_blocks_per_seq, w.k_scale, w.v_scale)
         c.record(stream)
     torch.cuda.synchronize(dev)
-    t1 = time.time()
-    launches = binding.launch_count() - n0
     barrier()
     time.sleep(0.2)
     clocks.stop()
-    step_ms = [a.elapsed_time(c) for a, _, c in ev]
-    dec_ms = [b.elapsed_time(c) for _, b, c in ev]
-    total_ms = sum(step_ms)
+    dec_ms = [b.elapsed_time(c) for _, b, c in ev[:dec_steps]]
     flags = binding.read_device_errors()
     if flags:
         raise SystemExit(f"device error word 0x{flags:x} during the bench")
 
     bytes_steps = [step_bytes(w, w.steps[k % nsteps]) for k in range(args.steps)]
-    dec_bytes = [decode_bytes(w, w.steps[k % nsteps]) for k in range(args.steps)]
+    dec_bytes = [decode_bytes(w, w.steps[k % nsteps]) for k in range(dec_steps)]
     my_time = torch.tensor([total_ms], dtype=torch.float64)
     my_bytes = torch.tensor([float(sum(bytes_steps))], dtype=torch.float64)
     if world > 1:

@@ -8,7 +8,9 @@
  *   pkv_copy_blocks              copy whole physical blocks (copy-on-write of blocks
  *                                shared between sequences);
  *   pkv_paged_attention_decode   single-query attention of every sequence over its
- *                                cached tokens, read through its block table.
+ *                                cached tokens, read through its block table;
+ *   pkv_decode_step              the cache write and the decode of one step in one
+ *                                call (the decode's preparation overlaps the write).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -157,6 +159,35 @@ pkv_status pkv_reshape_and_cache(const pkv_tensor* key, const pkv_tensor* value,
                                  const pkv_tensor* slot_mapping, pkv_stream stream);
 
 /*
+ * pkv_decode_step — append this step's tokens to the cache, then decode: the same
+ * results as pkv_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping)
+ * followed by pkv_paged_attention_decode(out, query, key_cache, value_cache,
+ * block_tables, context_lens, ...), on `stream`.
+ *
+ * Defined by: vasteelab.pages.dev "PagedAttentionとは？", section
+ * "PagedAttentionはAttention kernelとmemory managerの組み合わせである" (the new token's
+ * K/V go into their physical slot and the attention kernel then reads the sequence's
+ * blocks through the table), and the decode and write definitions above.
+ *
+ * Why a joint call: the decode kernel's preparation (sequence offsets, block-table and
+ * query loads) reads nothing the write produces, so the library launches it as a
+ * programmatic dependent of the write and it waits for the write only before its first
+ * read of the cache; the write itself is an ordinary launch, ordered after everything
+ * queued on the stream before the call.
+ *
+ * Arguments are those of the two calls (key_cache / value_cache shared).  Every
+ * argument of both is checked before anything is queued; an error returns without
+ * queueing either.  num_tokens may be 0 (decode only) and num_seqs may be 0 (write
+ * only).
+ */
+pkv_status pkv_decode_step(const pkv_tensor* out, const pkv_tensor* query, const pkv_tensor* key,
+                           const pkv_tensor* value, const pkv_tensor* slot_mapping,
+                           const pkv_tensor* key_cache, const pkv_tensor* value_cache,
+                           const pkv_tensor* block_tables, const pkv_tensor* context_lens,
+                           int32_t num_kv_heads, float scale, int32_t block_size,
+                           int32_t max_blocks_per_seq, pkv_stream stream);
+
+/*
  * pkv_copy_blocks — copy whole physical blocks of one cache tensor.
  *
  * Defined by: vasteelab.pages.dev "PagedAttentionとは？", section
@@ -190,9 +221,9 @@ pkv_status pkv_copy_blocks(const pkv_tensor* cache, const pkv_tensor* src_dst_pa
  * Arguments, results and errors are those of pkv_paged_attention_decode, except that
  * the partial results of split contexts go to a fixed scratch array compiled into the
  * library (pkv_noalloc_scratch_bytes(), 16 MiB), which every GPU that loads the library
- * holds until the process exits.  A call that would need more scratch than that
- * (num_seqs * num_heads * partitions * (head_dim + 2) * 4 bytes) returns
- * PKV_ERR_INVALID_ARG with a message and queues nothing.
+ * holds until the process exits.  A call that would need more scratch than that (at
+ * most pkv_decode_workspace_bytes() of its sizes) returns PKV_ERR_INVALID_ARG with a
+ * message and queues nothing.
  * The first call on each device looks up the array's device address (and may load the
  * library's device code there): make it before any stream capture.  All calls on a
  * device share the array, so calls whose GPU work overlaps (unordered streams) race on

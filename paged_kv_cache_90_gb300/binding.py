@@ -60,10 +60,11 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.pkv_reshape_and_cache.argtypes = [d, d, d, d, d, vp]
         lib.pkv_copy_blocks.argtypes = [d, d, vp]
         lib.pkv_paged_attention_decode_noalloc.argtypes = [d, d, d, d, d, d, i32, f32, i32, i32, vp]
+        lib.pkv_decode_step.argtypes = [d, d, d, d, d, d, d, d, d, i32, f32, i32, i32, vp]
         lib.pkv_noalloc_scratch_bytes.restype = i64
         lib.pkv_noalloc_scratch_bytes.argtypes = []
         for fn in ("pkv_paged_attention_decode", "pkv_paged_attention_decode_noalloc",
-                   "pkv_reshape_and_cache", "pkv_copy_blocks",
+                   "pkv_reshape_and_cache", "pkv_decode_step", "pkv_copy_blocks",
                    "pkv_set_option", "pkv_reserve_workspace", "pkv_read_device_errors"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.pkv_last_error.restype = ctypes.c_char_p
@@ -126,6 +127,21 @@ def paged_attention_decode(out, query, key_cache, value_cache, block_tables, con
     _check(lib.pkv_paged_attention_decode(*[ctypes.byref(x) for x in descs], int(num_kv_heads),
                                           float(scale), int(block_size), int(max_blocks_per_seq),
                                           _stream(stream)))
+    return out
+
+
+def decode_step(out, query, key, value, slot_mapping, key_cache, value_cache, block_tables, context_lens,
+                num_kv_heads: int, scale: float, block_size: int, max_blocks_per_seq: int,
+                k_scale: float = 1.0, v_scale: float = 1.0, stream=None) -> torch.Tensor:
+    """Append the step's new tokens (``key``/``value`` at ``slot_mapping``) to the cache
+    and decode into ``out`` (returned): the results of reshape_and_cache followed by
+    paged_attention_decode, with the decode's preparation overlapping the write."""
+    lib = load_library()
+    descs = [describe(out), describe(query), describe(key), describe(value), describe(slot_mapping),
+             describe(key_cache, k_scale), describe(value_cache, v_scale), describe(block_tables),
+             describe(context_lens)]
+    _check(lib.pkv_decode_step(*[ctypes.byref(x) for x in descs], int(num_kv_heads), float(scale),
+                               int(block_size), int(max_blocks_per_seq), _stream(stream)))
     return out
 
 

@@ -18,6 +18,9 @@ constexpr int kCopyThreads = 256;
 // Same dtype in and out: bit copy of each token's Hk x D row, 16 bytes at a time.
 __global__ void __launch_bounds__(kWriteThreads) cache_write_copy_kernel(const CacheWriteParams p,
                                                                          int elt_bytes) {
+  // a decode launched behind this write as a programmatic dependent may start its
+  // preparation now (it waits for this grid before it reads the cache)
+  asm volatile("griddepcontrol.launch_dependents;");
   const int64_t t = blockIdx.x;
   const int64_t slot = p.slot_mapping[t];
   if (slot < 0) return;  // padding token: nothing to write
@@ -71,6 +74,7 @@ __device__ __forceinline__ void load8<F32>(const unsigned char* p, float* f) {
 // bf16 / f32 source -> e4m3 cache, 8 elements per step.
 template <typename Src>
 __global__ void __launch_bounds__(kWriteThreads) cache_write_e4m3_kernel(const CacheWriteParams p) {
+  asm volatile("griddepcontrol.launch_dependents;");  // as in the copying write
   const int64_t t = blockIdx.x;
   const int64_t slot = p.slot_mapping[t];
   if (slot < 0) return;

@@ -102,9 +102,19 @@ cudaError_t launch_tpl(const DecodeParams& p, cudaStream_t stream) {
     if (dev >= 0 && dev < kMapCacheDevices) smem_set[dev] = smem;
   }
   static_assert(mma::kWarps == kMmaWarps, "warps per block");
-  kern<<<p.grid, mma::kThreads, smem, stream>>>(mk, mv, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(p.grid));
+  cfg.blockDim = dim3(unsigned(mma::kThreads));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.overlap_prologue ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, mk, mv, p);
   note_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // Merge of rows split across units of work.  A persistent grid; block b owns rows b,

@@ -460,6 +460,11 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
   int cslot = 0;
   uint32_t cphase = 0;
 
+  // Everything above reads only the call's inputs.  Launched as a programmatic
+  // dependent of the cache write that appends this step's tokens, wait for that write
+  // here, before the first copy out of the cache (a no-op in an ordinary launch).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
   while (true) {
     while (issued - consumed < uint32_t(C::kStages)) {  // keep the ring full
       if (icur.left == 0 && !next_unit()) break;

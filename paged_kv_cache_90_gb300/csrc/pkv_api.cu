@@ -335,6 +335,70 @@ pkv_status decode_prepare(const pkv_tensor* out, const pkv_tensor* query, const 
   return PKV_OK;
 }
 
+// Checks a cache-write call's arguments and fills the kernel parameters; *nothing_to_do
+// is set for a dry run or no tokens.
+pkv_status reshape_prepare(const pkv_tensor* key, const pkv_tensor* value, const pkv_tensor* key_cache,
+                           const pkv_tensor* value_cache, const pkv_tensor* slot_mapping, CacheWriteParams* pp,
+                           bool* nothing_to_do) {
+  *nothing_to_do = false;
+  pkv_status st;
+  if ((st = check_basic(key, "key", 3)) || (st = check_basic(value, "value", 3)) ||
+      (st = check_cache(key_cache, "key_cache")) || (st = check_cache(value_cache, "value_cache")) ||
+      (st = check_basic(slot_mapping, "slot_mapping", 1)))
+    return st;
+  if ((st = check_dtype(key, "key", PKV_F32, PKV_BF16, PKV_FP8_E4M3))) return st;
+  if ((st = check_dtype(slot_mapping, "slot_mapping", PKV_I64))) return st;
+  if (!same_layout(key, value)) return fail(PKV_ERR_INVALID_ARG, "key and value must share dtype, shape and strides");
+  if (!same_layout(key_cache, value_cache))
+    return fail(PKV_ERR_INVALID_ARG, "key_cache and value_cache must share dtype, shape and strides");
+  const int64_t T = key->shape[0], Hk = key->shape[1], D = key->shape[2];
+  if (key_cache->shape[1] != Hk || key_cache->shape[3] != D)
+    return fail(PKV_ERR_INVALID_ARG, "key [T, %lld, %lld] does not match the cache's [.., %lld, .., %lld]",
+                (long long)Hk, (long long)D, (long long)key_cache->shape[1], (long long)key_cache->shape[3]);
+  if (slot_mapping->shape[0] != T) return fail(PKV_ERR_INVALID_ARG, "slot_mapping must be [num_tokens]");
+  if (!supported_head_dim(D)) return fail(PKV_ERR_UNSUPPORTED, "head_dim %lld (supported: 64, 128)", (long long)D);
+  if (!supported_block_size(key_cache->shape[2]))
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %lld (supported: 2, 4, 8, 16, 32)", (long long)key_cache->shape[2]);
+  const bool same = key->dtype == key_cache->dtype;
+  const bool quant = key_cache->dtype == PKV_FP8_E4M3 && (key->dtype == PKV_F32 || key->dtype == PKV_BF16);
+  if (!same && !quant)
+    return fail(PKV_ERR_UNSUPPORTED, "writing %s tokens into a %s cache", dtype_name(key->dtype),
+                dtype_name(key_cache->dtype));
+  const int eb = elt_bytes(key->dtype);
+  if (!aligned16(key->data) || !aligned16(value->data) || (key->stride[0] * eb) % 16 || (key->stride[1] * eb) % 16)
+    return fail(PKV_ERR_INVALID_ARG, "key/value base pointers and strides must be multiples of 16 bytes");
+  if (T > 0x7fffffff) return fail(PKV_ERR_UNSUPPORTED, "too many tokens in one call");
+  if (g_opt_dry_run.load() || T == 0) {
+    *nothing_to_do = true;
+    return PKV_OK;
+  }
+
+  DeviceState* s;
+  if ((st = device_state(&s))) return st;
+  CacheWriteParams& p = *pp;
+  p = CacheWriteParams{};
+  p.key = key->data;
+  p.value = value->data;
+  p.src_stride_t = key->stride[0];
+  p.src_stride_h = key->stride[1];
+  p.src_dtype = key->dtype;
+  p.key_cache = key_cache->data;
+  p.value_cache = value_cache->data;
+  p.cs_block = key_cache->stride[0];
+  p.cs_head = key_cache->stride[1];
+  p.cache_dtype = key_cache->dtype;
+  p.k_scale = key_cache->scale;
+  p.v_scale = value_cache->scale;
+  p.slot_mapping = static_cast<const int64_t*>(slot_mapping->data);
+  p.num_tokens = T;
+  p.num_kv_heads = int(Hk);
+  p.head_dim = int(D);
+  p.block_size = int(key_cache->shape[2]);
+  p.num_blocks = key_cache->shape[0];
+  p.err = s->err;
+  return PKV_OK;
+}
+
 pkv_status set_error(pkv_status st, const char* msg) { return fail(st, "%s", msg); }
 
 pkv_status finish_launch(cudaError_t launch_err, cudaStream_t stream, const char* what) {
@@ -491,59 +555,47 @@ pkv_status pkv_paged_attention_decode(const pkv_tensor* out, const pkv_tensor* q
 pkv_status pkv_reshape_and_cache(const pkv_tensor* key, const pkv_tensor* value,
                                  const pkv_tensor* key_cache, const pkv_tensor* value_cache,
                                  const pkv_tensor* slot_mapping, pkv_stream stream) {
-  pkv_status st;
-  if ((st = check_basic(key, "key", 3)) || (st = check_basic(value, "value", 3)) ||
-      (st = check_cache(key_cache, "key_cache")) || (st = check_cache(value_cache, "value_cache")) ||
-      (st = check_basic(slot_mapping, "slot_mapping", 1)))
-    return st;
-  if ((st = check_dtype(key, "key", PKV_F32, PKV_BF16, PKV_FP8_E4M3))) return st;
-  if ((st = check_dtype(slot_mapping, "slot_mapping", PKV_I64))) return st;
-  if (!same_layout(key, value)) return fail(PKV_ERR_INVALID_ARG, "key and value must share dtype, shape and strides");
-  if (!same_layout(key_cache, value_cache))
-    return fail(PKV_ERR_INVALID_ARG, "key_cache and value_cache must share dtype, shape and strides");
-  const int64_t T = key->shape[0], Hk = key->shape[1], D = key->shape[2];
-  if (key_cache->shape[1] != Hk || key_cache->shape[3] != D)
-    return fail(PKV_ERR_INVALID_ARG, "key [T, %lld, %lld] does not match the cache's [.., %lld, .., %lld]",
-                (long long)Hk, (long long)D, (long long)key_cache->shape[1], (long long)key_cache->shape[3]);
-  if (slot_mapping->shape[0] != T) return fail(PKV_ERR_INVALID_ARG, "slot_mapping must be [num_tokens]");
-  if (!supported_head_dim(D)) return fail(PKV_ERR_UNSUPPORTED, "head_dim %lld (supported: 64, 128)", (long long)D);
-  if (!supported_block_size(key_cache->shape[2]))
-    return fail(PKV_ERR_UNSUPPORTED, "block_size %lld (supported: 2, 4, 8, 16, 32)", (long long)key_cache->shape[2]);
-  const bool same = key->dtype == key_cache->dtype;
-  const bool quant = key_cache->dtype == PKV_FP8_E4M3 && (key->dtype == PKV_F32 || key->dtype == PKV_BF16);
-  if (!same && !quant)
-    return fail(PKV_ERR_UNSUPPORTED, "writing %s tokens into a %s cache", dtype_name(key->dtype),
-                dtype_name(key_cache->dtype));
-  const int eb = elt_bytes(key->dtype);
-  if (!aligned16(key->data) || !aligned16(value->data) || (key->stride[0] * eb) % 16 || (key->stride[1] * eb) % 16)
-    return fail(PKV_ERR_INVALID_ARG, "key/value base pointers and strides must be multiples of 16 bytes");
-  if (T > 0x7fffffff) return fail(PKV_ERR_UNSUPPORTED, "too many tokens in one call");
-  if (g_opt_dry_run.load() || T == 0) return PKV_OK;
-
+  CacheWriteParams p;
+  bool nothing = false;
+  pkv_status st = reshape_prepare(key, value, key_cache, value_cache, slot_mapping, &p, &nothing);
+  if (st || nothing) return st;
   DeviceState* s;
   if ((st = device_state(&s))) return st;
-  CacheWriteParams p{};
-  p.key = key->data;
-  p.value = value->data;
-  p.src_stride_t = key->stride[0];
-  p.src_stride_h = key->stride[1];
-  p.src_dtype = key->dtype;
-  p.key_cache = key_cache->data;
-  p.value_cache = value_cache->data;
-  p.cs_block = key_cache->stride[0];
-  p.cs_head = key_cache->stride[1];
-  p.cache_dtype = key_cache->dtype;
-  p.k_scale = key_cache->scale;
-  p.v_scale = value_cache->scale;
-  p.slot_mapping = static_cast<const int64_t*>(slot_mapping->data);
-  p.num_tokens = T;
-  p.num_kv_heads = int(Hk);
-  p.head_dim = int(D);
-  p.block_size = int(key_cache->shape[2]);
-  p.num_blocks = key_cache->shape[0];
-  p.err = s->err;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   return finish_call(s, launch_reshape_and_cache(p, cs), cs, "reshape_and_cache");
+}
+
+pkv_status pkv_decode_step(const pkv_tensor* out, const pkv_tensor* query, const pkv_tensor* key,
+                           const pkv_tensor* value, const pkv_tensor* slot_mapping, const pkv_tensor* key_cache,
+                           const pkv_tensor* value_cache, const pkv_tensor* block_tables,
+                           const pkv_tensor* context_lens, int32_t num_kv_heads, float scale,
+                           int32_t block_size, int32_t max_blocks_per_seq, pkv_stream stream) {
+  // every check of both calls before anything is queued
+  CacheWriteParams wp;
+  bool no_write = false, no_decode = false;
+  pkv_status st = reshape_prepare(key, value, key_cache, value_cache, slot_mapping, &wp, &no_write);
+  if (st) return st;
+  DecodeParams p;
+  size_t ws_bytes = 0;
+  st = decode_prepare(out, query, key_cache, value_cache, block_tables, context_lens, num_kv_heads, scale,
+                      block_size, max_blocks_per_seq, &p, &ws_bytes, &no_decode);
+  if (st || g_opt_dry_run.load()) return st;
+  DeviceState* s;
+  if ((st = device_state(&s))) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (!no_decode && ws_bytes) {  // growth synchronises: before the write is queued
+    if ((st = ensure_workspace(s, ws_bytes, cs))) return st;
+    decode_set_workspace(&p, s->ws);
+  }
+  if (!no_write) {
+    cudaError_t e = launch_reshape_and_cache(wp, cs);
+    if (e != cudaSuccess || no_decode) return finish_call(s, e, cs, "decode_step (cache write)");
+    // the decode's preparation overlaps the write; it waits for the write before it
+    // reads the cache
+    p.overlap_prologue = p.kernel == 1;
+  }
+  if (no_decode) return PKV_OK;
+  return finish_call(s, launch_decode(p, cs), cs, "decode_step");
 }
 
 pkv_status pkv_copy_blocks(const pkv_tensor* cache, const pkv_tensor* src_dst_pairs, pkv_stream stream) {

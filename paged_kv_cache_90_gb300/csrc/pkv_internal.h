@@ -87,6 +87,10 @@ struct DecodeParams {
   int dyn_chunk;             // fewest stages per run-time unit
   int dyn_units_max;         // most run-time units (bounds the partial slots)
   int* work_ctr;             // [2]: next run-time unit, warps finished; zero between launches
+  // host only: launch the main kernel as a programmatic dependent of the kernel before
+  // it on the stream (set only when that kernel is this library's cache write, whose
+  // own launch ordered it after everything the caller queued)
+  bool overlap_prologue;
 };
 
 // The decode workspace starts with this many bytes of counters (zero while no launch

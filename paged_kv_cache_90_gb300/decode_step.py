@@ -49,19 +49,26 @@ class DeviceWorkload:
         self.out = torch.empty(s, hq, d, dtype=w.q_dtype, device=self.device)
 
     def run_step(self, i: int, out: Optional[torch.Tensor] = None, stream=None,
-                 step: Optional[DeviceStep] = None) -> torch.Tensor:
+                 step: Optional[DeviceStep] = None, joint: bool = True) -> torch.Tensor:
         """Run step ``i`` (or the given device-resident inputs) on the current
-        stream; returns the decode output tensor."""
+        stream; returns the decode output tensor.  ``joint`` issues the cache write and
+        the decode as one decode_step call, otherwise as two calls."""
         st = step if step is not None else self.steps[i]
         out = self.out if out is None else out
-        run_decode_step(self.w, self.key_cache, self.value_cache, st, out, stream)
+        run_decode_step(self.w, self.key_cache, self.value_cache, st, out, stream, joint)
         return out
 
 
-def run_decode_step(w: Workload, key_cache, value_cache, st: DeviceStep, out, stream=None) -> None:
+def run_decode_step(w: Workload, key_cache, value_cache, st: DeviceStep, out, stream=None,
+                    joint: bool = True) -> None:
     if st.cow_pairs.numel():
         binding.copy_blocks(key_cache, st.cow_pairs, stream)
         binding.copy_blocks(value_cache, st.cow_pairs, stream)
+    if joint:
+        binding.decode_step(out, st.query, st.new_key, st.new_value, st.slot_mapping, key_cache, value_cache,
+                            st.block_tables, st.context_lens, w.num_kv_heads, w.scale, w.block_size,
+                            w.max_blocks_per_seq, w.k_scale, w.v_scale, stream)
+        return
     if st.slot_mapping.numel():
         binding.reshape_and_cache(st.new_key, st.new_value, key_cache, value_cache, st.slot_mapping,
                                   w.k_scale, w.v_scale, stream)

@@ -59,6 +59,26 @@ def _status(fn, **kw):
         return e.status
 
 
+def test_decode_step_validation(dry):
+    """The joint write + decode call checks the arguments of both before queueing."""
+    def args(**over):
+        a = _decode_args()
+        T, Hk, D = 3, 2, 128
+        a.update(key=torch.zeros(T, Hk, D, dtype=torch.bfloat16), value=torch.zeros(T, Hk, D, dtype=torch.bfloat16),
+                 slot_mapping=torch.arange(T, dtype=torch.int64))
+        a.update(over)
+        return a
+    assert _status(binding.decode_step, **args()) == 0
+    assert _status(binding.decode_step, **args(slot_mapping=torch.arange(3, dtype=torch.int32))) == 2  # write side
+    assert _status(binding.decode_step, **args(key=torch.zeros(3, 2, 64, dtype=torch.bfloat16),
+                                               value=torch.zeros(3, 2, 64, dtype=torch.bfloat16))) == 1
+    assert _status(binding.decode_step, **args(num_kv_heads=3)) == 1                               # decode side
+    assert _status(binding.decode_step, **args(block_size=8)) == 1
+    empty = torch.zeros(0, 2, 128, dtype=torch.bfloat16)
+    assert _status(binding.decode_step, **args(key=empty, value=empty,
+                                               slot_mapping=torch.zeros(0, dtype=torch.int64))) == 0
+
+
 def test_decode_validation(dry):
     ok = _decode_args()
     assert _status(binding.paged_attention_decode, **ok) == 0

@@ -360,6 +360,28 @@ def test_launch_count_and_determinism(kernel):
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("case", ["llama3", "cb_e4m3_bs8", "cow"])
+def test_decode_step_equals_write_then_decode(case, kernel):
+    """The joint call gives the same bytes as the write and the decode issued as two
+    calls: outputs and both caches, step after step."""
+    make = {"llama3": lambda: wl.llama3_8b_decode(seed=41, num_seqs=12, len_range=(1, 1500), poison=True),
+            "cb_e4m3_bs8": lambda: wl.continuous_batching(seed=42, block_size=8, kv_dtype="e4m3", num_seqs=40,
+                                                          num_steps=3, median=300, cap=3000, poison=True),
+            "cow": lambda: wl.shared_prefix_cow(num_groups=4, prefix_blocks=8, suffix_range=(16, 120), poison=True)}
+    w = make[case]()
+    runs = {}
+    for joint in (True, False):
+        dw = DeviceWorkload(w)
+        outs = [dw.run_step(i, out=torch.empty_like(dw.out), joint=joint).clone() for i in range(len(w.steps))]
+        torch.cuda.synchronize()
+        runs[joint] = (outs, dw.key_cache.clone(), dw.value_cache.clone())
+    assert binding.read_device_errors() == 0
+    for a, b in zip(runs[True][0], runs[False][0]):
+        assert torch.equal(a, b)
+    assert torch.equal(raw(runs[True][1]), raw(runs[False][1]))
+    assert torch.equal(raw(runs[True][2]), raw(runs[False][2]))
+
+
 @pytest.fixture
 def work_split():
     def set_(share, chunk):
