@@ -382,6 +382,28 @@ def test_decode_step_equals_write_then_decode(case, kernel):
     assert torch.equal(raw(runs[True][2]), raw(runs[False][2]))
 
 
+def test_workspace_reuse_across_shapes_and_kernels():
+    """Calls with more, then fewer, then more rows share one workspace, with CUDA-core
+    calls (whose partial results use it differently) in between: every call matches the
+    oracle and raises no device error, so nothing is read that this call did not write
+    (partials of an earlier call with similar inputs would still be close)."""
+    cases = [("tensor", wl.llama3_8b_decode(seed=51, num_seqs=40, len_range=(1, 1200))),
+             ("core", wl.llama3_8b_decode(seed=52, num_seqs=24, len_range=(600, 3000))),
+             ("tensor", wl.llama3_8b_decode(seed=53, num_seqs=6, len_range=(1, 700))),
+             ("tensor", wl.continuous_batching(seed=54, block_size=16, kv_dtype="bf16", num_seqs=160, num_steps=2,
+                                               median=300, cap=3000)),
+             ("core", wl.llama3_8b_decode(seed=55, num_seqs=3, len_range=(900, 2000))),
+             ("tensor", wl.llama3_8b_decode(seed=56, num_seqs=64, len_range=(1, 2048)))]
+    try:
+        for kern, w in cases:
+            binding.set_option("decode_kernel", 2 if kern == "tensor" else 1)
+            binding.set_option("partition_tokens", 256 if kern == "core" else 0)
+            check_workload(w)
+    finally:
+        binding.set_option("decode_kernel", 0)
+        binding.set_option("partition_tokens", 0)
+
+
 @pytest.fixture
 def work_split():
     def set_(share, chunk):
