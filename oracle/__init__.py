@@ -56,6 +56,9 @@ def _load():
             lib.orc_paged_attention_decode.restype = i32
             lib.orc_paged_attention_decode.argtypes = (
                 [vp, vp, i32, vp, vp, i32, dbl, dbl, vp, vp] + [i64] * 10 + [dbl, i32])
+            lib.orc_paged_attention_decode_window.restype = i32
+            lib.orc_paged_attention_decode_window.argtypes = (
+                [vp, vp, i32, vp, vp, i32, dbl, dbl, vp, vp] + [i64] * 10 + [dbl, i64, i32])
             lib.orc_reshape_and_cache.restype = i32
             lib.orc_reshape_and_cache.argtypes = (
                 [vp, vp, i32, vp, vp, i32, ctypes.c_float, ctypes.c_float, vp] + [i64] * 8)
@@ -88,8 +91,9 @@ def max_threads() -> int:
 
 def paged_attention_decode(query, key_cache, value_cache, block_tables, context_lens,
                            scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
-                           num_threads: int = 1) -> torch.Tensor:
-    """Decode attention in fp64; returns a float64 tensor ``[S, Hq, D]``."""
+                           num_threads: int = 1, sliding_window: int = 0) -> torch.Tensor:
+    """Decode attention in fp64; returns a float64 tensor ``[S, Hq, D]``.  With
+    ``sliding_window`` W > 0 each sequence attends to its last W positions only."""
     lib = _load()
     q = _cpu(query)
     bt = _cpu(block_tables).to(torch.int32)
@@ -101,11 +105,11 @@ def paged_attention_decode(query, key_cache, value_cache, block_tables, context_
     cs = _cache_strides(key_cache)
     out = torch.zeros(s, hq, d, dtype=torch.float64)
     mb = bt.shape[1] if bt.dim() == 2 else 0
-    rc = lib.orc_paged_attention_decode(
+    rc = lib.orc_paged_attention_decode_window(
         out.data_ptr(), q.data_ptr(), _CODES[q.dtype], key_cache.data_ptr(),
         value_cache.data_ptr(), _CODES[key_cache.dtype], float(k_scale), float(v_scale),
         bt.data_ptr(), cl.data_ptr(), s, hq, hk, d, bs, nb, mb, cs[0], cs[1], cs[2],
-        float(scale), int(num_threads))
+        float(scale), int(sliding_window), int(num_threads))
     if rc != 0:
         raise ValueError(f"oracle decode failed with status {rc}")
     return out
@@ -176,4 +180,5 @@ def run_workload_step(w, step_index: int, key_cache, value_cache, num_threads: i
         reshape_and_cache(st.new_key, st.new_value, key_cache, value_cache, st.slot_mapping,
                           w.k_scale, w.v_scale)
     return paged_attention_decode(st.query, key_cache, value_cache, st.block_tables,
-                                  st.context_lens, w.scale, w.k_scale, w.v_scale, num_threads)
+                                  st.context_lens, w.scale, w.k_scale, w.v_scale, num_threads,
+                                  getattr(w, "sliding_window", 0))

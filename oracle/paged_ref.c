@@ -30,6 +30,16 @@
  *     scores, which the pseudo-code leaves out.)  Slots past L in the last block and
  *     table entries past ceil(L / bs) are never read.  L = 0 gives zeros.
  *
+ *  1b. Sliding-window decode.  A layer with attention window W > 0 attends to the last
+ *     W positions only: j in [max(0, L - W), L), the token just written included;
+ *     blocks wholly before the window are never read, so an engine may free them
+ *     (ya.zerocoder.ru "Что такое PagedAttention", section "Где подход не решает
+ *     задачу": TensorRT LLM's limited attention window frees blocks that leave the
+ *     window; vasteelab.pages.dev "PagedAttentionとは？", section "hybrid modelでは
+ *     block設計が複雑になる": sliding-window layers release old tokens).  The same
+ *     gather, scores, softmax and weighted sum run over that range; W <= 0 means no
+ *     window.
+ *
  *  2. Cache write ("reshape_and_cache").  New token t with slot = slot_mapping[t]:
  *       slot < 0  -> nothing is written (a padding token);
  *       else      -> cache[slot / bs, h, slot % bs, :] = encode(key[t, h, :])
@@ -169,7 +179,7 @@ void orc_bf16_decode_array(const uint16_t* bits, double* out, int64_t n) {
 
 /* Cache element (block b, KV head k, offset o, dim d) sits at
  *   b * cs_block + k * cs_head + o * cs_token + d      (elements). */
-int orc_paged_attention_decode(
+int orc_paged_attention_decode_window(
     double* out,                                 /* [S, Hq, D] */
     const void* query, int q_dtype,              /* [S, Hq, D], contiguous */
     const void* key_cache, const void* value_cache, int kv_dtype,
@@ -179,7 +189,7 @@ int orc_paged_attention_decode(
     int64_t num_seqs, int64_t num_heads, int64_t num_kv_heads, int64_t head_dim,
     int64_t block_size, int64_t num_blocks, int64_t max_blocks_per_seq,
     int64_t cs_block, int64_t cs_head, int64_t cs_token,
-    double scale, int num_threads) {
+    double scale, int64_t sliding_window, int num_threads) {
   int64_t group, work;
   int status = ORC_OK;
   if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
@@ -196,19 +206,24 @@ int orc_paged_attention_decode(
 #endif
   for (int64_t w = 0; w < work; ++w) {
     int64_t s = w / num_kv_heads, k = w % num_kv_heads;
-    int64_t L = context_lens[s];
+    int64_t Lctx = context_lens[s];
+    /* attended positions j0 .. Lctx-1; K, V, z below are indexed from j0 */
+    int64_t j0 = (sliding_window > 0 && Lctx > sliding_window) ? Lctx - sliding_window : 0;
+    int64_t L = Lctx - j0;
     double *K = NULL, *V = NULL, *z = NULL;
     int bad = 0;
-    if (L < 0 || L > max_blocks_per_seq * block_size) {
+    if (Lctx < 0 || Lctx > max_blocks_per_seq * block_size) {
       bad = ORC_BAD_TABLE;
+      L = 0;
     } else if (L > 0) {
       K = (double*)malloc(sizeof(double) * (size_t)(L * head_dim));
       V = (double*)malloc(sizeof(double) * (size_t)(L * head_dim));
       z = (double*)malloc(sizeof(double) * (size_t)L);
       if (!K || !V || !z) bad = ORC_NO_MEMORY;
     }
-    /* gather this sequence's K and V for KV head k, in logical order */
-    for (int64_t j = 0; j < L && !bad; ++j) {
+    /* gather this sequence's attended K and V for KV head k, in logical order */
+    for (int64_t i = 0; i < L && !bad; ++i) {
+      int64_t j = j0 + i;
       int64_t phys = block_tables[s * max_blocks_per_seq + j / block_size];
       int64_t base;
       if (phys < 0 || phys >= num_blocks) {
@@ -217,8 +232,8 @@ int orc_paged_attention_decode(
       }
       base = phys * cs_block + k * cs_head + (j % block_size) * cs_token;
       for (int64_t d = 0; d < head_dim; ++d) {
-        K[j * head_dim + d] = orc_load(key_cache, base + d, kv_dtype) * k_scale;
-        V[j * head_dim + d] = orc_load(value_cache, base + d, kv_dtype) * v_scale;
+        K[i * head_dim + d] = orc_load(key_cache, base + d, kv_dtype) * k_scale;
+        V[i * head_dim + d] = orc_load(value_cache, base + d, kv_dtype) * v_scale;
       }
     }
     for (int64_t h = k * group; h < (k + 1) * group; ++h) {
@@ -256,6 +271,19 @@ int orc_paged_attention_decode(
     }
   }
   return status;
+}
+
+/* Decode without a window. */
+int orc_paged_attention_decode(
+    double* out, const void* query, int q_dtype, const void* key_cache, const void* value_cache,
+    int kv_dtype, double k_scale, double v_scale, const int32_t* block_tables,
+    const int32_t* context_lens, int64_t num_seqs, int64_t num_heads, int64_t num_kv_heads,
+    int64_t head_dim, int64_t block_size, int64_t num_blocks, int64_t max_blocks_per_seq,
+    int64_t cs_block, int64_t cs_head, int64_t cs_token, double scale, int num_threads) {
+  return orc_paged_attention_decode_window(
+      out, query, q_dtype, key_cache, value_cache, kv_dtype, k_scale, v_scale, block_tables,
+      context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+      max_blocks_per_seq, cs_block, cs_head, cs_token, scale, 0, num_threads);
 }
 
 /* ---- 2. cache write -------------------------------------------------------------- */

@@ -85,16 +85,23 @@ class BlockAllocator:
         return self.refcount[block] == 0
 
 
+RELEASED = -1  # table entry of a block released after it left a sliding window
+
+
 @dataclass
 class SequenceBlocks:
     """One sequence's block table and its number of cached tokens."""
     blocks: List[int] = field(default_factory=list)
     length: int = 0
+    released: int = 0  # leading table entries released after they left a sliding window
 
     def slot(self, pos: int, block_size: int) -> int:
         if not 0 <= pos < len(self.blocks) * block_size:
             raise IndexError(f"position {pos} is outside the table")
-        return self.blocks[pos // block_size] * block_size + pos % block_size
+        b = self.blocks[pos // block_size]
+        if b == RELEASED:
+            raise IndexError(f"position {pos} lies in a released block")
+        return b * block_size + pos % block_size
 
 
 def blocks_needed(num_tokens: int, block_size: int) -> int:
@@ -130,13 +137,31 @@ class BlockManager:
             raise ValueError(f"sequence {child_id} exists")
         p = self.seqs[parent_id]
         for b in p.blocks:
-            self.alloc.incref(b)
-        self.seqs[child_id] = SequenceBlocks(list(p.blocks), p.length)
+            if b != RELEASED:
+                self.alloc.incref(b)
+        self.seqs[child_id] = SequenceBlocks(list(p.blocks), p.length, p.released)
 
     def free_sequence(self, seq_id) -> None:
         s = self.seqs.pop(seq_id)
         for b in s.blocks:
-            self.alloc.decref(b)
+            if b != RELEASED:
+                self.alloc.decref(b)
+
+    def release_outside_window(self, seq_id, window: int) -> List[int]:
+        """Sliding window of ``window`` positions: give back every block whose
+        positions all lie before the last ``window`` ones (attention never reads them
+        again); their table entries become RELEASED.  Returns the released ids
+        (ya.zerocoder.ru, section "Где подход не решает задачу": a limited attention
+        window frees the blocks that have left it)."""
+        s = self.seqs[seq_id]
+        first_kept = max(0, s.length - int(window)) // self.bs  # block holding the window's first position
+        out = []
+        for i in range(s.released, min(first_kept, len(s.blocks))):
+            self.alloc.decref(s.blocks[i])
+            out.append(s.blocks[i])
+            s.blocks[i] = RELEASED
+        s.released = max(s.released, min(first_kept, len(s.blocks)))
+        return out
 
     # -- growth ------------------------------------------------------------
     def append_token(self, seq_id) -> Tuple[int, Optional[Tuple[int, int]]]:
@@ -181,7 +206,8 @@ class BlockManager:
 
     # -- structural checks -------------------------------------------------
     def check_structure(self) -> None:
-        """Structural correctness: every table entry is an allocated block, each
+        """Structural correctness: every table entry is an allocated block (or, in a
+        leading run, a block released after it left a sliding window), each
         sequence's table covers its tokens exactly, reference counts equal the number
         of table entries pointing at each block, and no free block is referenced
         (ya.zerocoder.ru, section "Учебная трасса: рост последовательности": the
@@ -191,10 +217,15 @@ class BlockManager:
         for sid, s in self.seqs.items():
             if len(s.blocks) != blocks_needed(s.length, self.bs):
                 raise AssertionError(f"sequence {sid}: {len(s.blocks)} blocks for {s.length} tokens")
-            for b in s.blocks:
+            released = 0
+            while released < len(s.blocks) and s.blocks[released] == RELEASED:
+                released += 1
+            for b in s.blocks[released:]:
                 if not 0 <= b < self.alloc.num_blocks:
                     raise AssertionError(f"sequence {sid}: block {b} outside the pool")
                 counts[b] += 1
+            if released and released * self.bs >= s.length:
+                raise AssertionError(f"sequence {sid}: the block holding its last token was released")
         for b in range(self.alloc.num_blocks):
             if counts[b] != self.alloc.refcount[b]:
                 raise AssertionError(f"block {b}: refcount {self.alloc.refcount[b]} but {counts[b]} references")

@@ -61,6 +61,7 @@ class Workload:
     value_cache: torch.Tensor
     steps: List[DecodeStep] = field(default_factory=list)
     seed: int = 0
+    sliding_window: int = 0      # attend to the last W positions only (0: all)
 
     @property
     def num_seqs(self) -> int:
@@ -116,15 +117,18 @@ def _make_pool(nb, hk, bs, d, kv_dtype: str, g: torch.Generator):
 
 
 def _step(mgr: BlockManager, seq_ids: Sequence, g: torch.Generator, hq: int, hk: int,
-          d: int, q_dtype: torch.dtype, src_dtype: torch.dtype, mb: int) -> DecodeStep:
+          d: int, q_dtype: torch.dtype, src_dtype: torch.dtype, mb: int, window: int = 0) -> DecodeStep:
     """Every sequence in ``seq_ids`` appends one token (copy-on-write first if its
-    target block is shared); then the step's query and new K/V are drawn."""
+    target block is shared; with a sliding window, blocks that left it are released);
+    then the step's query and new K/V are drawn."""
     slots, pairs = [], []
     for sid in seq_ids:
         slot, pair = mgr.append_token(sid)
         slots.append(slot)
         if pair is not None:
             pairs.append(pair)
+        if window:
+            mgr.release_outside_window(sid, window)
     validate_cow_pairs(pairs, mgr.alloc.num_blocks)
     s = len(seq_ids)
     query = _randn((s, hq, d), q_dtype, g)
@@ -144,7 +148,8 @@ def _occupied_slots(mgr: BlockManager) -> torch.Tensor:
     occ = set()
     for s in mgr.seqs.values():
         for pos in range(s.length):
-            occ.add(s.slot(pos, mgr.bs))
+            if s.blocks[pos // mgr.bs] >= 0:  # not released
+                occ.add(s.slot(pos, mgr.bs))
     return torch.tensor(sorted(occ), dtype=torch.int64)
 
 
@@ -162,47 +167,62 @@ def _poison(cache: torch.Tensor, occupied: torch.Tensor) -> None:
         cache[~keep] = float("nan")
 
 
-def _finish(name, seed, hq, hk, d, bs, nb, mb, kc, vc, ks, vs, steps, scale=None) -> Workload:
+def _finish(name, seed, hq, hk, d, bs, nb, mb, kc, vc, ks, vs, steps, scale=None, window=0) -> Workload:
     return Workload(name=name, num_heads=hq, num_kv_heads=hk, head_dim=d, block_size=bs,
                     num_blocks=nb, max_blocks_per_seq=mb,
                     scale=float(scale if scale is not None else 1.0 / math.sqrt(d)),
-                    k_scale=ks, v_scale=vs, key_cache=kc, value_cache=vc, steps=steps, seed=seed)
+                    k_scale=ks, v_scale=vs, key_cache=kc, value_cache=vc, steps=steps, seed=seed,
+                    sliding_window=int(window))
 
 
 def variable_length_decode(name: str, seed: int, lengths: Sequence[int], num_heads: int,
                            num_kv_heads: int, head_dim: int, block_size: int, kv_dtype: str,
                            q_dtype: str = "bf16", num_steps: int = 1, pool_slack: float = 0.10,
                            num_blocks: Optional[int] = None, poison: bool = False,
-                           scale: Optional[float] = None) -> Workload:
+                           scale: Optional[float] = None, window: int = 0) -> Workload:
     """Sequences with the given context lengths *after* the first append.
 
     The pool holds the needed blocks (for all ``num_steps`` appends) plus
     ``pool_slack`` spare ones, handed out in a seeded random order so every table is a
-    scattered set of physical ids.  Each step appends one token per sequence.
+    scattered set of physical ids.  Each step appends one token per sequence.  With a
+    sliding ``window``, blocks wholly before each sequence's window are released (their
+    table entries -1; with ``poison`` their slots hold NaN) and may be handed out again.
     """
     g = torch.Generator().manual_seed(seed)
     lengths = [int(x) for x in lengths]
     if min(lengths) < 1:
         raise ValueError("every context length must count the appended token")
-    need = sum(blocks_needed(L + num_steps - 1, block_size) for L in lengths)
+    if window:  # a sequence holds its window's blocks, plus one being filled
+        need = sum(min(blocks_needed(L + num_steps - 1, block_size), blocks_needed(window, block_size) + 2)
+                   for L in lengths)
+    else:
+        need = sum(blocks_needed(L + num_steps - 1, block_size) for L in lengths)
     nb = num_blocks if num_blocks is not None else int(math.ceil(need * (1.0 + pool_slack)))
     mb = max(blocks_needed(L + num_steps - 1, block_size) for L in lengths)
     perm = torch.randperm(nb, generator=g).tolist()
     mgr = BlockManager(BlockAllocator(nb, block_size, perm))
     seq_ids = list(range(len(lengths)))
     for sid, L in zip(seq_ids, lengths):
-        mgr.add_sequence(sid, L - 1)
+        if not window:
+            mgr.add_sequence(sid, L - 1)
+            continue
+        # grow token by token, giving back what leaves the window; positions before the
+        # first step's window (L - window, after its append) are released too
+        mgr.add_sequence(sid, 0)
+        for _ in range(L - 1):
+            mgr.append_token(sid)
+            mgr.release_outside_window(sid, window - 1)
     kc, vc, ks, vs = _make_pool(nb, num_kv_heads, block_size, head_dim, kv_dtype, g)
     if poison:
         occ = _occupied_slots(mgr)
         _poison(kc, occ)
         _poison(vc, occ)
     src = torch.bfloat16 if kv_dtype == "e4m3" else DTYPES[kv_dtype]
-    steps = [_step(mgr, seq_ids, g, num_heads, num_kv_heads, head_dim, DTYPES[q_dtype], src, mb)
+    steps = [_step(mgr, seq_ids, g, num_heads, num_kv_heads, head_dim, DTYPES[q_dtype], src, mb, window)
              for _ in range(num_steps)]
     mgr.check_structure()
     return _finish(name, seed, num_heads, num_kv_heads, head_dim, block_size, nb, mb,
-                   kc, vc, ks, vs, steps, scale)
+                   kc, vc, ks, vs, steps, scale, window)
 
 
 # --- the five workloads -----------------------------------------------------------
@@ -323,10 +343,27 @@ def shared_prefix_cow(seed: int = 4, num_groups: int = 32, group_size: int = 4,
                    nb, mb, kc, vc, ks, vs, [step])
 
 
+def sliding_window_decode(seed: int = 6, num_seqs: int = 8, context_len: int = 32768, window: int = 4096,
+                          block_size: int = 16, kv_dtype: str = "bf16", num_steps: int = 1,
+                          len_range=None, poison: bool = False) -> Workload:
+    """Decode of a sliding-window layer: sequences of ``context_len`` tokens (or lengths
+    uniform in ``len_range``) attend to their last ``window`` positions; the blocks
+    before each window are released.  32/8 heads, head_dim 128."""
+    g = torch.Generator().manual_seed(seed)
+    if len_range is not None:
+        lens = (torch.randint(len_range[0], len_range[1] + 1, (num_seqs,), generator=g) + 1).tolist()
+    else:
+        lens = [context_len] * num_seqs
+    return variable_length_decode(f"sliding_window_s{num_seqs}_W{window}_bs{block_size}_{kv_dtype}", seed,
+                                  lens, 32, 8, 128, block_size, kv_dtype, num_steps=num_steps,
+                                  poison=poison, window=window)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "llama3_8b_decode": llama3_8b_decode,
     "long_context": long_context,
     "shared_prefix_cow": shared_prefix_cow,
     "continuous_batching": continuous_batching,
+    "sliding_window": sliding_window_decode,
 }

@@ -153,3 +153,31 @@ def test_pool_exhaustion_and_bad_pairs():
         validate_cow_pairs([(0, 1), (1, 2)], 4)
     with pytest.raises(ValueError):
         validate_cow_pairs([(0, 9)], 4)
+
+
+def test_release_outside_window():
+    """40 tokens at 16 per block with a window of 16: positions 24..39 are attended,
+    so block 0 (positions 0..15) is released and blocks 1 and 2 stay; releasing is
+    idempotent and the block returns to the free list."""
+    from paged_kv_cache_90_gb300.block_manager import RELEASED
+    mgr = BlockManager(BlockAllocator(8, 16, list(range(8))))
+    mgr.add_sequence("a", 40)
+    blocks = list(mgr.seqs["a"].blocks)
+    free0 = mgr.alloc.num_free
+    assert mgr.release_outside_window("a", 16) == [blocks[0]]
+    assert mgr.seqs["a"].blocks == [RELEASED] + blocks[1:]
+    assert mgr.release_outside_window("a", 16) == []
+    assert mgr.alloc.num_free == free0 + 1
+    mgr.check_structure()
+    with pytest.raises(IndexError):
+        mgr.seqs["a"].slot(3, 16)
+    assert mgr.seqs["a"].slot(24, 16) == blocks[1] * 16 + 8
+    # the released block is handed out again; the structure stays consistent
+    mgr.add_sequence("b", 16 * 6)
+    mgr.check_structure()
+    # a window of one token keeps only the block holding the last position
+    mgr.release_outside_window("a", 1)
+    assert mgr.seqs["a"].blocks[:2] == [RELEASED, RELEASED]
+    mgr.check_structure()
+    mgr.free_sequence("a")
+    mgr.check_structure()

@@ -390,3 +390,101 @@ def test_fp8_cache_write_matches_torch_cast():
         qv = (st.new_value[t].float() / w.v_scale).clamp(-448, 448).to(torch.float8_e4m3fn)
         assert torch.equal(kc[blk, :, off].view(torch.uint8), qk.view(torch.uint8))
         assert torch.equal(vc[blk, :, off].view(torch.uint8), qv.view(torch.uint8))
+
+
+# --- sliding-window decode ------------------------------------------------------------
+
+def _decode_w(w, window, step=0, kc=None, vc=None, tables=None):
+    st = w.steps[step]
+    if kc is None:
+        kc, vc = _materialize(w, step)
+    bt = st.block_tables if tables is None else tables
+    return oracle.paged_attention_decode(st.query, kc, vc, bt, st.context_lens, w.scale, w.k_scale,
+                                         w.v_scale, sliding_window=window)
+
+
+def test_window_covering_the_context_is_full_attention():
+    """A window at least as long as every context changes nothing, bit for bit."""
+    w = _small(41, [1, 7, 33, 64], poison=True)
+    kc, vc = _materialize(w)
+    full = _decode(w, kc=kc, vc=vc)
+    for window in (64, 65, 1000):
+        assert torch.equal(_decode_w(w, window, kc=kc, vc=vc), full)
+    assert torch.equal(_decode_w(w, 0, kc=kc, vc=vc), full)
+
+
+def test_window_of_one_returns_the_newest_value():
+    """W = 1: only the token just written is attended, so the output is its value
+    exactly, whatever the queries and keys."""
+    w = _small(42, [1, 6, 17, 40], kv="f32", q="f32", poison=True)
+    kc, vc = _materialize(w)
+    out = _decode_w(w, 1, kc=kc, vc=vc)
+    st = w.steps[0]
+    g = 4 // 2
+    for s, L in enumerate(st.context_lens.tolist()):
+        for h in range(4):
+            v = _gather(vc, st.block_tables[s], h // g, L, 4)[L - 1].double()
+            assert torch.equal(out[s, h], v)
+
+
+@pytest.mark.parametrize("bs", [4, 8, 16])
+@pytest.mark.parametrize("window", [2, 5, 16, 23])
+def test_window_equals_dense_sdpa_on_the_last_positions(bs, window):
+    """Against torch's scaled_dot_product_attention in float64 over the last W
+    gathered positions only."""
+    lens = [1, window - 1, window, window + 1, 3 * bs + 7, 70]
+    w = _small(43 + bs + window, [max(1, L) for L in lens], d=16, bs=bs, poison=True)
+    kc, vc = _materialize(w)
+    out = _decode_w(w, window, kc=kc, vc=vc)
+    st = w.steps[0]
+    for s, L in enumerate(st.context_lens.tolist()):
+        lo = max(0, L - window)
+        ks = torch.stack([_gather(kc, st.block_tables[s], k, L, bs)[lo:] for k in range(2)]).double()
+        vs = torch.stack([_gather(vc, st.block_tables[s], k, L, bs)[lo:] for k in range(2)]).double()
+        ks = ks.repeat_interleave(2, dim=0)[None]
+        vs = vs.repeat_interleave(2, dim=0)[None]
+        qs = st.query[s].double()[None, :, None, :]
+        ref = torch.nn.functional.scaled_dot_product_attention(qs, ks, vs, scale=w.scale)
+        assert torch.allclose(out[s], ref[0, :, 0], rtol=0, atol=1e-12), (s, L)
+
+
+def test_window_never_reads_blocks_before_it():
+    """Blocks wholly before the window may be released: -1 table entries and NaN in
+    those blocks give the same output as intact ones, while an entry inside the
+    window that is invalid is still reported."""
+    w = _small(44, [50, 70, 33], bs=4, poison=True)
+    kc, vc = _materialize(w)
+    window = 21
+    ref = _decode_w(w, window, kc=kc, vc=vc)
+    st = w.steps[0]
+    bt = st.block_tables.clone()
+    kc2, vc2 = kc.clone(), vc.clone()
+    for s, L in enumerate(st.context_lens.tolist()):
+        first = max(0, L - window) // 4
+        for i in range(first):
+            b = int(bt[s, i])
+            kc2[b] = float("nan")
+            vc2[b] = float("nan")
+            bt[s, i] = -1
+    assert torch.equal(_decode_w(w, window, kc=kc2, vc=vc2, tables=bt), ref)
+    s, L = 0, int(st.context_lens[0])
+    bt[s, (L - 1) // 4] = -1
+    with pytest.raises(ValueError):
+        _decode_w(w, window, kc=kc2, vc=vc2, tables=bt)
+
+
+def test_sliding_window_workload_releases_and_reuses_blocks():
+    """The harness releases the blocks that left each window (entries -1), hands them
+    out again, keeps the structure consistent, and the oracle never needs them."""
+    w = wl.sliding_window_decode(seed=45, num_seqs=6, window=24, block_size=8, num_steps=4,
+                                 len_range=(1, 120), poison=True)
+    kc, vc = w.key_cache.clone(), w.value_cache.clone()
+    for i, st in enumerate(w.steps):
+        for L, row in zip(st.context_lens.tolist(), st.block_tables.tolist()):
+            first = max(0, L - 24) // 8
+            assert all(x == -1 for x in row[:first])
+            assert all(x >= 0 for x in row[first:-(-L // 8)])
+        out = oracle.run_workload_step(w, i, kc, vc)
+        assert torch.isfinite(out).all()
+    # the pool is sized for the windows, far below the full contexts
+    assert w.num_blocks < sum(-(-int(L) // 8) for L in w.steps[-1].context_lens)
