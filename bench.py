@@ -61,6 +61,9 @@ def make_workload(name: str, rank: int = 0) -> wl.Workload:
     m = re.fullmatch(r"continuous_batching_bs(\d+)_(bf16|e4m3)", name)
     if m:
         return wl.continuous_batching(seed=5 + seed_off, block_size=int(m.group(1)), kv_dtype=m.group(2))
+    m = re.fullmatch(r"sliding_window(?:_bs(\d+))?", name)
+    if m:   # Mistral-style 4096-position window over 8 x 32768-token contexts
+        return wl.sliding_window_decode(seed=6 + seed_off, block_size=int(m.group(1) or 16))
     if name == "tiny":
         return wl.tiny(seed=1 + seed_off)
     raise SystemExit(f"unknown workload {name}")
@@ -74,13 +77,19 @@ def describe_workload(w: wl.Workload, name: str) -> str:
 
 
 def decode_bytes(w: wl.Workload, st) -> int:
-    """Bytes paged decode must move for one step: K and V of every context token of
-    every KV head, queries in, outputs out, table entries and lengths."""
+    """Bytes paged decode must move for one step: K and V of every attended token of
+    every KV head (with a sliding window, the last W positions), queries in, outputs
+    out, the table entries of the blocks holding those tokens, and lengths."""
     elt = w.key_cache.element_size()
     L = st.context_lens.long()
-    kv = int(L.sum()) * w.num_kv_heads * w.head_dim * elt * 2
+    W = int(getattr(w, "sliding_window", 0))
+    start = (L - W).clamp(min=0) if W > 0 else torch.zeros_like(L)
+    n = L - start
+    kv = int(n.sum()) * w.num_kv_heads * w.head_dim * elt * 2
     q = st.query.numel() * st.query.element_size()
-    tbl = int(((L + w.block_size - 1) // w.block_size).sum()) * 4 + 4 * L.numel()
+    first_blk = start // w.block_size
+    last_blk = (L + w.block_size - 1) // w.block_size
+    tbl = int((last_blk - first_blk).clamp(min=0).sum()) * 4 + 4 * L.numel()
     return kv + 2 * q + tbl
 
 
@@ -202,7 +211,7 @@ def oracle_throughput(w: wl.Workload, budget_s: float, max_seqs=None):
                             st.block_tables[:n], st.context_lens[:n], st.cow_pairs[:0])
         t = time.perf_counter()
         oracle.paged_attention_decode(sub.query, kc, vc, sub.block_tables, sub.context_lens, w.scale,
-                                      w.k_scale, w.v_scale, threads)
+                                      w.k_scale, w.v_scale, threads, w.sliding_window)
         elapsed += time.perf_counter() - t
         done_bytes += decode_bytes(w, sub)
         reps += 1
@@ -323,7 +332,7 @@ def run_gpu(args, world, rank, local):
         b.record(stream)
         binding.paged_attention_decode(dw.out, st.query, dw.key_cache, dw.value_cache, st.block_tables,
                                        st.context_lens, w.num_kv_heads, w.scale, w.block_size,
-                                       w.max_blocks_per_seq, w.k_scale, w.v_scale)
+                                       w.max_blocks_per_seq, w.k_scale, w.v_scale, None, w.sliding_window)
         c.record(stream)
     torch.cuda.synchronize(dev)
     barrier()

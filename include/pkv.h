@@ -10,7 +10,9 @@
  *   pkv_paged_attention_decode   single-query attention of every sequence over its
  *                                cached tokens, read through its block table;
  *   pkv_decode_step              the cache write and the decode of one step in one
- *                                call (the decode's preparation overlaps the write).
+ *                                call (the decode's preparation overlaps the write);
+ *   pkv_paged_attention_decode_window  decode of a sliding-window layer (only the
+ *                                last W positions; blocks before them never read).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -131,6 +133,31 @@ pkv_status pkv_paged_attention_decode(const pkv_tensor* out, const pkv_tensor* q
                                       int32_t max_blocks_per_seq, pkv_stream stream);
 
 /*
+ * pkv_paged_attention_decode_window — decode attention of a sliding-window layer:
+ * sequence s attends to its last `sliding_window` positions only.
+ *
+ * Defined by: ya.zerocoder.ru "Что такое PagedAttention", section "Где подход не
+ * решает задачу" (TensorRT LLM's limited attention window frees the blocks that have
+ * left the window) and vasteelab.pages.dev "PagedAttentionとは？", section "hybrid
+ * modelではblock設計が複雑になる" (sliding-window layers release old tokens).
+ *
+ * With L = context_lens[s] and W = sliding_window: the result of
+ * pkv_paged_attention_decode over positions j in [max(0, L - W), L) only (the token
+ * just written included).  W == 0 means no window (the full context).  Table entries of
+ * blocks that lie wholly before max(0, L - W) are never read, so an engine may free
+ * those blocks and leave any value (e.g. -1) in their entries.  Other arguments, layouts
+ * and errors as for pkv_paged_attention_decode; W < 0 returns PKV_ERR_INVALID_ARG.
+ */
+pkv_status pkv_paged_attention_decode_window(const pkv_tensor* out, const pkv_tensor* query,
+                                             const pkv_tensor* key_cache,
+                                             const pkv_tensor* value_cache,
+                                             const pkv_tensor* block_tables,
+                                             const pkv_tensor* context_lens,
+                                             int32_t num_kv_heads, float scale,
+                                             int32_t block_size, int32_t max_blocks_per_seq,
+                                             int32_t sliding_window, pkv_stream stream);
+
+/*
  * pkv_reshape_and_cache — write new tokens' K and V into their cache slots.
  *
  * Defined by: vasteelab.pages.dev "PagedAttentionとは？", section
@@ -175,17 +202,18 @@ pkv_status pkv_reshape_and_cache(const pkv_tensor* key, const pkv_tensor* value,
  * read of the cache; the write itself is an ordinary launch, ordered after everything
  * queued on the stream before the call.
  *
- * Arguments are those of the two calls (key_cache / value_cache shared).  Every
- * argument of both is checked before anything is queued; an error returns without
- * queueing either.  num_tokens may be 0 (decode only) and num_seqs may be 0 (write
- * only).
+ * Arguments are those of the two calls (key_cache / value_cache shared), the decode
+ * being pkv_paged_attention_decode_window with `sliding_window` (0: the full context).
+ * Every argument of both is checked before anything is queued; an error returns
+ * without queueing either.  num_tokens may be 0 (decode only) and num_seqs may be 0
+ * (write only).
  */
 pkv_status pkv_decode_step(const pkv_tensor* out, const pkv_tensor* query, const pkv_tensor* key,
                            const pkv_tensor* value, const pkv_tensor* slot_mapping,
                            const pkv_tensor* key_cache, const pkv_tensor* value_cache,
                            const pkv_tensor* block_tables, const pkv_tensor* context_lens,
                            int32_t num_kv_heads, float scale, int32_t block_size,
-                           int32_t max_blocks_per_seq, pkv_stream stream);
+                           int32_t max_blocks_per_seq, int32_t sliding_window, pkv_stream stream);
 
 /*
  * pkv_copy_blocks — copy whole physical blocks of one cache tensor.

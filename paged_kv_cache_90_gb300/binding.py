@@ -60,11 +60,13 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.pkv_reshape_and_cache.argtypes = [d, d, d, d, d, vp]
         lib.pkv_copy_blocks.argtypes = [d, d, vp]
         lib.pkv_paged_attention_decode_noalloc.argtypes = [d, d, d, d, d, d, i32, f32, i32, i32, vp]
-        lib.pkv_decode_step.argtypes = [d, d, d, d, d, d, d, d, d, i32, f32, i32, i32, vp]
+        lib.pkv_decode_step.argtypes = [d, d, d, d, d, d, d, d, d, i32, f32, i32, i32, i32, vp]
+        lib.pkv_paged_attention_decode_window.argtypes = [d, d, d, d, d, d, i32, f32, i32, i32, i32, vp]
         lib.pkv_noalloc_scratch_bytes.restype = i64
         lib.pkv_noalloc_scratch_bytes.argtypes = []
         for fn in ("pkv_paged_attention_decode", "pkv_paged_attention_decode_noalloc",
                    "pkv_reshape_and_cache", "pkv_decode_step", "pkv_copy_blocks",
+                   "pkv_paged_attention_decode_window",
                    "pkv_set_option", "pkv_reserve_workspace", "pkv_read_device_errors"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.pkv_last_error.restype = ctypes.c_char_p
@@ -119,20 +121,28 @@ def _stream(stream) -> ctypes.c_void_p:
 def paged_attention_decode(out, query, key_cache, value_cache, block_tables, context_lens,
                            num_kv_heads: int, scale: float, block_size: int,
                            max_blocks_per_seq: int, k_scale: float = 1.0, v_scale: float = 1.0,
-                           stream=None) -> torch.Tensor:
-    """Single-token decode attention over the paged cache into ``out`` (returned)."""
+                           stream=None, sliding_window: int = 0) -> torch.Tensor:
+    """Single-token decode attention over the paged cache into ``out`` (returned).
+    ``sliding_window`` W > 0: each sequence attends to its last W positions only
+    (pkv_paged_attention_decode_window)."""
     lib = load_library()
     descs = [describe(out), describe(query), describe(key_cache, k_scale),
              describe(value_cache, v_scale), describe(block_tables), describe(context_lens)]
-    _check(lib.pkv_paged_attention_decode(*[ctypes.byref(x) for x in descs], int(num_kv_heads),
-                                          float(scale), int(block_size), int(max_blocks_per_seq),
-                                          _stream(stream)))
+    args = [ctypes.byref(x) for x in descs]
+    if sliding_window:
+        _check(lib.pkv_paged_attention_decode_window(*args, int(num_kv_heads), float(scale), int(block_size),
+                                                     int(max_blocks_per_seq), int(sliding_window),
+                                                     _stream(stream)))
+    else:
+        _check(lib.pkv_paged_attention_decode(*args, int(num_kv_heads), float(scale), int(block_size),
+                                              int(max_blocks_per_seq), _stream(stream)))
     return out
 
 
 def decode_step(out, query, key, value, slot_mapping, key_cache, value_cache, block_tables, context_lens,
                 num_kv_heads: int, scale: float, block_size: int, max_blocks_per_seq: int,
-                k_scale: float = 1.0, v_scale: float = 1.0, stream=None) -> torch.Tensor:
+                k_scale: float = 1.0, v_scale: float = 1.0, stream=None,
+                sliding_window: int = 0) -> torch.Tensor:
     """Append the step's new tokens (``key``/``value`` at ``slot_mapping``) to the cache
     and decode into ``out`` (returned): the results of reshape_and_cache followed by
     paged_attention_decode, with the decode's preparation overlapping the write."""
@@ -141,7 +151,7 @@ def decode_step(out, query, key, value, slot_mapping, key_cache, value_cache, bl
              describe(key_cache, k_scale), describe(value_cache, v_scale), describe(block_tables),
              describe(context_lens)]
     _check(lib.pkv_decode_step(*[ctypes.byref(x) for x in descs], int(num_kv_heads), float(scale),
-                               int(block_size), int(max_blocks_per_seq), _stream(stream)))
+                               int(block_size), int(max_blocks_per_seq), int(sliding_window), _stream(stream)))
     return out
 
 

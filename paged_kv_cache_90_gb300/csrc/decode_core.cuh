@@ -97,12 +97,17 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const DecodeParams p)
     L = L < 0 ? 0 : max_ctx;
   }
   const int PT = p.partition_tokens;
-  const int nparts = L > 0 ? (L + PT - 1) / PT : 1;
-  if (part >= nparts) return;
-  const int tok_begin = part * PT;
-  const int ntok = L - tok_begin < PT ? L - tok_begin : PT;  // tokens of this partition (>= 0)
-  const int nstages = (ntok + T::kStageTokens - 1) / T::kStageTokens;
   const int bs = p.block_size;
+  // partitions tile [base, L): base is the window's first position rounded down to a
+  // block, so no block wholly before the window is read
+  const int start = window_start(L, p.sliding_window);
+  const int base = start - start % bs;
+  const int nparts = L > base ? (L - base + PT - 1) / PT : 1;
+  if (part >= nparts) return;
+  const int tok_begin = base + part * PT;
+  const int ntok = L - tok_begin < PT ? L - tok_begin : PT;  // tokens of this partition (>= 0)
+  const int lo_valid = start - tok_begin;                     // tokens before it are masked
+  const int nstages = (ntok + T::kStageTokens - 1) / T::kStageTokens;
   const int blk_begin = tok_begin / bs;
   const int nblk = (ntok + bs - 1) / bs;
 
@@ -186,6 +191,7 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const DecodeParams p)
     const unsigned char* Vs = Vst + size_t(sidx) * T::kStageBytes;
     const int nvalid = ntok - it * T::kStageTokens;     // valid tokens from the stage start
     const int wvalid = nvalid - wt0;                    // ... from this warp's first token
+    const int wlo = lo_valid - it * T::kStageTokens - wt0;  // first attended token of the warp
 
     // scores of this warp's tokens, all G heads
     float sc[T::kPasses][G];
@@ -210,7 +216,7 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const DecodeParams p)
       for (int off = 1; off < T::kLPT; off <<= 1)
 #pragma unroll
         for (int h = 0; h < G; ++h) acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], off);
-      const bool valid = tw < wvalid;
+      const bool valid = tw < wvalid && tw >= wlo;
 #pragma unroll
       for (int h = 0; h < G; ++h) sc[ps][h] = valid ? acc[h] : -INFINITY;
     }

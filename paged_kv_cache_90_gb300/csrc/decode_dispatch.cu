@@ -39,7 +39,9 @@ __global__ void decode_reduce_kernel(const DecodeParams p) {
   int L = p.context_lens[seq];
   const int max_ctx = p.max_blocks_per_seq * p.block_size;
   L = L < 0 ? 0 : (L > max_ctx ? max_ctx : L);
-  const int nparts = L > 0 ? (L + p.partition_tokens - 1) / p.partition_tokens : 1;
+  const int start = window_start(L, p.sliding_window);
+  const int first = start - start % p.block_size;  // the main kernel's partitions tile [first, L)
+  const int nparts = L > first ? (L - first + p.partition_tokens - 1) / p.partition_tokens : 1;
   if (nparts == 1) return;  // the main kernel wrote this row itself
   const int64_t base = (int64_t(seq) * p.num_heads + hq) * p.max_partitions;
   float M = -INFINITY;

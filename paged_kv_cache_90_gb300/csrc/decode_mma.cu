@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_split_rows_kernel(const D
     int local = 0;
     for (int s = s0; s < s0 + per && s < S; ++s) {
       const int L = min(max(p.context_lens[s], 0), max_ctx);
-      local += ((L + mma::kST - 1) & ~(mma::kST - 1)) * tiles;
+      local += ((L - mma::row_base(L, p.sliding_window, p.block_size) + mma::kST - 1) & ~(mma::kST - 1)) * tiles;
     }
     int incl = local;
 #pragma unroll
@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_split_rows_kernel(const D
     for (int s = s0; s < s0 + per && s < S; ++s) {
       cum[s] = run;
       const int L = min(max(p.context_lens[s], 0), max_ctx);
-      run += ((L + mma::kST - 1) & ~(mma::kST - 1)) * tiles;
+      run += ((L - mma::row_base(L, p.sliding_window, p.block_size) + mma::kST - 1) & ~(mma::kST - 1)) * tiles;
     }
     if (tid == kMergeThreads - 1) cum[S] = base + incl;
     __syncthreads();

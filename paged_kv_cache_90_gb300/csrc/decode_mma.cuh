@@ -144,20 +144,30 @@ struct Cfg {
 };
 
 // Position in the flattened (sequence, head tile, stage) order.  cum[s] is the first
-// flattened token of sequence s; a sequence holds `tiles` rows of equal padded length.
-// Everything the per-stage code needs is carried, so advancing costs no division.
+// flattened token of sequence s; a sequence holds `tiles` rows of equal padded length,
+// each covering its context from `base` (0, or with a sliding window the window's first
+// position rounded down to a stage and block boundary) to L.  Everything the per-stage
+// code needs is carried, so advancing costs no division.
 struct Cursor {
   int s, tile, kvh, sub;  // sequence, head tile, its KV head, tile within the KV head
-  int t0;                 // first token of the stage within the row
-  int rl, L;              // padded row length and context length of sequence s
+  int t0;                 // first token of the stage within the row (from base)
+  int rl, L, base;        // padded row length, context length and first row token of s
   int left;               // stages left in this warp's range, this one included
 };
 
 struct Geometry {
   const int* cum;    // shared memory: flattened offset of each sequence (S + 1 entries)
   const int* lens;   // shared memory: clamped context length of each sequence
-  int tiles, tiles_per_kv, max_ctx;
+  int tiles, tiles_per_kv, max_ctx, window, block_size;
 };
+
+// First token of a sequence's rows: the window's first position rounded down so that
+// stages start on a block (block size 8) or 16-token boundary.
+__device__ __forceinline__ int row_base(int L, int window, int block_size) {
+  const int start = window_start(L, window);
+  const int align = block_size < kST ? block_size : kST;
+  return start - start % align;
+}
 
 // Units of work over the NS flattened stages.  Units 0..GW-1 are the warps' static
 // units: stages [0, NSs) split evenly, q or q + 1 consecutive stages each (some empty
@@ -188,7 +198,8 @@ __device__ __forceinline__ int clamp_len(int L, int max_ctx) { return L < 0 ? 0 
 
 __device__ __forceinline__ void cursor_load_seq(Cursor& c, const Geometry& q) {
   c.L = q.lens[c.s];
-  c.rl = (c.L + kST - 1) & ~(kST - 1);
+  c.base = row_base(c.L, q.window, q.block_size);
+  c.rl = (c.L - c.base + kST - 1) & ~(kST - 1);
 }
 
 __device__ __forceinline__ void cursor_next(Cursor& c, const Geometry& q) {
@@ -227,7 +238,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
 
   const int max_ctx = p.max_blocks_per_seq * p.block_size;
   const int tiles = p.num_heads / G;
-  const Geometry geo{cum, lens, tiles, p.group / G, max_ctx};
+  const Geometry geo{cum, lens, tiles, p.group / G, max_ctx, p.sliding_window, p.block_size};
 
   // the merge kernel behind this one may be scheduled now (it waits for our writes)
   asm volatile("griddepcontrol.launch_dependents;");
@@ -241,7 +252,8 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
     for (int s = s0; s < s0 + per && s < S; ++s) {
       const int L = p.context_lens[s];
       if (L < 0 || L > max_ctx) raise_device_error(p.err, kErrContextLen);
-      local += ((clamp_len(L, max_ctx) + kST - 1) & ~(kST - 1)) * tiles;
+      const int Lc = clamp_len(L, max_ctx);
+      local += ((Lc - row_base(Lc, p.sliding_window, p.block_size) + kST - 1) & ~(kST - 1)) * tiles;
     }
     int incl = local;
 #pragma unroll
@@ -260,9 +272,10 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
     int run = base + incl - local;
     for (int s = s0; s < s0 + per && s < S; ++s) {
       const int L = clamp_len(p.context_lens[s], max_ctx);
+      const int b0 = row_base(L, p.sliding_window, p.block_size);
       cum[s] = run;
       lens[s] = L;
-      run += ((L + kST - 1) & ~(kST - 1)) * tiles;
+      run += ((L - b0 + kST - 1) & ~(kST - 1)) * tiles;
     }
     if (tid == kThreads - 1) cum[S] = base + incl;
     __syncthreads();
@@ -322,9 +335,10 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
         const int mid = (lo + hi + 1) >> 1;
         if (cum[mid] <= pos) lo = mid; else hi = mid - 1;
       }
-      const int rl = (lens[lo] + kST - 1) & ~(kST - 1);
+      const int b0 = row_base(lens[lo], p.sliding_window, bs);
+      const int rl = (lens[lo] - b0 + kST - 1) & ~(kST - 1);
       const int off = pos - cum[lo];
-      const int t0 = off - (off / rl) * rl;
+      const int t0 = b0 + off - (off / rl) * rl;  // the stage's first token in the context
       const int b = t0 >> bs_shift;
       const int32_t* row = p.block_tables + int64_t(lo) * bt_stride;
       e0 = __ldg(row + b);
@@ -385,7 +399,8 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
     }
     tags[islot] = iu;
     unsigned char* sb = wbase + size_t(islot) * C::kStageBytes;
-    const int nbox = (two_boxes && icur.t0 + 8 < icur.L) ? 2 : 1;
+    const int tok = icur.base + icur.t0;  // the stage's first token in the context
+    const int nbox = (two_boxes && tok + 8 < icur.L) ? 2 : 1;
     if (lane == 0) mbar_arrive_expect_tx(&bars[islot], uint32_t(kOpsPerBox * nbox) * box_bytes);
     if (lane < kOpsPerBox * nbox) {  // one copy per lane
       int blk = op_b == 0 ? e0 : e1;
@@ -393,7 +408,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
         raise_device_error(p.err, kErrTableEntry);
         blk = 0;
       }
-      tma_load_4d(sb + op_off, op_map, 64 * op_h, icur.t0 & (bs - 1), icur.kvh, blk, &bars[islot], stream_policy);
+      tma_load_4d(sb + op_off, op_map, 64 * op_h, tok & (bs - 1), icur.kvh, blk, &bars[islot], stream_policy);
     }
     cursor_next(icur, geo);
     ++issued;
@@ -519,7 +534,9 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
     unsigned char* sb = wbase + size_t(slot) * C::kStageBytes;
     const unsigned char* kt = sb;
     unsigned char* vt = sb + C::kRawTile;
-    const int nvalid = cc.L - cc.t0 < kST ? cc.L - cc.t0 : kST;
+    const int ctok = cc.base + cc.t0;                     // the stage's first token in the context
+    const int nvalid = cc.L - ctok < kST ? cc.L - ctok : kST;
+    const int lo_valid = window_start(cc.L, p.sliding_window) - ctok;  // > 0: window starts inside
 
     // values as 16-bit operand rows (8-bit cache: convert; rows past the context: zero)
     const unsigned char* vop = vt;
@@ -603,12 +620,14 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) s[nt][2 * rr + e] *= sl;
-      if (nvalid < kST) {  // the row's last, partly filled stage
+      if (nvalid < kST || lo_valid > 0) {  // the row's last stage, or the window's first
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int e = 0; e < 2; ++e)
-            if (nt * 8 + 2 * c4 + e >= nvalid) s[nt][2 * rr + e] = -INFINITY;
+          for (int e = 0; e < 2; ++e) {
+            const int t = nt * 8 + 2 * c4 + e;
+            if (t >= nvalid || t < lo_valid) s[nt][2 * rr + e] = -INFINITY;
+          }
       }
       float mx = fmaxf(fmaxf(s[0][2 * rr], s[0][2 * rr + 1]), fmaxf(s[1][2 * rr], s[1][2 * rr + 1]));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));

@@ -69,7 +69,7 @@ extern "C" pkv_status pkv_paged_attention_decode_noalloc(
   size_t ws_bytes = 0;
   bool nothing = false;
   pkv_status st = decode_prepare(out, query, key_cache, value_cache, block_tables, context_lens, num_kv_heads,
-                                 scale, block_size, max_blocks_per_seq, &p, &ws_bytes, &nothing);
+                                 scale, block_size, max_blocks_per_seq, 0, &p, &ws_bytes, &nothing);
   if (st || nothing) return st;
   if (ws_bytes > kStaticScratchBytes) {
     char msg[256];

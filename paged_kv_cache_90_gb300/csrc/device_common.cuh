@@ -22,6 +22,10 @@ constexpr unsigned int kErrCopyPair = 0x4u;
 constexpr unsigned int kErrContextLen = 0x8u;
 constexpr unsigned int kErrTimeout = 0x10u;
 
+// First attended position of a context of L tokens under a sliding window of W
+// positions (W <= 0: no window).
+__host__ __device__ __forceinline__ int window_start(int L, int W) { return (W > 0 && L > W) ? L - W : 0; }
+
 // ---- storage types ------------------------------------------------------------
 struct F32 { using storage = float; static constexpr int bytes = 4; };
 struct BF16 { using storage = uint16_t; static constexpr int bytes = 2; };

@@ -216,8 +216,8 @@ void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 pkv_status decode_prepare(const pkv_tensor* out, const pkv_tensor* query, const pkv_tensor* key_cache,
                           const pkv_tensor* value_cache, const pkv_tensor* block_tables,
                           const pkv_tensor* context_lens, int32_t num_kv_heads, float scale,
-                          int32_t block_size, int32_t max_blocks_per_seq, DecodeParams* pp,
-                          size_t* ws_bytes, bool* nothing_to_do) {
+                          int32_t block_size, int32_t max_blocks_per_seq, int32_t sliding_window,
+                          DecodeParams* pp, size_t* ws_bytes, bool* nothing_to_do) {
   *ws_bytes = 0;
   *nothing_to_do = false;
   pkv_status st;
@@ -262,6 +262,7 @@ pkv_status decode_prepare(const pkv_tensor* out, const pkv_tensor* query, const 
   if (S > 65535 || Hq > 65535)
     return fail(PKV_ERR_UNSUPPORTED, "num_seqs and num_heads must be <= 65535");
   if (!(std::isfinite(scale))) return fail(PKV_ERR_INVALID_ARG, "scale must be finite");
+  if (sliding_window < 0) return fail(PKV_ERR_INVALID_ARG, "sliding_window must be >= 0 (0: no window)");
   if (NB < 1) return fail(PKV_ERR_INVALID_ARG, "the cache holds no block");
 
   const int pt = choose_partition_tokens(max_ctx);
@@ -304,6 +305,7 @@ pkv_status decode_prepare(const pkv_tensor* out, const pkv_tensor* query, const 
   const float kscale = key_cache->dtype == PKV_FP8_E4M3 ? key_cache->scale : 1.0f;
   p.qk_scale_log2 = float(double(scale) * 1.4426950408889634 * double(kscale));
   p.v_scale = value_cache->dtype == PKV_FP8_E4M3 ? value_cache->scale : 1.0f;
+  p.sliding_window = sliding_window;
   p.partition_tokens = pt;
   p.max_partitions = int(parts);
   p.err = s->err;
@@ -536,11 +538,22 @@ pkv_status pkv_paged_attention_decode(const pkv_tensor* out, const pkv_tensor* q
                                       const pkv_tensor* context_lens, int32_t num_kv_heads,
                                       float scale, int32_t block_size,
                                       int32_t max_blocks_per_seq, pkv_stream stream) {
+  return pkv_paged_attention_decode_window(out, query, key_cache, value_cache, block_tables, context_lens,
+                                           num_kv_heads, scale, block_size, max_blocks_per_seq, 0, stream);
+}
+
+pkv_status pkv_paged_attention_decode_window(const pkv_tensor* out, const pkv_tensor* query,
+                                             const pkv_tensor* key_cache, const pkv_tensor* value_cache,
+                                             const pkv_tensor* block_tables, const pkv_tensor* context_lens,
+                                             int32_t num_kv_heads, float scale, int32_t block_size,
+                                             int32_t max_blocks_per_seq, int32_t sliding_window,
+                                             pkv_stream stream) {
   DecodeParams p;
   size_t ws_bytes = 0;
   bool nothing = false;
   pkv_status st = decode_prepare(out, query, key_cache, value_cache, block_tables, context_lens, num_kv_heads,
-                                 scale, block_size, max_blocks_per_seq, &p, &ws_bytes, &nothing);
+                                 scale, block_size, max_blocks_per_seq, sliding_window, &p, &ws_bytes,
+                                 &nothing);
   if (st || nothing) return st;
   DeviceState* s;
   if ((st = device_state(&s))) return st;
@@ -569,7 +582,8 @@ pkv_status pkv_decode_step(const pkv_tensor* out, const pkv_tensor* query, const
                            const pkv_tensor* value, const pkv_tensor* slot_mapping, const pkv_tensor* key_cache,
                            const pkv_tensor* value_cache, const pkv_tensor* block_tables,
                            const pkv_tensor* context_lens, int32_t num_kv_heads, float scale,
-                           int32_t block_size, int32_t max_blocks_per_seq, pkv_stream stream) {
+                           int32_t block_size, int32_t max_blocks_per_seq, int32_t sliding_window,
+                           pkv_stream stream) {
   // every check of both calls before anything is queued
   CacheWriteParams wp;
   bool no_write = false, no_decode = false;
@@ -578,7 +592,7 @@ pkv_status pkv_decode_step(const pkv_tensor* out, const pkv_tensor* query, const
   DecodeParams p;
   size_t ws_bytes = 0;
   st = decode_prepare(out, query, key_cache, value_cache, block_tables, context_lens, num_kv_heads, scale,
-                      block_size, max_blocks_per_seq, &p, &ws_bytes, &no_decode);
+                      block_size, max_blocks_per_seq, sliding_window, &p, &ws_bytes, &no_decode);
   if (st || g_opt_dry_run.load()) return st;
   DeviceState* s;
   if ((st = device_state(&s))) return st;

@@ -72,6 +72,7 @@ struct DecodeParams {
   int group;                 // num_heads / num_kv_heads
   float qk_scale_log2;       // scale * log2(e) * k_scale
   float v_scale;
+  int sliding_window;        // attend to the last W positions only (0: all)
   int partition_tokens;      // multiple of 256
   int max_partitions;        // ceil(max_blocks_per_seq * block_size / partition_tokens)
   int64_t partial_rows;      // rows of the partial arrays (0: none)
@@ -110,8 +111,8 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
 pkv_status decode_prepare(const pkv_tensor* out, const pkv_tensor* query, const pkv_tensor* key_cache,
                           const pkv_tensor* value_cache, const pkv_tensor* block_tables,
                           const pkv_tensor* context_lens, int32_t num_kv_heads, float scale,
-                          int32_t block_size, int32_t max_blocks_per_seq, DecodeParams* p,
-                          size_t* ws_bytes, bool* nothing_to_do);
+                          int32_t block_size, int32_t max_blocks_per_seq, int32_t sliding_window,
+                          DecodeParams* p, size_t* ws_bytes, bool* nothing_to_do);
 void decode_set_workspace(DecodeParams* p, void* ws);
 // Maps a launch result to a status (and, with debug sync on, checks the device).
 pkv_status finish_launch(cudaError_t launch_err, cudaStream_t stream, const char* what);

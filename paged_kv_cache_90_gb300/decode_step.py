@@ -67,11 +67,11 @@ def run_decode_step(w: Workload, key_cache, value_cache, st: DeviceStep, out, st
     if joint:
         binding.decode_step(out, st.query, st.new_key, st.new_value, st.slot_mapping, key_cache, value_cache,
                             st.block_tables, st.context_lens, w.num_kv_heads, w.scale, w.block_size,
-                            w.max_blocks_per_seq, w.k_scale, w.v_scale, stream)
+                            w.max_blocks_per_seq, w.k_scale, w.v_scale, stream, w.sliding_window)
         return
     if st.slot_mapping.numel():
         binding.reshape_and_cache(st.new_key, st.new_value, key_cache, value_cache, st.slot_mapping,
                                   w.k_scale, w.v_scale, stream)
     binding.paged_attention_decode(out, st.query, key_cache, value_cache, st.block_tables,
                                    st.context_lens, w.num_kv_heads, w.scale, w.block_size,
-                                   w.max_blocks_per_seq, w.k_scale, w.v_scale, stream)
+                                   w.max_blocks_per_seq, w.k_scale, w.v_scale, stream, w.sliding_window)

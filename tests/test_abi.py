@@ -82,6 +82,8 @@ def test_decode_step_validation(dry):
 def test_decode_validation(dry):
     ok = _decode_args()
     assert _status(binding.paged_attention_decode, **ok) == 0
+    assert _status(binding.paged_attention_decode, **ok, sliding_window=5) == 0
+    assert _status(binding.paged_attention_decode, **ok, sliding_window=-3) == 1
     assert _status(binding.paged_attention_decode, **_decode_args(kv=torch.float8_e4m3fn),
                    k_scale=0.01, v_scale=0.02) == 0
     assert _status(binding.paged_attention_decode, **_decode_args(dtype=torch.float32, kv=torch.float32, D=64)) == 0

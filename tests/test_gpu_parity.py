@@ -80,15 +80,20 @@ def weighted_abs_values(w, st, kc, vc):
     S, hq, d = st.query.shape
     hk, bs = w.num_kv_heads, w.block_size
     g = hq // hk
+    W = w.sliding_window
     out = torch.zeros(S, hq, d, dtype=torch.float64)
     for s in range(S):
         L = int(st.context_lens[s])
         if L == 0:
             continue
-        n = -(-L // bs)
-        blocks = st.block_tables[s, :n].long()
-        K = gather_blocks(kc, blocks).double().permute(1, 0, 2, 3).reshape(hk, n * bs, d)[:, :L] * w.k_scale
-        V = gather_blocks(vc, blocks).double().permute(1, 0, 2, 3).reshape(hk, n * bs, d)[:, :L].abs() * w.v_scale
+        lo = max(0, L - W) if W > 0 else 0       # first attended position
+        b0 = lo // bs                            # blocks before it may be released (-1)
+        n = -(-L // bs) - b0
+        blocks = st.block_tables[s, b0:b0 + n].long()
+        K = gather_blocks(kc, blocks).double().permute(1, 0, 2, 3).reshape(hk, n * bs, d)[:, lo - b0 * bs:L - b0 * bs]
+        V = gather_blocks(vc, blocks).double().permute(1, 0, 2, 3).reshape(hk, n * bs, d)[:, lo - b0 * bs:L - b0 * bs]
+        K = K * w.k_scale
+        V = V.abs() * w.v_scale
         q = st.query[s].double().view(hk, g, d)
         p = torch.softmax(w.scale * q @ K.transpose(1, 2), dim=-1)
         out[s] = (p @ V).reshape(hq, d)
@@ -193,6 +198,37 @@ def test_continuous_batching_small(bs, kv, kernel):
 @pytest.mark.parametrize("bs", [8, 16, 32])
 def test_continuous_batching_full(bs, kv, kernel):
     check_workload(wl.continuous_batching(block_size=bs, kv_dtype=kv))
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("window", [1, 7, 16, 17, 100])
+def test_sliding_window_small(bs, window, kernel):
+    """Windows shorter than, around and beyond a stage / block; blocks before each
+    window released (table entries -1, slots NaN) and handed out again."""
+    check_workload(wl.sliding_window_decode(seed=60 + window + bs, num_seqs=12, window=window, block_size=bs,
+                                            num_steps=2, len_range=(1, 600), poison=True))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_sliding_window_full(kv, kernel):
+    """8 sequences of 32768 tokens, window 4096 (the benchmark's sliding-window layer)."""
+    check_workload(wl.sliding_window_decode(kv_dtype=kv))
+
+
+def test_window_covering_every_context_is_the_plain_decode(kernel):
+    """A window no shorter than any context gives the plain decode's bits."""
+    w = wl.llama3_8b_decode(seed=61, num_seqs=8, len_range=(1, 900))
+    dw = DeviceWorkload(w)
+    dw.run_step(0)
+    st = dw.steps[0]
+    args = (st.query, dw.key_cache, dw.value_cache, st.block_tables, st.context_lens, w.num_kv_heads, w.scale,
+            w.block_size, w.max_blocks_per_seq)
+    plain = binding.paged_attention_decode(torch.empty_like(dw.out), *args).clone()
+    for window in (901, 5000):
+        got = binding.paged_attention_decode(torch.empty_like(dw.out), *args, sliding_window=window)
+        torch.cuda.synchronize()
+        assert torch.equal(got, plain)
+    assert binding.read_device_errors() == 0
 
 
 # --- edge cases -----------------------------------------------------------------
