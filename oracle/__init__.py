@@ -59,6 +59,12 @@ def _load():
             lib.orc_paged_attention_decode_window.restype = i32
             lib.orc_paged_attention_decode_window.argtypes = (
                 [vp, vp, i32, vp, vp, i32, dbl, dbl, vp, vp] + [i64] * 10 + [dbl, i64, i32])
+            lib.orc_paged_attention_decode_ex.restype = i32
+            lib.orc_paged_attention_decode_ex.argtypes = (
+                [vp, vp, i32, vp, vp, i32, dbl, dbl, vp, vp, vp, vp] + [i64] * 10 + [dbl, i64, i32])
+            lib.orc_reshape_and_cache_ex.restype = i32
+            lib.orc_reshape_and_cache_ex.argtypes = (
+                [vp, vp, i32, vp, vp, i32, ctypes.c_float, ctypes.c_float, vp, vp, vp, vp, vp] + [i64] * 8)
             lib.orc_reshape_and_cache.restype = i32
             lib.orc_reshape_and_cache.argtypes = (
                 [vp, vp, i32, vp, vp, i32, ctypes.c_float, ctypes.c_float, vp] + [i64] * 8)
@@ -89,11 +95,18 @@ def max_threads() -> int:
     return int(_load().orc_max_threads())
 
 
+def _head_scales(x):
+    """Per-KV-head scales as a contiguous float32 CPU tensor (or None)."""
+    return None if x is None else torch.as_tensor(x, dtype=torch.float32).detach().cpu().contiguous()
+
+
 def paged_attention_decode(query, key_cache, value_cache, block_tables, context_lens,
                            scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
-                           num_threads: int = 1, sliding_window: int = 0) -> torch.Tensor:
+                           num_threads: int = 1, sliding_window: int = 0,
+                           k_head_scales=None, v_head_scales=None) -> torch.Tensor:
     """Decode attention in fp64; returns a float64 tensor ``[S, Hq, D]``.  With
-    ``sliding_window`` W > 0 each sequence attends to its last W positions only."""
+    ``sliding_window`` W > 0 each sequence attends to its last W positions only;
+    ``k_head_scales`` / ``v_head_scales`` ([Hk]) replace the per-tensor scales."""
     lib = _load()
     q = _cpu(query)
     bt = _cpu(block_tables).to(torch.int32)
@@ -105,9 +118,14 @@ def paged_attention_decode(query, key_cache, value_cache, block_tables, context_
     cs = _cache_strides(key_cache)
     out = torch.zeros(s, hq, d, dtype=torch.float64)
     mb = bt.shape[1] if bt.dim() == 2 else 0
-    rc = lib.orc_paged_attention_decode_window(
+    ksh, vsh = _head_scales(k_head_scales), _head_scales(v_head_scales)
+    for t in (ksh, vsh):
+        if t is not None and t.numel() != hk:
+            raise ValueError("head scales must have one entry per KV head")
+    rc = lib.orc_paged_attention_decode_ex(
         out.data_ptr(), q.data_ptr(), _CODES[q.dtype], key_cache.data_ptr(),
         value_cache.data_ptr(), _CODES[key_cache.dtype], float(k_scale), float(v_scale),
+        None if ksh is None else ksh.data_ptr(), None if vsh is None else vsh.data_ptr(),
         bt.data_ptr(), cl.data_ptr(), s, hq, hk, d, bs, nb, mb, cs[0], cs[1], cs[2],
         float(scale), int(sliding_window), int(num_threads))
     if rc != 0:
@@ -116,8 +134,11 @@ def paged_attention_decode(query, key_cache, value_cache, block_tables, context_
 
 
 def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping,
-                      k_scale: float = 1.0, v_scale: float = 1.0) -> None:
-    """Write new tokens' K/V into the caches in place (CPU tensors)."""
+                      k_scale: float = 1.0, v_scale: float = 1.0,
+                      k_head_scales=None, v_head_scales=None, k_amax=None, v_amax=None) -> None:
+    """Write new tokens' K/V into the caches in place (CPU tensors).  Per-head scales
+    ([Hk]) replace the per-tensor ones; ``k_amax`` / ``v_amax`` (float64 [Hk] CPU
+    tensors) are raised to the largest |x| written for each head."""
     lib = _load()
     k, v = _cpu(key), _cpu(value)
     sm = _cpu(slot_mapping).to(torch.int64)
@@ -126,10 +147,17 @@ def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping,
     if hk2 != hk or d2 != d:
         raise ValueError("key / cache shapes disagree")
     cs = _cache_strides(key_cache)
-    rc = lib.orc_reshape_and_cache(
+    ksh, vsh = _head_scales(k_head_scales), _head_scales(v_head_scales)
+    for a in (k_amax, v_amax):
+        if a is not None and (a.dtype != torch.float64 or a.device.type != "cpu" or a.numel() != hk
+                              or not a.is_contiguous()):
+            raise ValueError("amax outputs must be contiguous float64 CPU tensors of num_kv_heads entries")
+    rc = lib.orc_reshape_and_cache_ex(
         k.data_ptr(), v.data_ptr(), _CODES[k.dtype], key_cache.data_ptr(), value_cache.data_ptr(),
-        _CODES[key_cache.dtype], float(k_scale), float(v_scale), sm.data_ptr(),
-        t, hk, d, bs, nb, cs[0], cs[1], cs[2])
+        _CODES[key_cache.dtype], float(k_scale), float(v_scale),
+        None if ksh is None else ksh.data_ptr(), None if vsh is None else vsh.data_ptr(),
+        None if k_amax is None else k_amax.data_ptr(), None if v_amax is None else v_amax.data_ptr(),
+        sm.data_ptr(), t, hk, d, bs, nb, cs[0], cs[1], cs[2])
     if rc != 0:
         raise ValueError(f"oracle reshape_and_cache failed with status {rc}")
 
@@ -176,9 +204,10 @@ def run_workload_step(w, step_index: int, key_cache, value_cache, num_threads: i
     if st.cow_pairs.numel():
         copy_blocks(key_cache, st.cow_pairs)
         copy_blocks(value_cache, st.cow_pairs)
+    ksh, vsh = getattr(w, "k_head_scales", None), getattr(w, "v_head_scales", None)
     if st.slot_mapping.numel():
         reshape_and_cache(st.new_key, st.new_value, key_cache, value_cache, st.slot_mapping,
-                          w.k_scale, w.v_scale)
+                          w.k_scale, w.v_scale, ksh, vsh)
     return paged_attention_decode(st.query, key_cache, value_cache, st.block_tables,
                                   st.context_lens, w.scale, w.k_scale, w.v_scale, num_threads,
-                                  getattr(w, "sliding_window", 0))
+                                  getattr(w, "sliding_window", 0), ksh, vsh)

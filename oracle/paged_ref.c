@@ -49,7 +49,13 @@
  *      key_pool[block_table[pos // block_size], pos % block_size] = key.)
  *     encode is a bit copy when source and cache dtypes agree; for an 8-bit cache it
  *     is e4m3(satfinite, round-to-nearest-even)(x / scale) with x / scale evaluated in
- *     binary32 (one per-tensor scale for K, one for V).
+ *     binary32 (ultralytics.com glossary "PagedAttention", section "관련 기법": an
+ *     FP8 cache stores keys and values in 8 bits, about half the memory of 16 bits).
+ *     The scale is one per tensor for K and one for V, or one per KV head when the
+ *     per-head scale arrays are given (then decode multiplies head h's codes by its
+ *     own scale too).  On request the write also reports, per KV head, the largest
+ *     |x| of the values it wrote (tokens with slot < 0 excluded) raised into amax[h],
+ *     so a caller can set scales as amax / 448.
  *
  *  3. Copy-on-write ("copy_blocks").  For each pair (src, dst): the whole physical
  *     block dst (all KV heads) becomes a byte copy of block src (vasteelab.pages.dev,
@@ -179,11 +185,13 @@ void orc_bf16_decode_array(const uint16_t* bits, double* out, int64_t n) {
 
 /* Cache element (block b, KV head k, offset o, dim d) sits at
  *   b * cs_block + k * cs_head + o * cs_token + d      (elements). */
-int orc_paged_attention_decode_window(
+int orc_paged_attention_decode_ex(
     double* out,                                 /* [S, Hq, D] */
     const void* query, int q_dtype,              /* [S, Hq, D], contiguous */
     const void* key_cache, const void* value_cache, int kv_dtype,
     double k_scale, double v_scale,              /* multiply the stored values */
+    const float* k_head_scales,                  /* [Hk] or NULL: then k_scale for every head */
+    const float* v_head_scales,                  /* [Hk] or NULL: then v_scale */
     const int32_t* block_tables,                 /* [S, MB] */
     const int32_t* context_lens,                 /* [S] */
     int64_t num_seqs, int64_t num_heads, int64_t num_kv_heads, int64_t head_dim,
@@ -206,6 +214,8 @@ int orc_paged_attention_decode_window(
 #endif
   for (int64_t w = 0; w < work; ++w) {
     int64_t s = w / num_kv_heads, k = w % num_kv_heads;
+    double ks = k_head_scales ? (double)k_head_scales[k] : k_scale;
+    double vs = v_head_scales ? (double)v_head_scales[k] : v_scale;
     int64_t Lctx = context_lens[s];
     /* attended positions j0 .. Lctx-1; K, V, z below are indexed from j0 */
     int64_t j0 = (sliding_window > 0 && Lctx > sliding_window) ? Lctx - sliding_window : 0;
@@ -232,8 +242,8 @@ int orc_paged_attention_decode_window(
       }
       base = phys * cs_block + k * cs_head + (j % block_size) * cs_token;
       for (int64_t d = 0; d < head_dim; ++d) {
-        K[i * head_dim + d] = orc_load(key_cache, base + d, kv_dtype) * k_scale;
-        V[i * head_dim + d] = orc_load(value_cache, base + d, kv_dtype) * v_scale;
+        K[i * head_dim + d] = orc_load(key_cache, base + d, kv_dtype) * ks;
+        V[i * head_dim + d] = orc_load(value_cache, base + d, kv_dtype) * vs;
       }
     }
     for (int64_t h = k * group; h < (k + 1) * group; ++h) {
@@ -273,7 +283,21 @@ int orc_paged_attention_decode_window(
   return status;
 }
 
-/* Decode without a window. */
+/* Decode with per-tensor scales, with and without a window. */
+int orc_paged_attention_decode_window(
+    double* out, const void* query, int q_dtype, const void* key_cache, const void* value_cache,
+    int kv_dtype, double k_scale, double v_scale, const int32_t* block_tables,
+    const int32_t* context_lens, int64_t num_seqs, int64_t num_heads, int64_t num_kv_heads,
+    int64_t head_dim, int64_t block_size, int64_t num_blocks, int64_t max_blocks_per_seq,
+    int64_t cs_block, int64_t cs_head, int64_t cs_token, double scale, int64_t sliding_window,
+    int num_threads) {
+  return orc_paged_attention_decode_ex(
+      out, query, q_dtype, key_cache, value_cache, kv_dtype, k_scale, v_scale, NULL, NULL,
+      block_tables, context_lens, num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+      num_blocks, max_blocks_per_seq, cs_block, cs_head, cs_token, scale, sliding_window,
+      num_threads);
+}
+
 int orc_paged_attention_decode(
     double* out, const void* query, int q_dtype, const void* key_cache, const void* value_cache,
     int kv_dtype, double k_scale, double v_scale, const int32_t* block_tables,
@@ -288,10 +312,12 @@ int orc_paged_attention_decode(
 
 /* ---- 2. cache write -------------------------------------------------------------- */
 
-int orc_reshape_and_cache(
+int orc_reshape_and_cache_ex(
     const void* key, const void* value, int src_dtype,   /* [T, Hk, D], contiguous */
     void* key_cache, void* value_cache, int cache_dtype,
     float k_scale, float v_scale,                         /* used by an e4m3 cache */
+    const float* k_head_scales, const float* v_head_scales, /* [Hk] or NULL */
+    double* k_amax, double* v_amax,                       /* [Hk] raised to max |x|, or NULL */
     const int64_t* slot_mapping,                          /* [T] */
     int64_t num_tokens, int64_t num_kv_heads, int64_t head_dim, int64_t block_size,
     int64_t num_blocks, int64_t cs_block, int64_t cs_head, int64_t cs_token) {
@@ -311,6 +337,13 @@ int orc_reshape_and_cache(
     for (int64_t h = 0; h < num_kv_heads; ++h) {
       int64_t src = (t * num_kv_heads + h) * head_dim;
       int64_t dst = blk * cs_block + h * cs_head + off * cs_token;
+      float ksh = k_head_scales ? k_head_scales[h] : k_scale;
+      float vsh = v_head_scales ? v_head_scales[h] : v_scale;
+      for (int64_t d = 0; d < head_dim; ++d) {
+        double ak = fabs(orc_load(key, src + d, src_dtype)), av = fabs(orc_load(value, src + d, src_dtype));
+        if (k_amax && (isnan(ak) || ak > k_amax[h])) k_amax[h] = ak;  /* a NaN stays */
+        if (v_amax && (isnan(av) || av > v_amax[h])) v_amax[h] = av;
+      }
       if (src_dtype == cache_dtype) {
         memcpy((char*)key_cache + dst * cb, (const char*)key + src * sb, (size_t)(head_dim * sb));
         memcpy((char*)value_cache + dst * cb, (const char*)value + src * sb, (size_t)(head_dim * sb));
@@ -319,8 +352,8 @@ int orc_reshape_and_cache(
           /* binary32 division, then round to e4m3 */
           float xk = (float)orc_load(key, src + d, src_dtype);
           float xv = (float)orc_load(value, src + d, src_dtype);
-          float yk = xk / k_scale;
-          float yv = xv / v_scale;
+          float yk = xk / ksh;
+          float yv = xv / vsh;
           ((uint8_t*)key_cache)[dst + d] = orc_f32_to_e4m3(yk);
           ((uint8_t*)value_cache)[dst + d] = orc_f32_to_e4m3(yv);
         }
@@ -328,6 +361,17 @@ int orc_reshape_and_cache(
     }
   }
   return ORC_OK;
+}
+
+int orc_reshape_and_cache(
+    const void* key, const void* value, int src_dtype, void* key_cache, void* value_cache,
+    int cache_dtype, float k_scale, float v_scale, const int64_t* slot_mapping, int64_t num_tokens,
+    int64_t num_kv_heads, int64_t head_dim, int64_t block_size, int64_t num_blocks,
+    int64_t cs_block, int64_t cs_head, int64_t cs_token) {
+  return orc_reshape_and_cache_ex(key, value, src_dtype, key_cache, value_cache, cache_dtype,
+                                  k_scale, v_scale, NULL, NULL, NULL, NULL, slot_mapping,
+                                  num_tokens, num_kv_heads, head_dim, block_size, num_blocks,
+                                  cs_block, cs_head, cs_token);
 }
 
 /* ---- 3. copy-on-write ------------------------------------------------------------ */

@@ -62,6 +62,8 @@ class Workload:
     steps: List[DecodeStep] = field(default_factory=list)
     seed: int = 0
     sliding_window: int = 0      # attend to the last W positions only (0: all)
+    k_head_scales: Optional[torch.Tensor] = None   # 8-bit cache: one fp32 scale per KV head
+    v_head_scales: Optional[torch.Tensor] = None
 
     @property
     def num_seqs(self) -> int:
@@ -104,16 +106,31 @@ def _amax(x: torch.Tensor) -> float:
     return m
 
 
-def _make_pool(nb, hk, bs, d, kv_dtype: str, g: torch.Generator):
-    """Random K and V pools (every slot holds N(0,1)-shaped data, used or not)."""
+def _make_pool(nb, hk, bs, d, kv_dtype: str, g: torch.Generator, head_spread: float = 0.0):
+    """Random K and V pools (every slot holds N(0,1)-shaped data, used or not).
+    ``head_spread`` > 0 (8-bit caches) multiplies KV head h's data by
+    2^(head_spread * (h / (hk - 1) - 1/2)) and returns one scale per head (amax / 448)
+    as the last two values; otherwise those are None."""
     src = torch.bfloat16 if kv_dtype == "e4m3" else DTYPES[kv_dtype]
     k = _randn((nb, hk, bs, d), src, g)
     v = _randn((nb, hk, bs, d), src, g)
     if kv_dtype != "e4m3":
-        return k, v, 1.0, 1.0
+        return k, v, 1.0, 1.0, None, None
+    if head_spread:
+        mult = torch.tensor([2.0 ** (head_spread * (h / max(hk - 1, 1) - 0.5)) for h in range(hk)])
+        k = (k.float() * mult.view(1, hk, 1, 1)).to(src)
+        v = (v.float() * mult.view(1, hk, 1, 1)).to(src)
+        ksh = torch.tensor([_amax(k[:, h]) / _E4M3_MAX for h in range(hk)], dtype=torch.float32)
+        vsh = torch.tensor([_amax(v[:, h]) / _E4M3_MAX for h in range(hk)], dtype=torch.float32)
+        kq = torch.empty(k.shape, dtype=torch.float8_e4m3fn)
+        vq = torch.empty(v.shape, dtype=torch.float8_e4m3fn)
+        for h in range(hk):
+            kq[:, h] = _quantize_e4m3(k[:, h], float(ksh[h]))
+            vq[:, h] = _quantize_e4m3(v[:, h], float(vsh[h]))
+        return kq, vq, 1.0, 1.0, ksh, vsh
     k_scale = float(torch.tensor(_amax(k) / _E4M3_MAX, dtype=torch.float32))
     v_scale = float(torch.tensor(_amax(v) / _E4M3_MAX, dtype=torch.float32))
-    return _quantize_e4m3(k, k_scale), _quantize_e4m3(v, v_scale), k_scale, v_scale
+    return _quantize_e4m3(k, k_scale), _quantize_e4m3(v, v_scale), k_scale, v_scale, None, None
 
 
 def _step(mgr: BlockManager, seq_ids: Sequence, g: torch.Generator, hq: int, hk: int,
@@ -167,19 +184,21 @@ def _poison(cache: torch.Tensor, occupied: torch.Tensor) -> None:
         cache[~keep] = float("nan")
 
 
-def _finish(name, seed, hq, hk, d, bs, nb, mb, kc, vc, ks, vs, steps, scale=None, window=0) -> Workload:
+def _finish(name, seed, hq, hk, d, bs, nb, mb, kc, vc, ks, vs, steps, scale=None, window=0,
+            ksh=None, vsh=None) -> Workload:
     return Workload(name=name, num_heads=hq, num_kv_heads=hk, head_dim=d, block_size=bs,
                     num_blocks=nb, max_blocks_per_seq=mb,
                     scale=float(scale if scale is not None else 1.0 / math.sqrt(d)),
                     k_scale=ks, v_scale=vs, key_cache=kc, value_cache=vc, steps=steps, seed=seed,
-                    sliding_window=int(window))
+                    sliding_window=int(window), k_head_scales=ksh, v_head_scales=vsh)
 
 
 def variable_length_decode(name: str, seed: int, lengths: Sequence[int], num_heads: int,
                            num_kv_heads: int, head_dim: int, block_size: int, kv_dtype: str,
                            q_dtype: str = "bf16", num_steps: int = 1, pool_slack: float = 0.10,
                            num_blocks: Optional[int] = None, poison: bool = False,
-                           scale: Optional[float] = None, window: int = 0) -> Workload:
+                           scale: Optional[float] = None, window: int = 0,
+                           head_spread: float = 0.0) -> Workload:
     """Sequences with the given context lengths *after* the first append.
 
     The pool holds the needed blocks (for all ``num_steps`` appends) plus
@@ -187,6 +206,8 @@ def variable_length_decode(name: str, seed: int, lengths: Sequence[int], num_hea
     scattered set of physical ids.  Each step appends one token per sequence.  With a
     sliding ``window``, blocks wholly before each sequence's window are released (their
     table entries -1; with ``poison`` their slots hold NaN) and may be handed out again.
+    ``head_spread`` > 0 with an 8-bit cache gives the KV heads different magnitudes and
+    one scale per head.
     """
     g = torch.Generator().manual_seed(seed)
     lengths = [int(x) for x in lengths]
@@ -212,7 +233,7 @@ def variable_length_decode(name: str, seed: int, lengths: Sequence[int], num_hea
         for _ in range(L - 1):
             mgr.append_token(sid)
             mgr.release_outside_window(sid, window - 1)
-    kc, vc, ks, vs = _make_pool(nb, num_kv_heads, block_size, head_dim, kv_dtype, g)
+    kc, vc, ks, vs, ksh, vsh = _make_pool(nb, num_kv_heads, block_size, head_dim, kv_dtype, g, head_spread)
     if poison:
         occ = _occupied_slots(mgr)
         _poison(kc, occ)
@@ -220,9 +241,15 @@ def variable_length_decode(name: str, seed: int, lengths: Sequence[int], num_hea
     src = torch.bfloat16 if kv_dtype == "e4m3" else DTYPES[kv_dtype]
     steps = [_step(mgr, seq_ids, g, num_heads, num_kv_heads, head_dim, DTYPES[q_dtype], src, mb, window)
              for _ in range(num_steps)]
+    if head_spread and ksh is not None:  # the new tokens have their head's magnitude too
+        mult = torch.tensor([2.0 ** (head_spread * (h / max(num_kv_heads - 1, 1) - 0.5))
+                             for h in range(num_kv_heads)]).view(1, num_kv_heads, 1)
+        for st in steps:
+            st.new_key = (st.new_key.float() * mult).to(src)
+            st.new_value = (st.new_value.float() * mult).to(src)
     mgr.check_structure()
     return _finish(name, seed, num_heads, num_kv_heads, head_dim, block_size, nb, mb,
-                   kc, vc, ks, vs, steps, scale, window)
+                   kc, vc, ks, vs, steps, scale, window, ksh, vsh)
 
 
 # --- the five workloads -----------------------------------------------------------
@@ -284,16 +311,18 @@ def long_context(seed: int = 3, block_size: int = 16, num_seqs: int = 8,
 
 def continuous_batching(seed: int = 5, block_size: int = 16, kv_dtype: str = "bf16",
                         num_seqs: int = 256, num_steps: int = 10, median: float = 512.0,
-                        sigma: float = 1.0, cap: int = 8192, poison: bool = False) -> Workload:
+                        sigma: float = 1.0, cap: int = 8192, poison: bool = False,
+                        head_spread: float = 0.0) -> Workload:
     """Continuous-batching mix: lengths round(lognormal(ln median, sigma)) clamped to
     [1, cap], ``num_steps`` decode steps each appending one token per sequence (a new
-    block is taken whenever a sequence's last block is full)."""
+    block is taken whenever a sequence's last block is full).  ``head_spread`` > 0 with
+    an 8-bit cache: KV heads of different magnitudes, one scale per head."""
     g = torch.Generator().manual_seed(seed)
     z = torch.randn(num_seqs, generator=g, dtype=torch.float64)
     lens = torch.exp(math.log(median) + sigma * z).round().clamp(1, cap).long().tolist()
     return variable_length_decode(f"continuous_batching_s{num_seqs}_bs{block_size}_{kv_dtype}",
                                   seed, lens, 32, 8, 128, block_size, kv_dtype,
-                                  num_steps=num_steps, poison=poison)
+                                  num_steps=num_steps, poison=poison, head_spread=head_spread)
 
 
 def shared_prefix_cow(seed: int = 4, num_groups: int = 32, group_size: int = 4,
@@ -332,7 +361,7 @@ def shared_prefix_cow(seed: int = 4, num_groups: int = 32, group_size: int = 4,
             seq_ids.append((gi, j))
     mgr.free_sequence("prefix")
     mb = prefix_blocks + max(blocks_needed(u + 1, block_size) for u in us)
-    kc, vc, ks, vs = _make_pool(nb, 8, block_size, 128, "bf16", g)
+    kc, vc, ks, vs, _, _ = _make_pool(nb, 8, block_size, 128, "bf16", g)
     if poison:
         occ = _occupied_slots(mgr)
         _poison(kc, occ)

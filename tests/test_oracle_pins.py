@@ -488,3 +488,74 @@ def test_sliding_window_workload_releases_and_reuses_blocks():
         assert torch.isfinite(out).all()
     # the pool is sized for the windows, far below the full contexts
     assert w.num_blocks < sum(-(-int(L) // 8) for L in w.steps[-1].context_lens)
+
+
+# --- per-head 8-bit scales and the amax report -----------------------------------------
+
+def _fp8_heads(seed=71, spread=3.0):
+    return wl.variable_length_decode("h", seed, [1, 9, 40, 77], 8, 4, 16, 8, "e4m3", num_steps=2,
+                                     head_spread=spread)
+
+
+def test_equal_head_scales_are_the_per_tensor_scale():
+    """Per-head scales all equal to s give the per-tensor-s bytes and outputs."""
+    w = wl.variable_length_decode("t", 72, [3, 17, 50], 8, 4, 16, 8, "e4m3", num_steps=2)
+    hk = w.num_kv_heads
+    kc1, vc1 = w.key_cache.clone(), w.value_cache.clone()
+    kc2, vc2 = w.key_cache.clone(), w.value_cache.clone()
+    ksh = torch.full((hk,), w.k_scale)
+    vsh = torch.full((hk,), w.v_scale)
+    for st in w.steps:
+        oracle.reshape_and_cache(st.new_key, st.new_value, kc1, vc1, st.slot_mapping, w.k_scale, w.v_scale)
+        oracle.reshape_and_cache(st.new_key, st.new_value, kc2, vc2, st.slot_mapping, 1.0, 1.0, ksh, vsh)
+        assert torch.equal(kc1.view(torch.uint8), kc2.view(torch.uint8))
+        assert torch.equal(vc1.view(torch.uint8), vc2.view(torch.uint8))
+        a = oracle.paged_attention_decode(st.query, kc1, vc1, st.block_tables, st.context_lens, w.scale,
+                                          w.k_scale, w.v_scale)
+        b = oracle.paged_attention_decode(st.query, kc2, vc2, st.block_tables, st.context_lens, w.scale,
+                                          1.0, 1.0, k_head_scales=ksh, v_head_scales=vsh)
+        assert torch.equal(a, b)
+
+
+def test_head_scales_act_head_by_head():
+    """With different scales per KV head, the write and the decode equal, bit for bit,
+    the per-tensor write and decode run on each KV head alone with its own scale (a
+    one-head slice of the cache and of the query group)."""
+    w = _fp8_heads()
+    hk, g = w.num_kv_heads, w.num_heads // w.num_kv_heads
+    assert len(set(w.k_head_scales.tolist())) == hk
+    kc, vc = w.key_cache.clone(), w.value_cache.clone()
+    for i, st in enumerate(w.steps):
+        ref_k, ref_v = kc.clone(), vc.clone()
+        out = oracle.run_workload_step(w, i, kc, vc)
+        for h in range(hk):
+            ks, vs = float(w.k_head_scales[h]), float(w.v_head_scales[h])
+            kh, vh = ref_k[:, h:h + 1], ref_v[:, h:h + 1]
+            oracle.reshape_and_cache(st.new_key[:, h:h + 1], st.new_value[:, h:h + 1], kh, vh, st.slot_mapping, ks, vs)
+            assert torch.equal(kh.view(torch.uint8), kc[:, h:h + 1].view(torch.uint8))
+            o = oracle.paged_attention_decode(st.query[:, h * g:(h + 1) * g], kh, vh, st.block_tables,
+                                              st.context_lens, w.scale, ks, vs)
+            assert torch.equal(o, out[:, h * g:(h + 1) * g])
+
+
+def test_write_reports_per_head_amax():
+    """amax[h] becomes max(amax[h], the largest |x| written for head h), tokens with a
+    negative slot excluded; a NaN makes its head's amax NaN and leaves the others."""
+    w = _fp8_heads(spread=4.0)
+    st = w.steps[0]
+    hk = w.num_kv_heads
+    kc, vc = w.key_cache.clone(), w.value_cache.clone()
+    sm = st.slot_mapping.clone()
+    sm[1] = -1
+    ka = torch.zeros(hk, dtype=torch.float64)
+    va = torch.full((hk,), 0.5, dtype=torch.float64)
+    key, value = st.new_key.clone(), st.new_value.clone()
+    oracle.reshape_and_cache(key, value, kc, vc, sm, 1.0, 1.0, w.k_head_scales, w.v_head_scales, ka, va)
+    keep = sm >= 0
+    ek = key[keep].double().abs().amax(dim=(0, 2))
+    ev = torch.maximum(value[keep].double().abs().amax(dim=(0, 2)), torch.tensor(0.5, dtype=torch.float64))
+    assert torch.equal(ka, ek) and torch.equal(va, ev)
+    key[0, 2, 5] = float("nan")
+    ka2 = torch.zeros(hk, dtype=torch.float64)
+    oracle.reshape_and_cache(key, value, kc, vc, sm, 1.0, 1.0, w.k_head_scales, w.v_head_scales, ka2, None)
+    assert torch.isnan(ka2[2]) and torch.equal(ka2[torch.arange(hk) != 2], ek[torch.arange(hk) != 2])
