@@ -58,9 +58,10 @@ def make_workload(name: str, rank: int = 0) -> wl.Workload:
         return wl.long_context(seed=3 + seed_off, block_size=bs)
     if name == "shared_prefix_cow":
         return wl.shared_prefix_cow(seed=4 + seed_off)
-    m = re.fullmatch(r"continuous_batching_bs(\d+)_(bf16|e4m3)", name)
-    if m:
-        return wl.continuous_batching(seed=5 + seed_off, block_size=int(m.group(1)), kv_dtype=m.group(2))
+    m = re.fullmatch(r"continuous_batching_bs(\d+)_(bf16|e4m3)(_headscales)?", name)
+    if m:   # _headscales: KV heads 2^3 apart in magnitude, one e4m3 scale each
+        return wl.continuous_batching(seed=5 + seed_off, block_size=int(m.group(1)), kv_dtype=m.group(2),
+                                      head_spread=3.0 if m.group(3) else 0.0)
     m = re.fullmatch(r"sliding_window(?:_bs(\d+))?", name)
     if m:   # Mistral-style 4096-position window over 8 x 32768-token contexts
         return wl.sliding_window_decode(seed=6 + seed_off, block_size=int(m.group(1) or 16))
@@ -202,7 +203,8 @@ def oracle_throughput(w: wl.Workload, budget_s: float, max_seqs=None):
     if st.cow_pairs.numel():
         oracle.copy_blocks(kc, st.cow_pairs)
         oracle.copy_blocks(vc, st.cow_pairs)
-    oracle.reshape_and_cache(st.new_key, st.new_value, kc, vc, st.slot_mapping, w.k_scale, w.v_scale)
+    oracle.reshape_and_cache(st.new_key, st.new_value, kc, vc, st.slot_mapping, w.k_scale, w.v_scale,
+                             w.k_head_scales, w.v_head_scales)
     s_total = st.query.shape[0]
     n = s_total if max_seqs is None else max(1, min(s_total, max_seqs))
     done_bytes, elapsed, reps = 0, 0.0, 0
@@ -211,7 +213,8 @@ def oracle_throughput(w: wl.Workload, budget_s: float, max_seqs=None):
                             st.block_tables[:n], st.context_lens[:n], st.cow_pairs[:0])
         t = time.perf_counter()
         oracle.paged_attention_decode(sub.query, kc, vc, sub.block_tables, sub.context_lens, w.scale,
-                                      w.k_scale, w.v_scale, threads, w.sliding_window)
+                                      w.k_scale, w.v_scale, threads, w.sliding_window, w.k_head_scales,
+                                      w.v_head_scales)
         elapsed += time.perf_counter() - t
         done_bytes += decode_bytes(w, sub)
         reps += 1
@@ -332,7 +335,8 @@ def run_gpu(args, world, rank, local):
         b.record(stream)
         binding.paged_attention_decode(dw.out, st.query, dw.key_cache, dw.value_cache, st.block_tables,
                                        st.context_lens, w.num_kv_heads, w.scale, w.block_size,
-                                       w.max_blocks_per_seq, w.k_scale, w.v_scale, None, w.sliding_window)
+                                       w.max_blocks_per_seq, w.k_scale, w.v_scale, None, w.sliding_window,
+                                       dw.k_head_scales, dw.v_head_scales)
         c.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -369,7 +373,8 @@ def run_gpu(args, world, rank, local):
         i = k % nsteps
         for f in fields:
             getattr(dev_in[i], f).copy_(getattr(host_steps[i], f), non_blocking=True)
-        run_decode_step(w, dw.key_cache, dw.value_cache, dev_in[i], dw.out)
+        run_decode_step(w, dw.key_cache, dw.value_cache, dev_in[i], dw.out, None, True, dw.k_head_scales,
+                        dw.v_head_scales)
         out_host.copy_(dw.out, non_blocking=True)
     torch.cuda.synchronize(dev)
     e_ms = 0.0
@@ -380,7 +385,8 @@ def run_gpu(args, world, rank, local):
         a.record(stream)
         for f in fields:
             getattr(dev_in[i], f).copy_(getattr(host_steps[i], f), non_blocking=True)
-        run_decode_step(w, dw.key_cache, dw.value_cache, dev_in[i], dw.out)
+        run_decode_step(w, dw.key_cache, dw.value_cache, dev_in[i], dw.out, None, True, dw.k_head_scales,
+                        dw.v_head_scales)
         out_host.copy_(dw.out, non_blocking=True)
         c.record(stream)
         c.synchronize()

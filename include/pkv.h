@@ -28,7 +28,9 @@
  *   of one larger tensor) but, like the base pointer, must be multiples of 16 bytes.
  * Dtypes.  Caches: PKV_F32, PKV_BF16 or PKV_FP8_E4M3 (OCP E4M3FN: bias 7, max 448,
  *   no infinity).  An e4m3 cache carries its per-tensor dequantisation scale in the
- *   descriptor's `scale` (stored code * scale = value); other dtypes ignore `scale`.
+ *   descriptor's `scale` (stored code * scale = value), or one scale per KV head in
+ *   `head_scales` (ultralytics.com glossary "PagedAttention", section "관련 기법": an
+ *   FP8 cache halves the memory of a 16-bit one); other dtypes ignore `scale`.
  *   Queries and outputs: PKV_F32 or PKV_BF16, the output in the query's dtype.
  *   Supported head_dim: 64 and 128.  Supported block_size: 2, 4, 8, 16, 32.
  * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream) of the
@@ -54,7 +56,7 @@
 extern "C" {
 #endif
 
-#define PKV_ABI_VERSION 2
+#define PKV_ABI_VERSION 3
 
 typedef enum pkv_dtype {
   PKV_F32 = 0,
@@ -86,6 +88,11 @@ typedef struct pkv_tensor {
   int64_t shape[4];
   int64_t stride[4];  /* in elements */
   float scale;        /* e4m3 caches: dequantisation scale; ignored otherwise */
+  /* e4m3 caches only, or NULL: DEVICE pointer to num_kv_heads fp32 scales, one per KV
+   * head, used instead of `scale` (stored code * head_scales[h] = value of head h);
+   * must be NULL for other dtypes.  Read by the kernels on the device, so it may be
+   * updated there (e.g. from an amax report) between calls on the stream. */
+  const float* head_scales;
 } pkv_tensor;
 
 typedef void* pkv_stream; /* a cudaStream_t */
@@ -214,6 +221,25 @@ pkv_status pkv_decode_step(const pkv_tensor* out, const pkv_tensor* query, const
                            const pkv_tensor* block_tables, const pkv_tensor* context_lens,
                            int32_t num_kv_heads, float scale, int32_t block_size,
                            int32_t max_blocks_per_seq, int32_t sliding_window, pkv_stream stream);
+
+/*
+ * pkv_reshape_and_cache_amax — pkv_reshape_and_cache that also reports, per KV head,
+ * the largest magnitude it wrote (for choosing 8-bit scales as amax / 448).
+ *
+ * Defined by: the cache write above, and ultralytics.com glossary "PagedAttention",
+ * section "관련 기법" (FP8 cache quantization).
+ *
+ * k_amax, v_amax: DEVICE arrays of num_kv_heads fp32 (either may be NULL), whose entries
+ * must start >= 0 (e.g. zeroed by the caller): entry h becomes max(entry, max |x|) over
+ * the values of head h of every token written (slot >= 0), in the source dtype before
+ * any scaling; a NaN source value makes the entry NaN.  Entries of other heads are not
+ * touched.  Works for every cache dtype.  Arguments and errors otherwise as for
+ * pkv_reshape_and_cache; an amax pointer not 4-byte aligned is PKV_ERR_INVALID_ARG.
+ */
+pkv_status pkv_reshape_and_cache_amax(const pkv_tensor* key, const pkv_tensor* value,
+                                      const pkv_tensor* key_cache, const pkv_tensor* value_cache,
+                                      const pkv_tensor* slot_mapping, float* k_amax, float* v_amax,
+                                      pkv_stream stream);
 
 /*
  * pkv_copy_blocks — copy whole physical blocks of one cache tensor.

@@ -36,7 +36,8 @@ class PkvError(RuntimeError):
 
 class PkvTensor(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
-                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4), ("scale", ctypes.c_float)]
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4), ("scale", ctypes.c_float),
+                ("head_scales", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -61,12 +62,13 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.pkv_copy_blocks.argtypes = [d, d, vp]
         lib.pkv_paged_attention_decode_noalloc.argtypes = [d, d, d, d, d, d, i32, f32, i32, i32, vp]
         lib.pkv_decode_step.argtypes = [d, d, d, d, d, d, d, d, d, i32, f32, i32, i32, i32, vp]
+        lib.pkv_reshape_and_cache_amax.argtypes = [d, d, d, d, d, vp, vp, vp]
         lib.pkv_paged_attention_decode_window.argtypes = [d, d, d, d, d, d, i32, f32, i32, i32, i32, vp]
         lib.pkv_noalloc_scratch_bytes.restype = i64
         lib.pkv_noalloc_scratch_bytes.argtypes = []
         for fn in ("pkv_paged_attention_decode", "pkv_paged_attention_decode_noalloc",
                    "pkv_reshape_and_cache", "pkv_decode_step", "pkv_copy_blocks",
-                   "pkv_paged_attention_decode_window",
+                   "pkv_paged_attention_decode_window", "pkv_reshape_and_cache_amax",
                    "pkv_set_option", "pkv_reserve_workspace", "pkv_read_device_errors"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.pkv_last_error.restype = ctypes.c_char_p
@@ -91,8 +93,9 @@ def _check(status: int) -> None:
         raise PkvError(status, msg.decode() if msg else "")
 
 
-def describe(t: torch.Tensor, scale: float = 1.0) -> PkvTensor:
-    """pkv_tensor descriptor of a tensor (pointer, dtype code, shape, strides)."""
+def describe(t: torch.Tensor, scale: float = 1.0, head_scales: Optional[torch.Tensor] = None) -> PkvTensor:
+    """pkv_tensor descriptor of a tensor (pointer, dtype code, shape, strides); an 8-bit
+    cache may carry one scale per KV head (a float32 tensor on the cache's device)."""
     if t.dim() > 4 or t.dim() < 1:
         raise ValueError("descriptors cover 1 to 4 dimensions")
     if t.dtype not in _DTYPES:
@@ -105,6 +108,10 @@ def describe(t: torch.Tensor, scale: float = 1.0) -> PkvTensor:
         d.shape[i] = t.shape[i] if i < t.dim() else 1
         d.stride[i] = t.stride(i) if i < t.dim() else 1
     d.scale = float(scale)
+    if head_scales is not None:
+        if head_scales.dtype != torch.float32 or not head_scales.is_contiguous() or head_scales.device != t.device:
+            raise ValueError("head scales must be a contiguous float32 tensor on the cache's device")
+        d.head_scales = head_scales.data_ptr()
     return d
 
 
@@ -121,13 +128,15 @@ def _stream(stream) -> ctypes.c_void_p:
 def paged_attention_decode(out, query, key_cache, value_cache, block_tables, context_lens,
                            num_kv_heads: int, scale: float, block_size: int,
                            max_blocks_per_seq: int, k_scale: float = 1.0, v_scale: float = 1.0,
-                           stream=None, sliding_window: int = 0) -> torch.Tensor:
+                           stream=None, sliding_window: int = 0, k_head_scales=None,
+                           v_head_scales=None) -> torch.Tensor:
     """Single-token decode attention over the paged cache into ``out`` (returned).
     ``sliding_window`` W > 0: each sequence attends to its last W positions only
-    (pkv_paged_attention_decode_window)."""
+    (pkv_paged_attention_decode_window).  ``k_head_scales`` / ``v_head_scales``: one
+    scale per KV head of an 8-bit cache (device float32), instead of k_scale / v_scale."""
     lib = load_library()
-    descs = [describe(out), describe(query), describe(key_cache, k_scale),
-             describe(value_cache, v_scale), describe(block_tables), describe(context_lens)]
+    descs = [describe(out), describe(query), describe(key_cache, k_scale, k_head_scales),
+             describe(value_cache, v_scale, v_head_scales), describe(block_tables), describe(context_lens)]
     args = [ctypes.byref(x) for x in descs]
     if sliding_window:
         _check(lib.pkv_paged_attention_decode_window(*args, int(num_kv_heads), float(scale), int(block_size),
@@ -142,14 +151,14 @@ def paged_attention_decode(out, query, key_cache, value_cache, block_tables, con
 def decode_step(out, query, key, value, slot_mapping, key_cache, value_cache, block_tables, context_lens,
                 num_kv_heads: int, scale: float, block_size: int, max_blocks_per_seq: int,
                 k_scale: float = 1.0, v_scale: float = 1.0, stream=None,
-                sliding_window: int = 0) -> torch.Tensor:
+                sliding_window: int = 0, k_head_scales=None, v_head_scales=None) -> torch.Tensor:
     """Append the step's new tokens (``key``/``value`` at ``slot_mapping``) to the cache
     and decode into ``out`` (returned): the results of reshape_and_cache followed by
     paged_attention_decode, with the decode's preparation overlapping the write."""
     lib = load_library()
     descs = [describe(out), describe(query), describe(key), describe(value), describe(slot_mapping),
-             describe(key_cache, k_scale), describe(value_cache, v_scale), describe(block_tables),
-             describe(context_lens)]
+             describe(key_cache, k_scale, k_head_scales), describe(value_cache, v_scale, v_head_scales),
+             describe(block_tables), describe(context_lens)]
     _check(lib.pkv_decode_step(*[ctypes.byref(x) for x in descs], int(num_kv_heads), float(scale),
                                int(block_size), int(max_blocks_per_seq), int(sliding_window), _stream(stream)))
     return out
@@ -178,12 +187,24 @@ def noalloc_scratch_bytes() -> int:
 
 
 def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, k_scale: float = 1.0,
-                      v_scale: float = 1.0, stream=None) -> None:
-    """Write the new tokens' K/V into their cache slots (in place)."""
+                      v_scale: float = 1.0, stream=None, k_head_scales=None, v_head_scales=None,
+                      k_amax=None, v_amax=None) -> None:
+    """Write the new tokens' K/V into their cache slots (in place).  ``k_amax`` /
+    ``v_amax`` (device float32 [Hk], starting >= 0) are raised to the largest |x|
+    written per KV head (pkv_reshape_and_cache_amax)."""
     lib = load_library()
-    descs = [describe(key), describe(value), describe(key_cache, k_scale),
-             describe(value_cache, v_scale), describe(slot_mapping)]
-    _check(lib.pkv_reshape_and_cache(*[ctypes.byref(x) for x in descs], _stream(stream)))
+    descs = [describe(key), describe(value), describe(key_cache, k_scale, k_head_scales),
+             describe(value_cache, v_scale, v_head_scales), describe(slot_mapping)]
+    args = [ctypes.byref(x) for x in descs]
+    if k_amax is None and v_amax is None:
+        _check(lib.pkv_reshape_and_cache(*args, _stream(stream)))
+        return
+    for a in (k_amax, v_amax):
+        if a is not None and (a.dtype != torch.float32 or not a.is_contiguous() or a.device != key_cache.device):
+            raise ValueError("amax arrays must be contiguous float32 tensors on the cache's device")
+    _check(lib.pkv_reshape_and_cache_amax(*args, None if k_amax is None else ctypes.c_void_p(k_amax.data_ptr()),
+                                          None if v_amax is None else ctypes.c_void_p(v_amax.data_ptr()),
+                                          _stream(stream)))
 
 
 def copy_blocks(cache, src_dst_pairs, stream=None) -> None:

@@ -15,6 +15,28 @@ namespace {
 constexpr int kWriteThreads = 128;
 constexpr int kCopyThreads = 256;
 
+// Largest |x| of a run of values; any NaN makes it NaN.
+struct AmaxAcc {
+  float m = 0.f;
+  bool nan = false;
+  __device__ void add(float x) {
+    nan |= x != x;
+    m = fmaxf(m, fabsf(x));
+  }
+  __device__ float value() const { return nan ? __uint_as_float(0x7fc00000u) : m; }
+};
+
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t w) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// Raise amax[h] to x >= 0 (non-negative floats order like their bit patterns, so an
+// integer max is a float max; the NaN pattern used here is above every finite value's).
+__device__ __forceinline__ void raise_amax(float* amax, int h, float x) {
+  if (amax) atomicMax(reinterpret_cast<int*>(amax) + h, __float_as_int(x));
+}
+
 // Same dtype in and out: bit copy of each token's Hk x D row, 16 bytes at a time.
 __global__ void __launch_bounds__(kWriteThreads) cache_write_copy_kernel(const CacheWriteParams p,
                                                                          int elt_bytes) {
@@ -41,6 +63,33 @@ __global__ void __launch_bounds__(kWriteThreads) cache_write_copy_kernel(const C
     const uint4 vv = *reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(p.value) + src);
     *reinterpret_cast<uint4*>(static_cast<unsigned char*>(p.key_cache) + dst) = kv;
     *reinterpret_cast<uint4*>(static_cast<unsigned char*>(p.value_cache) + dst) = vv;
+    if (p.k_amax || p.v_amax) {  // the largest magnitude of the 16 bytes, per tensor
+      AmaxAcc ak, av;
+      const uint32_t wk[4] = {kv.x, kv.y, kv.z, kv.w}, wv[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (elt_bytes == 4) {
+          ak.add(__uint_as_float(wk[q]));
+          av.add(__uint_as_float(wv[q]));
+        } else if (elt_bytes == 2) {  // two bf16 per word
+          ak.add(__uint_as_float(wk[q] << 16));
+          ak.add(__uint_as_float(wk[q] & 0xffff0000u));
+          av.add(__uint_as_float(wv[q] << 16));
+          av.add(__uint_as_float(wv[q] & 0xffff0000u));
+        } else {  // four e4m3 codes per word
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            const float2 fk = e4m3x2_to_float2(wk[q] >> (16 * b)), fv = e4m3x2_to_float2(wv[q] >> (16 * b));
+            ak.add(fk.x);
+            ak.add(fk.y);
+            av.add(fv.x);
+            av.add(fv.y);
+          }
+        }
+      }
+      raise_amax(p.k_amax, h, ak.value());
+      raise_amax(p.v_amax, h, av.value());
+    }
   }
 }
 
@@ -94,8 +143,20 @@ __global__ void __launch_bounds__(kWriteThreads) cache_write_e4m3_kernel(const C
     float xk[8], xv[8];
     load8<Src>(static_cast<const unsigned char*>(p.key) + src, xk);
     load8<Src>(static_cast<const unsigned char*>(p.value) + src, xv);
-    *reinterpret_cast<uint2*>(static_cast<unsigned char*>(p.key_cache) + dst) = quantize8(xk, p.k_scale);
-    *reinterpret_cast<uint2*>(static_cast<unsigned char*>(p.value_cache) + dst) = quantize8(xv, p.v_scale);
+    const float ks = p.k_head_scales ? __ldg(p.k_head_scales + h) : p.k_scale;
+    const float vs = p.v_head_scales ? __ldg(p.v_head_scales + h) : p.v_scale;
+    *reinterpret_cast<uint2*>(static_cast<unsigned char*>(p.key_cache) + dst) = quantize8(xk, ks);
+    *reinterpret_cast<uint2*>(static_cast<unsigned char*>(p.value_cache) + dst) = quantize8(xv, vs);
+    if (p.k_amax || p.v_amax) {
+      AmaxAcc ak, av;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        ak.add(xk[e]);
+        av.add(xv[e]);
+      }
+      raise_amax(p.k_amax, h, ak.value());
+      raise_amax(p.v_amax, h, av.value());
+    }
   }
 }
 

@@ -126,13 +126,16 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const DecodeParams p)
     }
     tbl[i] = e;
   }
-  // queries of the G heads, scaled by scale * log2(e) (* k dequant scale)
+  // queries of the G heads, scaled by scale * log2(e) (* k dequant scale, per KV head
+  // when the cache has per-head scales)
+  const float qk_scale = p.k_head_scales ? p.qk_scale_log2 * __ldg(p.k_head_scales + kvh) : p.qk_scale_log2;
+  const float v_scale = p.v_head_scales ? __ldg(p.v_head_scales + kvh) : p.v_scale;
   for (int i = tid; i < G * D; i += T::kThreads) {
     const int h = i / D, d = i % D;
     const int64_t qi = int64_t(seq) * p.q_stride_s + int64_t(h0 + h) * p.q_stride_h + d;
     const float qv = p.q_dtype == kF32 ? static_cast<const float*>(p.query)[qi]
                                        : __uint_as_float(uint32_t(static_cast<const uint16_t*>(p.query)[qi]) << 16);
-    q_s[i] = qv * p.qk_scale_log2;
+    q_s[i] = qv * qk_scale;
   }
   __syncthreads();
 
@@ -334,7 +337,7 @@ __global__ void __launch_bounds__(128) paged_decode_kernel(const DecodeParams p)
         den = fmaf(wt, l_s[w * G + h], den);
       }
     }
-    const float res = den > 0.f ? num / den * p.v_scale : 0.f;
+    const float res = den > 0.f ? num / den * v_scale : 0.f;
     const int hq = h0 + h;
     if (nparts == 1) {
       const int64_t oi = int64_t(seq) * p.out_stride_s + int64_t(hq) * p.out_stride_h + d;

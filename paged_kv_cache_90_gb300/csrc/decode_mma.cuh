@@ -468,7 +468,8 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
   cc.left = 0;
   int cu = 0;  // unit being consumed
   uint32_t qa[C::kKS][4], qa_next[C::kKS][4];
-  const float sl = p.qk_scale_log2;
+  float sl = p.qk_scale_log2;  // score scale (base 2) of the current row's KV head
+  float vsc = p.v_scale;       // value scale of the current row's KV head
   float o[C::kNT][4];
   float m_ref[C::kRows], l_run[C::kRows];
   bool first = true, aborted = false;
@@ -494,6 +495,8 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
     }
     const bool last = cc.left == 1 || cc.t0 + kST >= cc.rl;
     if (first) {
+      if (p.k_head_scales) sl = p.qk_scale_log2 * __ldg(p.k_head_scales + cc.kvh);
+      if (p.v_head_scales) vsc = __ldg(p.v_head_scales + cc.kvh);
       if (unit_start) {
         load_q(cc.s, cc.kvh * p.group + cc.sub * G, qa);
       } else {
@@ -707,7 +710,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
         for (int rr = 0; rr < C::kRows; ++rr) {
           const int hr = g + 8 * rr;
           if (hr < G) {
-            const float inv = l_run[rr] > 0.f ? p.v_scale / l_run[rr] : 0.f;
+            const float inv = l_run[rr] > 0.f ? vsc / l_run[rr] : 0.f;
             __nv_bfloat16* out = outs + int64_t(h0 + hr) * p.out_stride_h;
 #pragma unroll
             for (int n = 0; n < C::kNT; ++n)
@@ -722,7 +725,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
           const int hr = g + 8 * rr;
           if (hr < G) {
             const int64_t pr = int64_t(slot_id) * G + hr;
-            const float inv = l_run[rr] > 0.f ? p.v_scale / l_run[rr] : 0.f;
+            const float inv = l_run[rr] > 0.f ? vsc / l_run[rr] : 0.f;
             float* po = p.part_o + pr * D;
 #pragma unroll
             for (int n = 0; n < C::kNT; ++n)

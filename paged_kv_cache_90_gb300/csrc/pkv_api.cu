@@ -184,8 +184,14 @@ pkv_status check_cache(const pkv_tensor* c, const char* name) {
   const int eb = elt_bytes(c->dtype);
   if (!aligned16(c->data) || (c->stride[0] * eb) % 16 || (c->stride[1] * eb) % 16)
     return fail(PKV_ERR_INVALID_ARG, "%s: base pointer and block/head strides must be multiples of 16 bytes", name);
-  if (c->dtype == PKV_FP8_E4M3 && !(std::isfinite(c->scale) && c->scale > 0.f))
+  if (c->head_scales) {
+    if (c->dtype != PKV_FP8_E4M3)
+      return fail(PKV_ERR_INVALID_ARG, "%s: per-head scales are for an e4m3 cache only", name);
+    if (reinterpret_cast<uintptr_t>(c->head_scales) & 3)
+      return fail(PKV_ERR_INVALID_ARG, "%s: head_scales must be 4-byte aligned", name);
+  } else if (c->dtype == PKV_FP8_E4M3 && !(std::isfinite(c->scale) && c->scale > 0.f)) {
     return fail(PKV_ERR_INVALID_ARG, "%s: an e4m3 cache needs a finite positive scale", name);
+  }
   return PKV_OK;
 }
 
@@ -302,9 +308,13 @@ pkv_status decode_prepare(const pkv_tensor* out, const pkv_tensor* query, const 
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.num_blocks = NB;
   p.group = int(Hq / num_kv_heads);
-  const float kscale = key_cache->dtype == PKV_FP8_E4M3 ? key_cache->scale : 1.0f;
+  // per-head K / V scales (e4m3 only) are applied on the device, per KV head
+  const bool fp8 = key_cache->dtype == PKV_FP8_E4M3;
+  p.k_head_scales = fp8 ? key_cache->head_scales : nullptr;
+  p.v_head_scales = fp8 ? value_cache->head_scales : nullptr;
+  const float kscale = fp8 && !p.k_head_scales ? key_cache->scale : 1.0f;
   p.qk_scale_log2 = float(double(scale) * 1.4426950408889634 * double(kscale));
-  p.v_scale = value_cache->dtype == PKV_FP8_E4M3 ? value_cache->scale : 1.0f;
+  p.v_scale = fp8 && !p.v_head_scales ? value_cache->scale : 1.0f;
   p.sliding_window = sliding_window;
   p.partition_tokens = pt;
   p.max_partitions = int(parts);
@@ -391,6 +401,8 @@ pkv_status reshape_prepare(const pkv_tensor* key, const pkv_tensor* value, const
   p.cache_dtype = key_cache->dtype;
   p.k_scale = key_cache->scale;
   p.v_scale = value_cache->scale;
+  p.k_head_scales = key_cache->head_scales;
+  p.v_head_scales = value_cache->head_scales;
   p.slot_mapping = static_cast<const int64_t*>(slot_mapping->data);
   p.num_tokens = T;
   p.num_kv_heads = int(Hk);
@@ -576,6 +588,24 @@ pkv_status pkv_reshape_and_cache(const pkv_tensor* key, const pkv_tensor* value,
   if ((st = device_state(&s))) return st;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   return finish_call(s, launch_reshape_and_cache(p, cs), cs, "reshape_and_cache");
+}
+
+pkv_status pkv_reshape_and_cache_amax(const pkv_tensor* key, const pkv_tensor* value,
+                                      const pkv_tensor* key_cache, const pkv_tensor* value_cache,
+                                      const pkv_tensor* slot_mapping, float* k_amax, float* v_amax,
+                                      pkv_stream stream) {
+  if ((reinterpret_cast<uintptr_t>(k_amax) & 3) || (reinterpret_cast<uintptr_t>(v_amax) & 3))
+    return fail(PKV_ERR_INVALID_ARG, "amax arrays must be 4-byte aligned");
+  CacheWriteParams p;
+  bool nothing = false;
+  pkv_status st = reshape_prepare(key, value, key_cache, value_cache, slot_mapping, &p, &nothing);
+  if (st || nothing) return st;
+  p.k_amax = k_amax;
+  p.v_amax = v_amax;
+  DeviceState* s;
+  if ((st = device_state(&s))) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  return finish_call(s, launch_reshape_and_cache(p, cs), cs, "reshape_and_cache_amax");
 }
 
 pkv_status pkv_decode_step(const pkv_tensor* out, const pkv_tensor* query, const pkv_tensor* key,

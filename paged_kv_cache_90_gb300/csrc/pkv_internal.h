@@ -28,6 +28,10 @@ struct CacheWriteParams {
   int cache_dtype;           // kF32 / kBF16 / kE4M3
   float k_scale;             // e4m3 cache: value = code * scale
   float v_scale;
+  const float* k_head_scales;  // e4m3 cache: [Hk] per-head scales instead (or null)
+  const float* v_head_scales;
+  float* k_amax;             // [Hk] raised to max |x| written per head (or null)
+  float* v_amax;
   const int64_t* slot_mapping;
   int64_t num_tokens;
   int num_kv_heads;
@@ -70,8 +74,10 @@ struct DecodeParams {
   int num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq;
   int64_t num_blocks;
   int group;                 // num_heads / num_kv_heads
-  float qk_scale_log2;       // scale * log2(e) * k_scale
-  float v_scale;
+  float qk_scale_log2;       // scale * log2(e) * k_scale (without it with per-head K scales)
+  float v_scale;             // 1 with per-head V scales
+  const float* k_head_scales;  // e4m3 cache: [Hk] per-head scales (or null)
+  const float* v_head_scales;
   int sliding_window;        // attend to the last W positions only (0: all)
   int partition_tokens;      // multiple of 256
   int max_partitions;        // ceil(max_blocks_per_seq * block_size / partition_tokens)

@@ -44,6 +44,9 @@ class DeviceWorkload:
         self.device = torch.device(device)
         self.key_cache = w.key_cache.to(self.device)
         self.value_cache = w.value_cache.to(self.device)
+        # an 8-bit cache with one scale per KV head keeps the scales on the device
+        self.k_head_scales = None if w.k_head_scales is None else w.k_head_scales.to(self.device)
+        self.v_head_scales = None if w.v_head_scales is None else w.v_head_scales.to(self.device)
         self.steps: List[DeviceStep] = [DeviceStep.from_host(st, self.device) for st in w.steps]
         s, hq, d = w.steps[0].query.shape
         self.out = torch.empty(s, hq, d, dtype=w.q_dtype, device=self.device)
@@ -55,23 +58,26 @@ class DeviceWorkload:
         the decode as one decode_step call, otherwise as two calls."""
         st = step if step is not None else self.steps[i]
         out = self.out if out is None else out
-        run_decode_step(self.w, self.key_cache, self.value_cache, st, out, stream, joint)
+        run_decode_step(self.w, self.key_cache, self.value_cache, st, out, stream, joint,
+                        self.k_head_scales, self.v_head_scales)
         return out
 
 
 def run_decode_step(w: Workload, key_cache, value_cache, st: DeviceStep, out, stream=None,
-                    joint: bool = True) -> None:
+                    joint: bool = True, k_head_scales=None, v_head_scales=None) -> None:
     if st.cow_pairs.numel():
         binding.copy_blocks(key_cache, st.cow_pairs, stream)
         binding.copy_blocks(value_cache, st.cow_pairs, stream)
     if joint:
         binding.decode_step(out, st.query, st.new_key, st.new_value, st.slot_mapping, key_cache, value_cache,
                             st.block_tables, st.context_lens, w.num_kv_heads, w.scale, w.block_size,
-                            w.max_blocks_per_seq, w.k_scale, w.v_scale, stream, w.sliding_window)
+                            w.max_blocks_per_seq, w.k_scale, w.v_scale, stream, w.sliding_window,
+                            k_head_scales, v_head_scales)
         return
     if st.slot_mapping.numel():
         binding.reshape_and_cache(st.new_key, st.new_value, key_cache, value_cache, st.slot_mapping,
-                                  w.k_scale, w.v_scale, stream)
+                                  w.k_scale, w.v_scale, stream, k_head_scales, v_head_scales)
     binding.paged_attention_decode(out, st.query, key_cache, value_cache, st.block_tables,
                                    st.context_lens, w.num_kv_heads, w.scale, w.block_size,
-                                   w.max_blocks_per_seq, w.k_scale, w.v_scale, stream, w.sliding_window)
+                                   w.max_blocks_per_seq, w.k_scale, w.v_scale, stream, w.sliding_window,
+                                   k_head_scales, v_head_scales)

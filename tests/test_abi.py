@@ -39,7 +39,7 @@ def test_exports_every_declared_function(lib):
     assert {"pkv_paged_attention_decode", "pkv_reshape_and_cache", "pkv_copy_blocks"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} is declared in pkv.h but not exported"
-    assert binding.abi_version() == 2
+    assert binding.abi_version() == 3
 
 
 def _decode_args(S=3, Hq=8, Hk=2, D=128, bs=16, NB=20, MB=4, dtype=torch.bfloat16, kv=torch.bfloat16):
@@ -77,6 +77,33 @@ def test_decode_step_validation(dry):
     empty = torch.zeros(0, 2, 128, dtype=torch.bfloat16)
     assert _status(binding.decode_step, **args(key=empty, value=empty,
                                                slot_mapping=torch.zeros(0, dtype=torch.int64))) == 0
+
+
+def test_head_scales_and_amax_validation(dry):
+    """Per-head scales belong to 8-bit caches only and must be 4-byte aligned; the
+    per-tensor scale is not checked when they are given; amax arrays must be aligned."""
+    hs = torch.ones(2, dtype=torch.float32)
+    a = _decode_args(kv=torch.float8_e4m3fn)
+    assert _status(binding.paged_attention_decode, **a, k_head_scales=hs, v_head_scales=hs) == 0
+    assert _status(binding.paged_attention_decode, **a, k_scale=0.0, v_scale=0.0, k_head_scales=hs,
+                   v_head_scales=hs) == 0
+    assert _status(binding.paged_attention_decode, **_decode_args(), k_head_scales=hs) == 1   # bf16 cache
+    lib = binding.load_library()
+    descs = [binding.describe(a[k]) for k in ("out", "query")]
+    kc = binding.describe(a["key_cache"], 1.0)
+    kc.head_scales = hs.data_ptr() + 2
+    descs += [kc, binding.describe(a["value_cache"], 1.0), binding.describe(a["block_tables"]),
+              binding.describe(a["context_lens"])]
+    rc = lib.pkv_paged_attention_decode(*[ctypes.byref(x) for x in descs], 2, 0.1, 16, 4, None)
+    assert rc == 1 and b"aligned" in lib.pkv_last_error()
+    T = 3
+    w = [binding.describe(torch.zeros(T, 2, 128, dtype=torch.bfloat16)) for _ in range(2)]
+    c = [binding.describe(torch.zeros(20, 2, 16, 128, dtype=torch.float8_e4m3fn), 0.5) for _ in range(2)]
+    sm = binding.describe(torch.arange(T, dtype=torch.int64))
+    amax = torch.zeros(4, dtype=torch.float32)
+    args = [ctypes.byref(x) for x in (w[0], w[1], c[0], c[1], sm)]
+    assert lib.pkv_reshape_and_cache_amax(*args, ctypes.c_void_p(amax.data_ptr()), None, None) == 0
+    assert lib.pkv_reshape_and_cache_amax(*args, ctypes.c_void_p(amax.data_ptr() + 2), None, None) == 1
 
 
 def test_decode_validation(dry):

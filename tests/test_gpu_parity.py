@@ -92,8 +92,10 @@ def weighted_abs_values(w, st, kc, vc):
         blocks = st.block_tables[s, b0:b0 + n].long()
         K = gather_blocks(kc, blocks).double().permute(1, 0, 2, 3).reshape(hk, n * bs, d)[:, lo - b0 * bs:L - b0 * bs]
         V = gather_blocks(vc, blocks).double().permute(1, 0, 2, 3).reshape(hk, n * bs, d)[:, lo - b0 * bs:L - b0 * bs]
-        K = K * w.k_scale
-        V = V.abs() * w.v_scale
+        ks = w.k_head_scales.double().view(hk, 1, 1) if w.k_head_scales is not None else w.k_scale
+        vs = w.v_head_scales.double().view(hk, 1, 1) if w.v_head_scales is not None else w.v_scale
+        K = K * ks
+        V = V.abs() * vs
         q = st.query[s].double().view(hk, g, d)
         p = torch.softmax(w.scale * q @ K.transpose(1, 2), dim=-1)
         out[s] = (p @ V).reshape(hq, d)
@@ -198,6 +200,50 @@ def test_continuous_batching_small(bs, kv, kernel):
 @pytest.mark.parametrize("bs", [8, 16, 32])
 def test_continuous_batching_full(bs, kv, kernel):
     check_workload(wl.continuous_batching(block_size=bs, kv_dtype=kv))
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_fp8_head_scales_small(bs, kernel):
+    """An 8-bit cache whose KV heads differ by 2^3 in magnitude, one scale per head:
+    the write quantises each head with its scale and decode dequantises with it."""
+    check_workload(wl.continuous_batching(seed=70 + bs, block_size=bs, kv_dtype="e4m3", num_seqs=24, num_steps=3,
+                                          median=200, cap=2000, poison=True, head_spread=3.0))
+
+
+def test_fp8_head_scales_full(kernel):
+    check_workload(wl.continuous_batching(kv_dtype="e4m3", head_spread=3.0))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3", "f32"])
+def test_write_reports_amax(kv):
+    """The amax report equals the oracle's per-head max |x| (bf16 / f32 sources are
+    exact in fp32), keeps a larger starting value, skips padding tokens, and turns NaN
+    for a head whose source holds a NaN."""
+    dt = "f32" if kv == "f32" else "bf16"
+    w = wl.variable_length_decode("a", 73, [5, 40, 99, 7], 8, 4, 128, 16, kv, q_dtype=dt, num_steps=1,
+                                  head_spread=4.0 if kv == "e4m3" else 0.0)
+    st = w.steps[0]
+    dw = DeviceWorkload(w)
+    sm = st.slot_mapping.clone()
+    sm[2] = -1
+    key, value = st.new_key.clone(), st.new_value.clone()
+    key[1, 3, 17] = float("nan")
+    ka = torch.zeros(4, dtype=torch.float32, device="cuda")
+    va = torch.full((4,), 1e9, dtype=torch.float32, device="cuda")
+    binding.reshape_and_cache(key.cuda(), value.cuda(), dw.key_cache, dw.value_cache, sm.cuda(), w.k_scale,
+                              w.v_scale, None, dw.k_head_scales, dw.v_head_scales, ka, va)
+    torch.cuda.synchronize()
+    ref_k = torch.zeros(4, dtype=torch.float64)
+    ref_v = torch.zeros(4, dtype=torch.float64)
+    kc, vc = w.key_cache.clone(), w.value_cache.clone()
+    oracle.reshape_and_cache(key, value, kc, vc, sm, w.k_scale, w.v_scale, w.k_head_scales, w.v_head_scales,
+                             ref_k, ref_v)
+    got_k = ka.cpu().double()
+    assert torch.isnan(got_k[3]) and torch.isnan(ref_k[3])
+    assert torch.equal(got_k[:3], ref_k[:3])
+    assert torch.equal(va.cpu(), torch.full((4,), 1e9))
+    assert torch.equal(raw(dw.key_cache.cpu()), raw(kc)) and torch.equal(raw(dw.value_cache.cpu()), raw(vc))
+    assert binding.read_device_errors() == 0
 
 
 @pytest.mark.parametrize("bs", [8, 16, 32])
