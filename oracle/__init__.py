@@ -62,6 +62,9 @@ def _load():
             lib.orc_paged_attention_decode_ex.restype = i32
             lib.orc_paged_attention_decode_ex.argtypes = (
                 [vp, vp, i32, vp, vp, i32, dbl, dbl, vp, vp, vp, vp] + [i64] * 10 + [dbl, i64, i32])
+            lib.orc_paged_attention_prefill.restype = i32
+            lib.orc_paged_attention_prefill.argtypes = (
+                [vp, vp, i32, vp, vp, i32, dbl, dbl, vp, vp, vp] + [i64] * 10 + [dbl, i32])
             lib.orc_reshape_and_cache_ex.restype = i32
             lib.orc_reshape_and_cache_ex.argtypes = (
                 [vp, vp, i32, vp, vp, i32, ctypes.c_float, ctypes.c_float, vp, vp, vp, vp, vp] + [i64] * 8)
@@ -130,6 +133,36 @@ def paged_attention_decode(query, key_cache, value_cache, block_tables, context_
         float(scale), int(sliding_window), int(num_threads))
     if rc != 0:
         raise ValueError(f"oracle decode failed with status {rc}")
+    return out
+
+
+def paged_attention_prefill(query, key_cache, value_cache, block_tables, context_lens, query_start_loc,
+                            scale: float, k_scale: float = 1.0, v_scale: float = 1.0,
+                            num_threads: int = 1) -> torch.Tensor:
+    """Causal attention of the packed new tokens of every sequence over its cache, in
+    fp64; returns ``[T, Hq, D]`` float64.  Sequence s owns query rows
+    ``query_start_loc[s] .. query_start_loc[s+1]-1``, the last of its
+    ``context_lens[s]`` cached positions."""
+    lib = _load()
+    q = _cpu(query)
+    bt = _cpu(block_tables).to(torch.int32)
+    cl = _cpu(context_lens).to(torch.int32)
+    qsl = _cpu(query_start_loc).to(torch.int32)
+    t, hq, d = q.shape
+    nb, hk, bs, dk = key_cache.shape
+    if dk != d or value_cache.shape != key_cache.shape or value_cache.stride() != key_cache.stride():
+        raise ValueError("cache shapes disagree")
+    if qsl.numel() != cl.numel() + 1 or int(qsl[-1]) != t:
+        raise ValueError("query_start_loc must have num_seqs + 1 entries ending at the number of queries")
+    cs = _cache_strides(key_cache)
+    out = torch.zeros(t, hq, d, dtype=torch.float64)
+    mb = bt.shape[1] if bt.dim() == 2 else 0
+    rc = lib.orc_paged_attention_prefill(
+        out.data_ptr(), q.data_ptr(), _CODES[q.dtype], key_cache.data_ptr(), value_cache.data_ptr(),
+        _CODES[key_cache.dtype], float(k_scale), float(v_scale), bt.data_ptr(), cl.data_ptr(), qsl.data_ptr(),
+        cl.numel(), hq, hk, d, bs, nb, mb, cs[0], cs[1], cs[2], float(scale), int(num_threads))
+    if rc != 0:
+        raise ValueError(f"oracle prefill failed with status {rc}")
     return out
 
 
@@ -208,6 +241,9 @@ def run_workload_step(w, step_index: int, key_cache, value_cache, num_threads: i
     if st.slot_mapping.numel():
         reshape_and_cache(st.new_key, st.new_value, key_cache, value_cache, st.slot_mapping,
                           w.k_scale, w.v_scale, ksh, vsh)
+    if getattr(st, "query_start_loc", None) is not None:   # a prefill step
+        return paged_attention_prefill(st.query, key_cache, value_cache, st.block_tables, st.context_lens,
+                                       st.query_start_loc, w.scale, w.k_scale, w.v_scale, num_threads)
     return paged_attention_decode(st.query, key_cache, value_cache, st.block_tables,
                                   st.context_lens, w.scale, w.k_scale, w.v_scale, num_threads,
                                   getattr(w, "sliding_window", 0), ksh, vsh)

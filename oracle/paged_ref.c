@@ -40,6 +40,16 @@
  *     gather, scores, softmax and weighted sum run over that range; W <= 0 means no
  *     window.
  *
+ *  1c. Prefill / chunked prefill.  A sequence whose cache holds L tokens, the last n of
+ *     them new this step (a prompt, or the next chunk of one, written by the cache write
+ *     first), computes attention for each new token: query i (i < n) sits at position
+ *     p = L - n + i and attends causally to positions j <= p through the same table
+ *     (ya.zerocoder.ru "Что такое PagedAttention", section "Зачем KV cache вообще
+ *     нужен": full causal attention, each token using the keys and values of the
+ *     positions before it; the same gather, scores, softmax and weighted sum as
+ *     decode).  Queries of all sequences are packed: sequence s owns rows
+ *     query_start_loc[s] .. query_start_loc[s+1]-1 of query and out.
+ *
  *  2. Cache write ("reshape_and_cache").  New token t with slot = slot_mapping[t]:
  *       slot < 0  -> nothing is written (a padding token);
  *       else      -> cache[slot / bs, h, slot % bs, :] = encode(key[t, h, :])
@@ -386,6 +396,101 @@ int orc_copy_blocks(void* cache, int64_t block_bytes, int64_t num_blocks,
             (size_t)block_bytes);
   }
   return ORC_OK;
+}
+
+/* ---- 1c. prefill ---------------------------------------------------------------- */
+
+int orc_paged_attention_prefill(
+    double* out,                                 /* [T, Hq, D] */
+    const void* query, int q_dtype,              /* [T, Hq, D], contiguous */
+    const void* key_cache, const void* value_cache, int kv_dtype,
+    double k_scale, double v_scale,
+    const int32_t* block_tables,                 /* [S, MB] */
+    const int32_t* context_lens,                 /* [S]: cached tokens, new ones included */
+    const int32_t* query_start_loc,              /* [S + 1] */
+    int64_t num_seqs, int64_t num_heads, int64_t num_kv_heads, int64_t head_dim,
+    int64_t block_size, int64_t num_blocks, int64_t max_blocks_per_seq,
+    int64_t cs_block, int64_t cs_head, int64_t cs_token,
+    double scale, int num_threads) {
+  int64_t group, work;
+  int status = ORC_OK;
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      block_size <= 0 || num_blocks <= 0 || max_blocks_per_seq < 0 ||
+      num_heads % num_kv_heads != 0 || orc_elem_bytes(q_dtype) == 0 ||
+      orc_elem_bytes(kv_dtype) == 0)
+    return ORC_BAD_ARG;
+  group = num_heads / num_kv_heads;
+  work = num_seqs * num_kv_heads;
+
+#ifdef _OPENMP
+  if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1) if (num_threads > 1)
+#endif
+  for (int64_t w = 0; w < work; ++w) {
+    int64_t s = w / num_kv_heads, k = w % num_kv_heads;
+    int64_t L = context_lens[s];
+    int64_t q0 = query_start_loc[s], n = query_start_loc[s + 1] - q0;
+    double *K = NULL, *V = NULL, *z = NULL;
+    int bad = 0;
+    if (L < 0 || L > max_blocks_per_seq * block_size || n < 0 || n > L) {
+      bad = ORC_BAD_TABLE;
+      L = 0;
+      n = 0;
+    } else if (L > 0) {
+      K = (double*)malloc(sizeof(double) * (size_t)(L * head_dim));
+      V = (double*)malloc(sizeof(double) * (size_t)(L * head_dim));
+      z = (double*)malloc(sizeof(double) * (size_t)L);
+      if (!K || !V || !z) bad = ORC_NO_MEMORY;
+    }
+    /* gather the whole context of KV head k in logical order */
+    for (int64_t j = 0; j < L && !bad; ++j) {
+      int64_t phys = block_tables[s * max_blocks_per_seq + j / block_size];
+      int64_t base;
+      if (phys < 0 || phys >= num_blocks) {
+        bad = ORC_BAD_TABLE;
+        break;
+      }
+      base = phys * cs_block + k * cs_head + (j % block_size) * cs_token;
+      for (int64_t d = 0; d < head_dim; ++d) {
+        K[j * head_dim + d] = orc_load(key_cache, base + d, kv_dtype) * k_scale;
+        V[j * head_dim + d] = orc_load(value_cache, base + d, kv_dtype) * v_scale;
+      }
+    }
+    for (int64_t i = 0; i < n; ++i) {
+      int64_t pos = L - n + i;        /* this query's position; it sees 0..pos */
+      for (int64_t h = k * group; h < (k + 1) * group; ++h) {
+        double* o = out + ((q0 + i) * num_heads + h) * head_dim;
+        const int64_t qoff = ((q0 + i) * num_heads + h) * head_dim;
+        double zmax = -INFINITY, den = 0.0;
+        for (int64_t d = 0; d < head_dim; ++d) o[d] = 0.0;
+        if (bad) continue;
+        for (int64_t j = 0; j <= pos; ++j) {
+          double acc = 0.0;
+          for (int64_t d = 0; d < head_dim; ++d)
+            acc += orc_load(query, qoff + d, q_dtype) * K[j * head_dim + d];
+          z[j] = scale * acc;
+          if (z[j] > zmax) zmax = z[j];
+        }
+        for (int64_t j = 0; j <= pos; ++j) {
+          z[j] = exp(z[j] - zmax);
+          den += z[j];
+        }
+        for (int64_t j = 0; j <= pos; ++j) z[j] /= den;
+        for (int64_t j = 0; j <= pos; ++j)
+          for (int64_t d = 0; d < head_dim; ++d) o[d] += z[j] * V[j * head_dim + d];
+      }
+    }
+    free(K);
+    free(V);
+    free(z);
+    if (bad) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+      status = bad;
+    }
+  }
+  return status;
 }
 
 int orc_max_threads(void) {

@@ -43,6 +43,9 @@ class DecodeStep:
     block_tables: torch.Tensor   # [S, MB] int32, padded with -1
     context_lens: torch.Tensor   # [S] int32, counts the new token
     cow_pairs: torch.Tensor      # [n, 2] int64 (src, dst), copied before the append
+    # prefill: query rows of sequence s are query_start_loc[s] .. query_start_loc[s+1]-1
+    # (then query, new_key, new_value and slot_mapping hold every new token, packed)
+    query_start_loc: Optional[torch.Tensor] = None
 
 
 @dataclass
@@ -388,6 +391,60 @@ def sliding_window_decode(seed: int = 6, num_seqs: int = 8, context_len: int = 3
                                   poison=poison, window=window)
 
 
+def chunked_prefill(seed: int = 7, prefix_lens: Sequence[int] = (0, 0, 512, 1536),
+                    chunk_lens: Sequence[int] = (2048, 1024, 512, 512), num_heads: int = 32,
+                    num_kv_heads: int = 8, head_dim: int = 128, block_size: int = 16,
+                    kv_dtype: str = "bf16", pool_slack: float = 0.10, poison: bool = False) -> Workload:
+    """Prefill of prompts (prefix 0) and of later chunks of long prompts: sequence s has
+    ``prefix_lens[s]`` tokens cached and appends ``chunk_lens[s]`` new ones, whose K/V
+    the step writes and whose queries attend causally to everything before them.  The
+    step's query, new K/V and slot mapping hold all new tokens packed, sequence by
+    sequence (``query_start_loc``)."""
+    g = torch.Generator().manual_seed(seed)
+    prefix = [int(x) for x in prefix_lens]
+    chunk = [int(x) for x in chunk_lens]
+    if len(prefix) != len(chunk) or min(chunk) < 1 or min(prefix) < 0:
+        raise ValueError("one prefix and one chunk of >= 1 token per sequence")
+    need = sum(blocks_needed(a + b, block_size) for a, b in zip(prefix, chunk))
+    nb = int(math.ceil(need * (1.0 + pool_slack))) + 1
+    mb = max(blocks_needed(a + b, block_size) for a, b in zip(prefix, chunk))
+    perm = torch.randperm(nb, generator=g).tolist()
+    mgr = BlockManager(BlockAllocator(nb, block_size, perm))
+    seq_ids = list(range(len(prefix)))
+    for sid, a in zip(seq_ids, prefix):
+        mgr.add_sequence(sid, a)
+    kc, vc, ks, vs, _, _ = _make_pool(nb, num_kv_heads, block_size, head_dim, kv_dtype, g)
+    if poison:
+        # the chunk's slots are written by the step; everything else unused is NaN
+        occ = _occupied_slots(mgr)
+        _poison(kc, occ)
+        _poison(vc, occ)
+    slots = []
+    for sid, c in zip(seq_ids, chunk):
+        for _ in range(c):
+            slot, pair = mgr.append_token(sid)
+            assert pair is None
+            slots.append(slot)
+    t = sum(chunk)
+    src = torch.bfloat16 if kv_dtype == "e4m3" else DTYPES[kv_dtype]
+    q_dtype = torch.float32 if kv_dtype == "f32" else torch.bfloat16
+    qsl = [0]
+    for c in chunk:
+        qsl.append(qsl[-1] + c)
+    step = DecodeStep(
+        query=_randn((t, num_heads, head_dim), q_dtype, g),
+        new_key=_randn((t, num_kv_heads, head_dim), src, g),
+        new_value=_randn((t, num_kv_heads, head_dim), src, g),
+        slot_mapping=torch.tensor(slots, dtype=torch.int64),
+        block_tables=torch.tensor(mgr.block_table_rows(seq_ids, mb), dtype=torch.int32).view(len(seq_ids), mb),
+        context_lens=torch.tensor([a + b for a, b in zip(prefix, chunk)], dtype=torch.int32),
+        cow_pairs=torch.zeros(0, 2, dtype=torch.int64),
+        query_start_loc=torch.tensor(qsl, dtype=torch.int32))
+    mgr.check_structure()
+    return _finish(f"chunked_prefill_s{len(chunk)}_T{t}_bs{block_size}_{kv_dtype}", seed, num_heads,
+                   num_kv_heads, head_dim, block_size, nb, mb, kc, vc, ks, vs, [step])
+
+
 WORKLOADS = {
     "tiny": tiny,
     "llama3_8b_decode": llama3_8b_decode,
@@ -395,4 +452,5 @@ WORKLOADS = {
     "shared_prefix_cow": shared_prefix_cow,
     "continuous_batching": continuous_batching,
     "sliding_window": sliding_window_decode,
+    "chunked_prefill": chunked_prefill,
 }

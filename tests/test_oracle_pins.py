@@ -559,3 +559,74 @@ def test_write_reports_per_head_amax():
     ka2 = torch.zeros(hk, dtype=torch.float64)
     oracle.reshape_and_cache(key, value, kc, vc, sm, 1.0, 1.0, w.k_head_scales, w.v_head_scales, ka2, None)
     assert torch.isnan(ka2[2]) and torch.equal(ka2[torch.arange(hk) != 2], ek[torch.arange(hk) != 2])
+
+
+# --- prefill / chunked prefill ------------------------------------------------------------
+
+def _prefill_small(seed=81, prefix=(0, 5, 13, 40), chunk=(7, 1, 20, 9), bs=4, kv="bf16", poison=True):
+    return wl.chunked_prefill(seed=seed, prefix_lens=prefix, chunk_lens=chunk, num_heads=4, num_kv_heads=2,
+                              head_dim=16, block_size=bs, kv_dtype=kv, poison=poison)
+
+
+def test_prefill_is_a_chain_of_decodes():
+    """Each new token's output equals, bit for bit, decode of one query over the
+    context cut at its own position (causal attention is decode at every position)."""
+    w = _prefill_small()
+    kc, vc = _materialize(w)
+    st = w.steps[0]
+    out = oracle.paged_attention_prefill(st.query, kc, vc, st.block_tables, st.context_lens, st.query_start_loc,
+                                         w.scale)
+    qsl = st.query_start_loc.tolist()
+    for s, L in enumerate(st.context_lens.tolist()):
+        n = qsl[s + 1] - qsl[s]
+        for i in range(n):
+            row = qsl[s] + i
+            ref = oracle.paged_attention_decode(st.query[row:row + 1], kc, vc, st.block_tables[s:s + 1],
+                                                torch.tensor([L - n + i + 1], dtype=torch.int32), w.scale)
+            assert torch.equal(out[row], ref[0]), (s, i)
+
+
+@pytest.mark.parametrize("bs", [4, 16])
+def test_prefill_equals_causal_sdpa(bs):
+    """Against torch's scaled_dot_product_attention in float64 with a causal mask
+    shifted by the cached prefix, on the gathered K/V of each sequence."""
+    w = _prefill_small(seed=82 + bs, prefix=(0, 3, 16, 33), chunk=(9, 17, 4, 30), bs=bs)
+    kc, vc = _materialize(w)
+    st = w.steps[0]
+    out = oracle.paged_attention_prefill(st.query, kc, vc, st.block_tables, st.context_lens, st.query_start_loc,
+                                         w.scale)
+    qsl = st.query_start_loc.tolist()
+    for s, L in enumerate(st.context_lens.tolist()):
+        n = qsl[s + 1] - qsl[s]
+        ks = torch.stack([_gather(kc, st.block_tables[s], k, L, bs) for k in range(2)]).double()
+        vs = torch.stack([_gather(vc, st.block_tables[s], k, L, bs) for k in range(2)]).double()
+        ks = ks.repeat_interleave(2, dim=0)[None]
+        vs = vs.repeat_interleave(2, dim=0)[None]
+        qs = st.query[qsl[s]:qsl[s + 1]].double().permute(1, 0, 2)[None]     # [1, Hq, n, D]
+        mask = torch.arange(L)[None, :] <= (L - n + torch.arange(n))[:, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(qs, ks, vs, attn_mask=mask, scale=w.scale)
+        assert torch.allclose(out[qsl[s]:qsl[s + 1]], ref[0].permute(1, 0, 2), rtol=0, atol=1e-12), s
+
+
+def test_prefill_of_one_token_is_decode():
+    """A chunk of one token per sequence is exactly the decode step."""
+    w = _prefill_small(seed=84, prefix=(3, 16, 40), chunk=(1, 1, 1))
+    kc, vc = _materialize(w)
+    st = w.steps[0]
+    pre = oracle.paged_attention_prefill(st.query, kc, vc, st.block_tables, st.context_lens, st.query_start_loc,
+                                         w.scale)
+    dec = oracle.paged_attention_decode(st.query, kc, vc, st.block_tables, st.context_lens, w.scale)
+    assert torch.equal(pre, dec)
+
+
+def test_prefill_first_token_of_a_prompt_returns_its_value():
+    """The first token of a fresh prompt sees only itself: its output is its V."""
+    w = _prefill_small(seed=85, prefix=(0, 0), chunk=(5, 12), kv="f32")
+    kc, vc = _materialize(w)
+    st = w.steps[0]
+    out = oracle.paged_attention_prefill(st.query, kc, vc, st.block_tables, st.context_lens, st.query_start_loc,
+                                         w.scale)
+    for s, q0 in enumerate(st.query_start_loc.tolist()[:-1]):
+        for h in range(4):
+            v = _gather(vc, st.block_tables[s], h // 2, 1, 4)[0].double()
+            assert torch.equal(out[q0, h], v)
