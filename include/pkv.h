@@ -12,7 +12,9 @@
  *   pkv_decode_step              the cache write and the decode of one step in one
  *                                call (the decode's preparation overlaps the write);
  *   pkv_paged_attention_decode_window  decode of a sliding-window layer (only the
- *                                last W positions; blocks before them never read).
+ *                                last W positions; blocks before them never read);
+ *   pkv_paged_attention_prefill  causal attention of a prompt's (or a prompt chunk's)
+ *                                new tokens over the cache.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -163,6 +165,40 @@ pkv_status pkv_paged_attention_decode_window(const pkv_tensor* out, const pkv_te
                                              int32_t num_kv_heads, float scale,
                                              int32_t block_size, int32_t max_blocks_per_seq,
                                              int32_t sliding_window, pkv_stream stream);
+
+/*
+ * pkv_paged_attention_prefill — causal attention of the new tokens of a prefill or
+ * chunked-prefill step over the paged cache.
+ *
+ * Defined by: ya.zerocoder.ru "Что такое PagedAttention", section "Зачем KV cache вообще
+ * нужен" (full causal attention: each token uses the keys and values of the positions
+ * before it, kept in the cache) with the block gather of pkv_paged_attention_decode.
+ *
+ * Sequence s has L = context_lens[s] tokens in the cache, the last n = qsl[s+1] - qsl[s]
+ * of them new this step (already written, e.g. by pkv_reshape_and_cache), where
+ * qsl = query_start_loc.  Query row r = qsl[s] + i (i < n) sits at position
+ * p = L - n + i and
+ *   out[r, h, :] = sum_{j <= p} softmax_j(scale * query[r, h, :] . K_s[j]) * V_s[j]
+ * with K_s, V_s gathered through the block table as for decode (KV head h / (Hq / Hk)).
+ * n = 0 is allowed; n > L or L past the table sets PKV_DEVERR_CONTEXT_LEN and leaves the
+ * sequence's rows unwritten.
+ *
+ * out, query     [num_tokens, num_heads, head_dim] bf16, last dim contiguous; rows of
+ *                each sequence packed in order (num_tokens = qsl[num_seqs]).
+ * key_cache,
+ * value_cache    bf16, layout as for decode.
+ * block_tables   [num_seqs, max_blocks_per_seq] int32 (max_blocks_per_seq <= 8192).
+ * context_lens   [num_seqs] int32; query_start_loc [num_seqs + 1] int32, contiguous,
+ *                non-decreasing, starting at 0.
+ * Supported: bf16, head_dim 64/128, block size 8/16/32; otherwise PKV_ERR_UNSUPPORTED.
+ */
+pkv_status pkv_paged_attention_prefill(const pkv_tensor* out, const pkv_tensor* query,
+                                       const pkv_tensor* key_cache, const pkv_tensor* value_cache,
+                                       const pkv_tensor* block_tables,
+                                       const pkv_tensor* context_lens,
+                                       const pkv_tensor* query_start_loc, int32_t num_kv_heads,
+                                       float scale, int32_t block_size, int32_t max_blocks_per_seq,
+                                       pkv_stream stream);
 
 /*
  * pkv_reshape_and_cache — write new tokens' K and V into their cache slots.

@@ -63,12 +63,14 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.pkv_paged_attention_decode_noalloc.argtypes = [d, d, d, d, d, d, i32, f32, i32, i32, vp]
         lib.pkv_decode_step.argtypes = [d, d, d, d, d, d, d, d, d, i32, f32, i32, i32, i32, vp]
         lib.pkv_reshape_and_cache_amax.argtypes = [d, d, d, d, d, vp, vp, vp]
+        lib.pkv_paged_attention_prefill.argtypes = [d, d, d, d, d, d, d, i32, f32, i32, i32, vp]
         lib.pkv_paged_attention_decode_window.argtypes = [d, d, d, d, d, d, i32, f32, i32, i32, i32, vp]
         lib.pkv_noalloc_scratch_bytes.restype = i64
         lib.pkv_noalloc_scratch_bytes.argtypes = []
         for fn in ("pkv_paged_attention_decode", "pkv_paged_attention_decode_noalloc",
                    "pkv_reshape_and_cache", "pkv_decode_step", "pkv_copy_blocks",
                    "pkv_paged_attention_decode_window", "pkv_reshape_and_cache_amax",
+                   "pkv_paged_attention_prefill",
                    "pkv_set_option", "pkv_reserve_workspace", "pkv_read_device_errors"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.pkv_last_error.restype = ctypes.c_char_p
@@ -161,6 +163,20 @@ def decode_step(out, query, key, value, slot_mapping, key_cache, value_cache, bl
              describe(block_tables), describe(context_lens)]
     _check(lib.pkv_decode_step(*[ctypes.byref(x) for x in descs], int(num_kv_heads), float(scale),
                                int(block_size), int(max_blocks_per_seq), int(sliding_window), _stream(stream)))
+    return out
+
+
+def paged_attention_prefill(out, query, key_cache, value_cache, block_tables, context_lens, query_start_loc,
+                            num_kv_heads: int, scale: float, block_size: int, max_blocks_per_seq: int,
+                            stream=None) -> torch.Tensor:
+    """Causal attention of the packed new tokens of every sequence (rows
+    query_start_loc[s] .. query_start_loc[s+1]-1, the last of its context_lens[s]
+    cached positions) over the paged cache, into ``out`` (returned)."""
+    lib = load_library()
+    descs = [describe(out), describe(query), describe(key_cache), describe(value_cache), describe(block_tables),
+             describe(context_lens), describe(query_start_loc)]
+    _check(lib.pkv_paged_attention_prefill(*[ctypes.byref(x) for x in descs], int(num_kv_heads), float(scale),
+                                           int(block_size), int(max_blocks_per_seq), _stream(stream)))
     return out
 
 

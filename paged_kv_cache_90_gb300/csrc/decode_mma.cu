@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "decode_mma.cuh"
+#include "prefill_mma.cuh"
 
 namespace pkv {
 
@@ -320,7 +321,61 @@ size_t smem_for(int G, int S) {
   }
 }
 
+template <int D, int GC>
+cudaError_t launch_prefill_tpl(const DecodeParams& p, cudaStream_t stream) {
+  using C = prefill::PCfg<D, GC>;
+  const int box_rows = p.block_size < mma::kST ? p.block_size : mma::kST;
+  CUtensorMap mk, mv;
+  cudaError_t e = cached_cache_map(&mk, p.key_cache, p, box_rows);
+  if (e != cudaSuccess) return e;
+  if ((e = cached_cache_map(&mv, p.value_cache, p, box_rows)) != cudaSuccess) return e;
+  const size_t smem = C::smem_bytes(p.max_blocks_per_seq);
+  auto kern = prefill::paged_prefill_kernel<D, GC>;
+  static size_t smem_set[kMapCacheDevices] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMapCacheDevices || smem > smem_set[dev]) {
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) != cudaSuccess)
+      return e;
+    if (dev >= 0 && dev < kMapCacheDevices) smem_set[dev] = smem;
+  }
+  // one block per (query tile, group of GC heads); the tiles of all sequences number at
+  // most ceil(T / TQ) + S, surplus blocks exit at once
+  const dim3 grid(unsigned((p.num_tokens + C::kTQ - 1) / C::kTQ + p.num_seqs), unsigned(p.num_heads / GC));
+  kern<<<grid, C::kThreads, smem, stream>>>(mk, mv, p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// query heads of a KV head's group that one prefill block takes: the largest of 8, 4,
+// 2, 1 that divides the group
+int prefill_heads_per_block(int group) {
+  for (int gc : {8, 4, 2}) if (group % gc == 0) return gc;
+  return 1;
+}
+
 }  // namespace
+
+bool prefill_supported(const DecodeParams& p) {
+  if (p.q_dtype != kBF16 || p.out_dtype != kBF16 || p.kv_dtype != kBF16) return false;
+  if (!(p.head_dim == 64 || p.head_dim == 128)) return false;
+  if (!(p.block_size == 8 || p.block_size == 16 || p.block_size == 32)) return false;
+  if (p.max_blocks_per_seq > kPrefillMaxTableEntries) return false;
+  if (!encode_fn()) return false;
+  if ((reinterpret_cast<uintptr_t>(p.query) & 15) || (p.q_stride_s & 7) || (p.q_stride_h & 7)) return false;
+  if ((reinterpret_cast<uintptr_t>(p.out) & 15) || (p.out_stride_s & 7) || (p.out_stride_h & 7)) return false;
+  return true;
+}
+
+cudaError_t launch_prefill(const DecodeParams& p, cudaStream_t stream) {
+  const int gc = prefill_heads_per_block(p.group);
+#define PKV_PREFILL_CASE(DD, GG) \
+  if (p.head_dim == DD && gc == GG) return launch_prefill_tpl<DD, GG>(p, stream);
+  PKV_PREFILL_CASE(128, 8) PKV_PREFILL_CASE(128, 4) PKV_PREFILL_CASE(128, 2) PKV_PREFILL_CASE(128, 1)
+  PKV_PREFILL_CASE(64, 8) PKV_PREFILL_CASE(64, 4) PKV_PREFILL_CASE(64, 2) PKV_PREFILL_CASE(64, 1)
+#undef PKV_PREFILL_CASE
+  return cudaErrorInvalidValue;
+}
 
 int mma_heads_per_item(int group) {
   if (group % 16 == 0) return 16;

@@ -577,6 +577,82 @@ pkv_status pkv_paged_attention_decode_window(const pkv_tensor* out, const pkv_te
   return finish_call(s, launch_decode(p, cs), cs, "paged_attention_decode");
 }
 
+pkv_status pkv_paged_attention_prefill(const pkv_tensor* out, const pkv_tensor* query,
+                                       const pkv_tensor* key_cache, const pkv_tensor* value_cache,
+                                       const pkv_tensor* block_tables, const pkv_tensor* context_lens,
+                                       const pkv_tensor* query_start_loc, int32_t num_kv_heads, float scale,
+                                       int32_t block_size, int32_t max_blocks_per_seq, pkv_stream stream) {
+  pkv_status st;
+  if ((st = check_basic(out, "out", 3)) || (st = check_basic(query, "query", 3)) ||
+      (st = check_cache(key_cache, "key_cache")) || (st = check_cache(value_cache, "value_cache")) ||
+      (st = check_basic(block_tables, "block_tables", 2)) ||
+      (st = check_basic(context_lens, "context_lens", 1)) ||
+      (st = check_basic(query_start_loc, "query_start_loc", 1)))
+    return st;
+  if ((st = check_dtype(query, "query", PKV_BF16))) return st;
+  if ((st = check_dtype(out, "out", PKV_BF16))) return st;
+  if ((st = check_dtype(key_cache, "key_cache", PKV_BF16))) return st;
+  if ((st = check_dtype(block_tables, "block_tables", PKV_I32))) return st;
+  if ((st = check_dtype(context_lens, "context_lens", PKV_I32))) return st;
+  if ((st = check_dtype(query_start_loc, "query_start_loc", PKV_I32))) return st;
+  const int64_t T = query->shape[0], Hq = query->shape[1], D = query->shape[2];
+  const int64_t S = block_tables->shape[0];
+  if (out->shape[0] != T || out->shape[1] != Hq || out->shape[2] != D)
+    return fail(PKV_ERR_INVALID_ARG, "out shape must equal query shape");
+  if (!same_layout(key_cache, value_cache))
+    return fail(PKV_ERR_INVALID_ARG, "key_cache and value_cache must share dtype, shape and strides");
+  if (num_kv_heads <= 0 || key_cache->shape[1] != num_kv_heads || Hq % num_kv_heads)
+    return fail(PKV_ERR_INVALID_ARG, "num_kv_heads must equal key_cache.shape[1] and divide num_heads");
+  if (key_cache->shape[2] != block_size || key_cache->shape[3] != D)
+    return fail(PKV_ERR_INVALID_ARG, "block_size / head_dim must match the cache");
+  if (block_tables->shape[1] != max_blocks_per_seq || max_blocks_per_seq < 1)
+    return fail(PKV_ERR_INVALID_ARG, "block_tables must be [num_seqs, max_blocks_per_seq]");
+  if (context_lens->shape[0] != S || query_start_loc->shape[0] != S + 1 ||
+      (S > 0 && query_start_loc->stride[0] != 1))
+    return fail(PKV_ERR_INVALID_ARG, "context_lens must be [num_seqs], query_start_loc a contiguous [num_seqs + 1]");
+  if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale must be finite");
+  if (T > 0x7fffffff / 2 || S > 65535 || Hq > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many tokens, sequences or heads");
+  DecodeParams p{};
+  p.out = out->data;
+  p.out_dtype = out->dtype;
+  p.out_stride_s = out->stride[0];
+  p.out_stride_h = out->stride[1];
+  p.query = query->data;
+  p.q_dtype = query->dtype;
+  p.q_stride_s = query->stride[0];
+  p.q_stride_h = query->stride[1];
+  p.key_cache = key_cache->data;
+  p.value_cache = value_cache->data;
+  p.kv_dtype = key_cache->dtype;
+  p.cs_block = key_cache->stride[0];
+  p.cs_head = key_cache->stride[1];
+  p.block_tables = static_cast<const int32_t*>(block_tables->data);
+  p.bt_stride = block_tables->stride[0];
+  p.context_lens = static_cast<const int32_t*>(context_lens->data);
+  p.query_start_loc = static_cast<const int32_t*>(query_start_loc->data);
+  p.num_seqs = int(S);
+  p.num_tokens = int(T);
+  p.num_heads = int(Hq);
+  p.num_kv_heads = num_kv_heads;
+  p.head_dim = int(D);
+  p.block_size = block_size;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_blocks = key_cache->shape[0];
+  p.group = int(Hq / num_kv_heads);
+  p.qk_scale_log2 = float(double(scale) * 1.4426950408889634);
+  p.v_scale = 1.0f;
+  if (!prefill_supported(p))
+    return fail(PKV_ERR_UNSUPPORTED, "prefill needs bf16 queries, outputs and caches, head_dim 64/128, block size "
+                "8/16/32, at most %d table entries per sequence, 16-byte aligned query/out rows",
+                kPrefillMaxTableEntries);
+  if (g_opt_dry_run.load() || S == 0 || T == 0) return PKV_OK;
+  DeviceState* ds;
+  if ((st = device_state(&ds))) return st;
+  p.err = ds->err;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  return finish_call(ds, launch_prefill(p, cs), cs, "paged_attention_prefill");
+}
+
 pkv_status pkv_reshape_and_cache(const pkv_tensor* key, const pkv_tensor* value,
                                  const pkv_tensor* key_cache, const pkv_tensor* value_cache,
                                  const pkv_tensor* slot_mapping, pkv_stream stream) {

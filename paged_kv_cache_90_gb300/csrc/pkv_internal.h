@@ -79,6 +79,8 @@ struct DecodeParams {
   const float* k_head_scales;  // e4m3 cache: [Hk] per-head scales (or null)
   const float* v_head_scales;
   int sliding_window;        // attend to the last W positions only (0: all)
+  const int32_t* query_start_loc;  // prefill: [S + 1] packed query rows of each sequence
+  int num_tokens;            // prefill: packed query rows
   int partition_tokens;      // multiple of 256
   int max_partitions;        // ceil(max_blocks_per_seq * block_size / partition_tokens)
   int64_t partial_rows;      // rows of the partial arrays (0: none)
@@ -131,6 +133,11 @@ int mma_heads_per_item(int group);
 bool mma_decode_supported(const DecodeParams& p);
 constexpr int kMmaWarps = 8;  // warps per thread block of the tensor-core kernel
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream);
+// Prefill (prefill_mma.cuh, launched from decode_mma.cu): whether it handles a call,
+// and its launch.
+bool prefill_supported(const DecodeParams& p);
+cudaError_t launch_prefill(const DecodeParams& p, cudaStream_t stream);
+constexpr int kPrefillMaxTableEntries = 8192;  // block-table entries a prefill CTA holds
 
 // Per-dtype launchers (one translation unit each).
 cudaError_t launch_decode_f32(const DecodeParams& p, int g, cudaStream_t stream);

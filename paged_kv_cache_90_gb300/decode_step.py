@@ -28,12 +28,13 @@ class DeviceStep:
     block_tables: torch.Tensor
     context_lens: torch.Tensor
     cow_pairs: torch.Tensor
+    query_start_loc: Optional[torch.Tensor] = None   # prefill steps only
 
     @staticmethod
     def from_host(st: DecodeStep, device, pin: bool = False) -> "DeviceStep":
         def mv(t):
-            return t.to(device, non_blocking=pin)
-        return DeviceStep(*(mv(getattr(st, f)) for f in DeviceStep.__dataclass_fields__))
+            return None if t is None else t.to(device, non_blocking=pin)
+        return DeviceStep(*(mv(getattr(st, f, None)) for f in DeviceStep.__dataclass_fields__))
 
 
 class DeviceWorkload:
@@ -48,7 +49,7 @@ class DeviceWorkload:
         self.k_head_scales = None if w.k_head_scales is None else w.k_head_scales.to(self.device)
         self.v_head_scales = None if w.v_head_scales is None else w.v_head_scales.to(self.device)
         self.steps: List[DeviceStep] = [DeviceStep.from_host(st, self.device) for st in w.steps]
-        s, hq, d = w.steps[0].query.shape
+        s, hq, d = w.steps[0].query.shape   # (packed query rows for a prefill)
         self.out = torch.empty(s, hq, d, dtype=w.q_dtype, device=self.device)
 
     def run_step(self, i: int, out: Optional[torch.Tensor] = None, stream=None,
@@ -68,6 +69,14 @@ def run_decode_step(w: Workload, key_cache, value_cache, st: DeviceStep, out, st
     if st.cow_pairs.numel():
         binding.copy_blocks(key_cache, st.cow_pairs, stream)
         binding.copy_blocks(value_cache, st.cow_pairs, stream)
+    if st.query_start_loc is not None:   # prefill: write every new token, then attend causally
+        if st.slot_mapping.numel():
+            binding.reshape_and_cache(st.new_key, st.new_value, key_cache, value_cache, st.slot_mapping,
+                                      w.k_scale, w.v_scale, stream, k_head_scales, v_head_scales)
+        binding.paged_attention_prefill(out, st.query, key_cache, value_cache, st.block_tables, st.context_lens,
+                                        st.query_start_loc, w.num_kv_heads, w.scale, w.block_size,
+                                        w.max_blocks_per_seq, stream)
+        return
     if joint:
         binding.decode_step(out, st.query, st.new_key, st.new_value, st.slot_mapping, key_cache, value_cache,
                             st.block_tables, st.context_lens, w.num_kv_heads, w.scale, w.block_size,

@@ -102,6 +102,30 @@ def weighted_abs_values(w, st, kc, vc):
     return out
 
 
+def weighted_abs_values_prefill(w, st, kc, vc):
+    """sum_j p_j |V_j| for every packed query row of a prefill step (causal softmax over
+    positions 0..p), in fp64 with torch."""
+    T, hq, d = st.query.shape
+    hk, bs = w.num_kv_heads, w.block_size
+    g = hq // hk
+    out = torch.zeros(T, hq, d, dtype=torch.float64)
+    qsl = st.query_start_loc.tolist()
+    for s in range(len(qsl) - 1):
+        L, n = int(st.context_lens[s]), qsl[s + 1] - qsl[s]
+        if n == 0:
+            continue
+        nb = -(-L // bs)
+        blocks = st.block_tables[s, :nb].long()
+        K = gather_blocks(kc, blocks).double().permute(1, 0, 2, 3).reshape(hk, nb * bs, d)[:, :L]
+        V = gather_blocks(vc, blocks).double().permute(1, 0, 2, 3).reshape(hk, nb * bs, d)[:, :L].abs()
+        q = st.query[qsl[s]:qsl[s + 1]].double().view(n, hk, g, d).permute(1, 2, 0, 3)   # [hk, g, n, d]
+        z = w.scale * q @ K.transpose(1, 2)[:, None]                                      # [hk, g, n, L]
+        mask = torch.arange(L)[None, :] > (L - n + torch.arange(n))[:, None]
+        p = torch.softmax(z.masked_fill(mask, float("-inf")), dim=-1)
+        out[qsl[s]:qsl[s + 1]] = (p @ V[:, None]).permute(2, 0, 1, 3).reshape(n, hq, d)
+    return out
+
+
 def assert_decode_close(got, ref, w, wabs=None):
     err = (got - ref).abs()
     assert torch.isfinite(got).all()
@@ -125,7 +149,11 @@ def check_workload(w):
     routs, wabs = [], []
     for i in range(len(w.steps)):
         routs.append(oracle.run_workload_step(w, i, kc0, vc0, THREADS))
-        wabs.append(weighted_abs_values(w, w.steps[i], kc0, vc0) if w.q_dtype == torch.bfloat16 else None)
+        wa = None
+        if w.q_dtype == torch.bfloat16:
+            wa = (weighted_abs_values_prefill if w.steps[i].query_start_loc is not None
+                  else weighted_abs_values)(w, w.steps[i], kc0, vc0)
+        wabs.append(wa)
     assert torch.equal(raw(kc), raw(kc0)), "key cache differs from the oracle's"
     assert torch.equal(raw(vc), raw(vc0)), "value cache differs from the oracle's"
     for got, ref, wa in zip(outs, routs, wabs):
@@ -200,6 +228,40 @@ def test_continuous_batching_small(bs, kv, kernel):
 @pytest.mark.parametrize("bs", [8, 16, 32])
 def test_continuous_batching_full(bs, kv, kernel):
     check_workload(wl.continuous_batching(block_size=bs, kv_dtype=kv))
+
+
+# --- prefill / chunked prefill ----------------------------------------------------
+
+@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("heads", [(32, 8), (16, 16), (16, 8), (32, 2), (12, 4)])
+def test_prefill_small(bs, heads):
+    """Prompts and later chunks of different lengths (tile edges, prefixes off the
+    stage grid), GQA groups 1 to 16, every unused slot NaN."""
+    hq, hk = heads
+    check_workload(wl.chunked_prefill(seed=90 + bs + hq + hk, prefix_lens=(0, 0, 5, 37, 16, 200, 0),
+                                      chunk_lens=(1, 17, 33, 64, 127, 40, 130), num_heads=hq, num_kv_heads=hk,
+                                      head_dim=128 if hq != 12 else 64, block_size=bs, poison=True))
+
+
+def test_prefill_empty_chunk_and_single_tokens():
+    """A sequence with no new token leaves nothing to write; one-token chunks equal
+    decode (checked against the oracle like every prefill)."""
+    check_workload(wl.chunked_prefill(seed=95, prefix_lens=(10, 300, 0, 47), chunk_lens=(1, 1, 1, 1), poison=True))
+    w = wl.chunked_prefill(seed=96, prefix_lens=(10, 20, 30), chunk_lens=(5, 1, 9), poison=True)
+    st = w.steps[0]
+    # drop the middle sequence's chunk: its context shrinks to its prefix, no rows
+    keep = torch.tensor([0, 1, 2, 3, 4, 6, 7, 8, 9, 10, 11, 12, 13, 14])
+    st.query, st.new_key, st.new_value = st.query[keep], st.new_key[keep], st.new_value[keep]
+    st.slot_mapping = st.slot_mapping[keep]
+    st.context_lens = torch.tensor([15, 20, 39], dtype=torch.int32)
+    st.query_start_loc = torch.tensor([0, 5, 5, 14], dtype=torch.int32)
+    check_workload(w)
+
+
+def test_prefill_full():
+    """Llama-3-8B-shaped prefill: two 2048-token prompts and two 512-token chunks of
+    long prompts (prefixes 512 and 1536)."""
+    check_workload(wl.chunked_prefill())
 
 
 @pytest.mark.parametrize("bs", [8, 16, 32])
