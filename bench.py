@@ -65,6 +65,12 @@ def make_workload(name: str, rank: int = 0) -> wl.Workload:
     m = re.fullmatch(r"sliding_window(?:_bs(\d+))?", name)
     if m:   # Mistral-style 4096-position window over 8 x 32768-token contexts
         return wl.sliding_window_decode(seed=6 + seed_off, block_size=int(m.group(1) or 16))
+    if name == "chunked_prefill":  # two 2048-token prompts, two 512-token chunks after 512 / 1536 cached
+        return wl.chunked_prefill(seed=7 + seed_off)
+    m = re.fullmatch(r"prefill_(\d+)x(\d+)", name)
+    if m:   # N fresh prompts of T tokens each
+        n, t = int(m.group(1)), int(m.group(2))
+        return wl.chunked_prefill(seed=8 + seed_off, prefix_lens=[0] * n, chunk_lens=[t] * n)
     if name == "tiny":
         return wl.tiny(seed=1 + seed_off)
     raise SystemExit(f"unknown workload {name}")
@@ -72,6 +78,12 @@ def make_workload(name: str, rank: int = 0) -> wl.Workload:
 
 def describe_workload(w: wl.Workload, name: str) -> str:
     L = torch.cat([st.context_lens for st in w.steps]).float()
+    if w.steps[0].query_start_loc is not None:
+        st = w.steps[0]
+        return (f"{name}: {st.context_lens.numel()} seqs, {st.query.shape[0]} new tokens (chunks "
+                f"{(st.query_start_loc[1:] - st.query_start_loc[:-1]).tolist()}), contexts "
+                f"{st.context_lens.tolist()}, {w.num_heads}/{w.num_kv_heads} heads, head_dim {w.head_dim}, "
+                f"{wl.DTYPE_NAMES[w.kv_dtype]} KV, block {w.block_size}")
     return (f"{name}: {w.num_seqs} seqs, {w.num_heads}/{w.num_kv_heads} heads, head_dim {w.head_dim}, "
             f"{wl.DTYPE_NAMES[w.kv_dtype]} KV, block {w.block_size}, ctx mean {L.mean():.0f} "
             f"[{int(L.min())}, {int(L.max())}], {len(w.steps)} distinct step(s)")
@@ -224,6 +236,160 @@ def oracle_throughput(w: wl.Workload, budget_s: float, max_seqs=None):
     return done_bytes / elapsed / 1e9, threads, desc
 
 
+# ---- prefill: causal attention of new tokens, a tensor-core contraction ---------------
+
+PREFILL_METRIC = "paged prefill attention: causal attention TFLOP/s (fp32 accumulate)"
+
+
+def is_prefill(w: wl.Workload) -> bool:
+    return w.steps[0].query_start_loc is not None
+
+
+def prefill_flops(w: wl.Workload, st) -> int:
+    """Multiply-adds of a prefill step, two flops each: every new token at position p
+    scores p + 1 keys (D each) and sums p + 1 values (D each), in every query head."""
+    qsl = st.query_start_loc.tolist()
+    total = 0
+    for s, L in enumerate(st.context_lens.tolist()):
+        n = qsl[s + 1] - qsl[s]
+        pairs = n * (L - n) + n * (n + 1) // 2     # sum over the new tokens of (p + 1)
+        total += 4 * w.head_dim * w.num_heads * pairs
+    return total
+
+
+def oracle_prefill_throughput(w: wl.Workload, budget_s: float):
+    """TFLOP/s of the CPU oracle's prefill on the first sequence(s) of the step."""
+    import oracle
+    oracle.build()
+    threads = len(os.sched_getaffinity(0))
+    st = w.steps[0]
+    kc, vc = w.key_cache.clone(), w.value_cache.clone()
+    oracle.reshape_and_cache(st.new_key, st.new_value, kc, vc, st.slot_mapping, w.k_scale, w.v_scale)
+    qsl = st.query_start_loc
+    done, elapsed, reps, n = 0, 0.0, 0, 1
+    sub_qsl = qsl[:n + 1].clone()
+    sub = wl.DecodeStep(st.query[:int(sub_qsl[-1])], st.new_key[:0], st.new_value[:0], st.slot_mapping[:0],
+                        st.block_tables[:n], st.context_lens[:n], st.cow_pairs[:0], sub_qsl)
+    while True:
+        t = time.perf_counter()
+        oracle.paged_attention_prefill(sub.query, kc, vc, sub.block_tables, sub.context_lens, sub.query_start_loc,
+                                       w.scale, w.k_scale, w.v_scale, threads)
+        elapsed += time.perf_counter() - t
+        done += prefill_flops(w, sub)
+        reps += 1
+        if elapsed >= budget_s or reps >= 1000:
+            break
+    desc = (f"fp64 C oracle prefill of the first sequence ({int(sub_qsl[-1])} new tokens) x {reps} "
+            f"repetition(s), {elapsed:.1f} s")
+    return done / elapsed / 1e12, threads, desc
+
+
+def run_prefill_gpu(args, world, rank, local, w, dw, dev, flush_l2, barrier):
+    """Steps = the new tokens' cache write + causal prefill attention."""
+    stream = torch.cuda.current_stream(dev)
+    st = dw.steps[0]
+    for _ in range(args.warmup):
+        flush_l2()
+        dw.run_step(0)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
+                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    n0 = binding.launch_count()
+    t0 = time.time()
+    for k in range(args.steps):
+        flush_l2()
+        a, c = ev[k]
+        a.record(stream)
+        dw.run_step(0)                 # cache write of the new tokens, then prefill attention
+        c.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    launches = binding.launch_count() - n0
+    total_ms = sum(a.elapsed_time(c) for a, c in ev)
+    # the prefill kernel alone, for the roofline
+    pre_steps = min(args.steps, 200)
+    for k in range(pre_steps):
+        flush_l2()
+        a, c = ev[k]
+        a.record(stream)
+        binding.paged_attention_prefill(dw.out, st.query, dw.key_cache, dw.value_cache, st.block_tables,
+                                        st.context_lens, st.query_start_loc, w.num_kv_heads, w.scale, w.block_size,
+                                        w.max_blocks_per_seq)
+        c.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    time.sleep(0.2)
+    clocks.stop()
+    pre_ms = sum(a.elapsed_time(c) for a, c in ev[:pre_steps]) / pre_steps
+    flops = prefill_flops(w, w.steps[0])
+    my = torch.tensor([total_ms, float(flops * args.steps)], dtype=torch.float64)
+    if world > 1:
+        import torch.distributed as dist
+        t_ = my.to(dev)
+        dist.all_reduce(t_[:1], op=dist.ReduceOp.MAX)
+        dist.all_reduce(t_[1:], op=dist.ReduceOp.SUM)
+        my = t_.cpu()
+    max_ms, all_flops = float(my[0]), float(my[1])
+    value = all_flops / (max_ms * 1e-3) / 1e12
+    # end to end: step inputs from pinned host memory, output back
+    fields = ("query", "new_key", "new_value", "slot_mapping", "block_tables", "context_lens", "cow_pairs",
+              "query_start_loc")
+    hs = DeviceStep(*(getattr(w.steps[0], f).pin_memory() for f in fields))
+    di = DeviceStep(*(torch.empty_like(getattr(w.steps[0], f), device=dev) for f in fields))
+    out_host = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
+    h2d = sum(getattr(hs, f).numel() * getattr(hs, f).element_size() for f in fields)
+    d2h = out_host.numel() * out_host.element_size()
+    e_ms, e_steps = 0.0, max(5, min(args.steps, 50))
+    for k in range(e_steps + 3):
+        flush_l2()
+        a, c = ev[k % len(ev)]
+        a.record(stream)
+        for f in fields:
+            getattr(di, f).copy_(getattr(hs, f), non_blocking=True)
+        run_decode_step(w, dw.key_cache, dw.value_cache, di, dw.out)
+        out_host.copy_(dw.out, non_blocking=True)
+        c.record(stream)
+        c.synchronize()
+        if k >= 3:
+            e_ms += a.elapsed_time(c)
+    e2e = flops * e_steps / (e_ms * 1e-3) / 1e12
+    if rank != 0:
+        return 0
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, peak_kind = float(json.load(f)["bf16_tflops"]), "measured (bf16 dense, burst)"
+    except Exception:
+        peak, peak_kind = 1900.0, "fallback"
+    achieved = flops / (pre_ms * 1e-3) / 1e12
+    cpu_base = None
+    if world == 1 and not args.no_cpu_baseline:
+        g, threads, desc = oracle_prefill_throughput(w, args.cpu_budget)
+        cpu_base = {"value": round(g, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
+    line = {
+        "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": describe_workload(w, args.workload),
+                   "new_tokens": int(st.query.shape[0]), "flops_per_step": flops,
+                   "l2": "flushed between steps (256 MiB write + 256 MiB read, untimed)", "accumulate": "f32",
+                   "prefill_us": round(pre_ms * 1e3, 2), "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "paged_prefill_kernel (mma.sync bf16)", "peak_kind": peak_kind},
+        "cpu_baseline": cpu_base,
+        "e2e": {"value": round(e2e, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(launches),
+        "clocks": clocks.summary(t0, t1),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ---- the two arms --------------------------------------------------------------------
 
 def init_dist(args):
@@ -245,6 +411,22 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     w = make_workload(args.workload)
+    if is_prefill(w):
+        vals = []
+        for i in range(args.warmup + args.steps):
+            g, threads, desc = oracle_prefill_throughput(w, 120.0 / (args.warmup + args.steps))
+            if i >= args.warmup:
+                vals.append(g)
+        value = statistics.median(vals)
+        line = {"impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": describe_workload(w, args.workload), "l2": "n/a (host)"},
+                "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                 "sample": "each step: " + desc},
+                "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
     steps = args.warmup + args.steps
     # calibrate: one sequence, then size the per-step sample to fit ~2 minutes overall
     gbs1, threads, _ = oracle_throughput(w, 0.0, max_seqs=1)
@@ -298,6 +480,9 @@ def run_gpu(args, world, rank, local):
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
+
+    if is_prefill(w):
+        return run_prefill_gpu(args, world, rank, local, w, dw, dev, flush_l2, barrier)
 
     # ---- device-resident timing (value) ----
     for i in range(args.warmup):
