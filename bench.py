@@ -10,12 +10,17 @@ decode layer (64 sequences, contexts uniform in [128, 2048] plus the new token,
 Metric: effective GB/s = algorithmic bytes of a step / step time, where the bytes are
 those the step must move: every context token's K and V (for its KV head), the
 queries, the outputs, the block-table entries and lengths, the new tokens read and
-written, and the copied blocks.  Timing: CUDA events on the launching stream around
-each step, the L2 flushed between steps outside the events (a 256 MiB write, then a
-256 MiB read so that the write's dirty lines are written back before the step starts).
-A step issues the cache write and the decode as one pkv_decode_step call.  The roofline
-entry times the decode kernels alone (main kernel + merge of split rows) in a second
-loop of decode calls on the same resident caches, bracketed the same way.
+written, and the copied blocks.  Timing: CUDA events on the launching stream.  A step
+that reads more than twice the L2 (the Llama-3-8B, long-context and continuous-batching
+workloads) runs back to back with the others between two events: its K/V are streamed
+with an evict-first policy, so no step finds the previous one's data in L2.  Smaller
+steps, and steps whose sequences share blocks, are timed one by one with the L2 flushed
+between them outside the events (a 256 MiB write, then a 256 MiB read so that the
+write's dirty lines are written back before the step starts); the flushed per-step
+figures of the large workloads are reported beside the back-to-back ones.  A step issues
+the cache write and the decode as one pkv_decode_step call.  The roofline entry times
+the decode kernels alone (main kernel + merge of split rows) in a second loop of decode
+calls on the same resident caches, timed the same way.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 """
@@ -485,9 +490,20 @@ def run_gpu(args, world, rank, local):
         return run_prefill_gpu(args, world, rank, local, w, dw, dev, flush_l2, barrier)
 
     # ---- device-resident timing (value) ----
+    # Steps that read more than twice the L2 run back to back (their K/V are streamed with
+    # an evict-first policy, so a step does not find the previous one's data in L2);
+    # smaller ones, and steps that share blocks between sequences, flush the L2 between
+    # steps outside the timed events.
+    try:
+        l2_bytes = int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    except Exception:
+        l2_bytes = 129 << 20
+    joint = STEP_MODES[args.step_mode]
+    step0_bytes = decode_bytes(w, w.steps[0])
+    back_to_back = step0_bytes > 2 * l2_bytes and not any(st.cow_pairs.numel() for st in w.steps)
     for i in range(args.warmup):
         flush_l2()
-        dw.run_step(i % nsteps)
+        dw.run_step(i % nsteps, joint=joint)
     torch.cuda.synchronize(dev)
     clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local)
@@ -497,43 +513,65 @@ def run_gpu(args, world, rank, local):
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize(dev)
-    n0 = binding.launch_count()
-    t0 = time.time()
-    for k in range(args.steps):
-        flush_l2()
-        a, _, c = ev[k]
-        a.record(stream)
-        dw.run_step(k % nsteps)        # CoW copies, then the cache write and decode in one call
-        c.record(stream)
-    torch.cuda.synchronize(dev)
-    t1 = time.time()
-    launches = binding.launch_count() - n0
-    step_ms = [a.elapsed_time(c) for a, _, c in ev]
-    total_ms = sum(step_ms)
-    # the decode kernels alone (main + merge), for the roofline: the same calls on the
-    # same resident caches, each bracketed by events on the launching stream
-    dec_steps = min(args.steps, 500)
-    for k in range(dec_steps):
-        flush_l2()
+    def decode_call(k):
         st = dw.steps[k % nsteps]
-        _, b, c = ev[k]
-        b.record(stream)
         binding.paged_attention_decode(dw.out, st.query, dw.key_cache, dw.value_cache, st.block_tables,
                                        st.context_lens, w.num_kv_heads, w.scale, w.block_size,
                                        w.max_blocks_per_seq, w.k_scale, w.v_scale, None, w.sliding_window,
                                        dw.k_head_scales, dw.v_head_scales)
+
+    def time_flushed(fn, count):
+        """Per-call times (ms), the L2 flushed before each call, outside its events."""
+        for k in range(count):
+            flush_l2()
+            a, _, c = ev[k]
+            a.record(stream)
+            fn(k)
+            c.record(stream)
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(c) for a, _, c in ev[:count]]
+
+    def time_back_to_back(fn, count):
+        """Total time (ms) of `count` calls queued back to back between two events."""
+        a, _, c = ev[0]
+        a.record(stream)
+        for k in range(count):
+            fn(k)
         c.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(c)
+
+    def step_call(k):
+        dw.run_step(k % nsteps, joint=joint)  # CoW copies, then the cache write and the decode
+
+    n0 = binding.launch_count()
+    t0 = time.time()
+    if back_to_back:
+        total_ms = time_back_to_back(step_call, args.steps)
+    else:
+        total_ms = sum(time_flushed(step_call, args.steps))
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    launches = binding.launch_count() - n0
+    # the decode kernels alone (main + merge), for the roofline: the same calls on the
+    # same resident caches, timed the same way
+    dec_steps = min(args.steps, 500)
+    if back_to_back:
+        dec_ms = [time_back_to_back(decode_call, dec_steps) / dec_steps]
+        flushed_step_ms = statistics.mean(time_flushed(step_call, min(args.steps, 500)))
+        flushed_dec_ms = statistics.mean(time_flushed(decode_call, dec_steps))
+    else:
+        dec_ms = time_flushed(decode_call, dec_steps)
     torch.cuda.synchronize(dev)
     barrier()
     time.sleep(0.2)
     clocks.stop()
-    dec_ms = [b.elapsed_time(c) for _, b, c in ev[:dec_steps]]
     flags = binding.read_device_errors()
     if flags:
         raise SystemExit(f"device error word 0x{flags:x} during the bench")
 
     bytes_steps = [step_bytes(w, w.steps[k % nsteps]) for k in range(args.steps)]
-    dec_bytes = [decode_bytes(w, w.steps[k % nsteps]) for k in range(dec_steps)]
+    dec_bytes = [float(statistics.mean(decode_bytes(w, w.steps[k % nsteps]) for k in range(dec_steps)))]
     my_time = torch.tensor([total_ms], dtype=torch.float64)
     my_bytes = torch.tensor([float(sum(bytes_steps))], dtype=torch.float64)
     if world > 1:
@@ -558,7 +596,7 @@ def run_gpu(args, world, rank, local):
         i = k % nsteps
         for f in fields:
             getattr(dev_in[i], f).copy_(getattr(host_steps[i], f), non_blocking=True)
-        run_decode_step(w, dw.key_cache, dw.value_cache, dev_in[i], dw.out, None, True, dw.k_head_scales,
+        run_decode_step(w, dw.key_cache, dw.value_cache, dev_in[i], dw.out, None, joint, dw.k_head_scales,
                         dw.v_head_scales)
         out_host.copy_(dw.out, non_blocking=True)
     torch.cuda.synchronize(dev)
@@ -570,7 +608,7 @@ def run_gpu(args, world, rank, local):
         a.record(stream)
         for f in fields:
             getattr(dev_in[i], f).copy_(getattr(host_steps[i], f), non_blocking=True)
-        run_decode_step(w, dw.key_cache, dw.value_cache, dev_in[i], dw.out, None, True, dw.k_head_scales,
+        run_decode_step(w, dw.key_cache, dw.value_cache, dev_in[i], dw.out, None, joint, dw.k_head_scales,
                         dw.v_head_scales)
         out_host.copy_(dw.out, non_blocking=True)
         c.record(stream)
@@ -596,9 +634,17 @@ def run_gpu(args, world, rank, local):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.DTYPE_NAMES[w.kv_dtype], "data": "synthetic",
-        "config": {"workload": describe_workload(w, args.workload), "l2": "flushed between steps (256 MiB write + 256 MiB read, untimed)",
-                   "accumulate": "f32", "us_per_step": round(max_ms / args.steps * 1e3, 2),
+        "config": {"workload": describe_workload(w, args.workload),
+                   "l2": (f"not flushed: steps back to back, each reading {step0_bytes / 1e6:.0f} MB, over twice the "
+                          f"{l2_bytes / 2**20:.0f} MiB L2 (K/V streamed evict-first)" if back_to_back else
+                          "flushed between steps (256 MiB write + 256 MiB read, untimed)"),
+                   "accumulate": "f32", "step_mode": args.step_mode,
+                   "us_per_step": round(max_ms / args.steps * 1e3, 2),
                    "decode_us": round(dec_avg_s * 1e6, 2),
+                   **({"flushed_step_us": round(flushed_step_ms * 1e3, 2),
+                       "flushed_decode_us": round(flushed_dec_ms * 1e3, 2),
+                       "flushed_step_gbs": round(step_bytes(w, w.steps[0]) / (flushed_step_ms * 1e-3) / 1e9, 1)}
+                      if back_to_back else {}),
                    "tokens_per_s": round(w.num_seqs * world / (max_ms / args.steps * 1e-3), 1),
                    "pct_of_8TBps": round(value / 8000 * 100, 2), "parallelism": f"replicas x{world}"},
         "roofline": roofline,
@@ -612,6 +658,9 @@ def run_gpu(args, world, rank, local):
     return 0
 
 
+STEP_MODES = {"fused": "fused", "joint": True, "split": False}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -623,6 +672,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle CPU time")
     ap.add_argument("--decode-kernel", choices=["auto", "tensor", "core"], default="auto",
                     help="decode kernel: chosen by the library, tensor-core, or CUDA-core")
+    ap.add_argument("--step-mode", choices=sorted(STEP_MODES), default="fused",
+                    help="how a decode step's cache write is issued: fused into the decode kernel, "
+                         "joint (write + dependent decode launch in one call), or split (two calls)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("at least 3 warm-up steps")

@@ -14,7 +14,9 @@
  *   pkv_paged_attention_decode_window  decode of a sliding-window layer (only the
  *                                last W positions; blocks before them never read);
  *   pkv_paged_attention_prefill  causal attention of a prompt's (or a prompt chunk's)
- *                                new tokens over the cache.
+ *                                new tokens over the cache;
+ *   pkv_decode_append            a decode step whose cache write happens inside the
+ *                                decode kernel (one new token per sequence).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -140,6 +142,32 @@ pkv_status pkv_paged_attention_decode(const pkv_tensor* out, const pkv_tensor* q
                                       const pkv_tensor* context_lens, int32_t num_kv_heads,
                                       float scale, int32_t block_size,
                                       int32_t max_blocks_per_seq, pkv_stream stream);
+
+/*
+ * pkv_decode_append — one decode step with the cache write fused into the decode
+ * kernel: the same results as pkv_decode_step when token s of key / value is sequence
+ * s's newest token (num_tokens == num_seqs, slot_mapping[s] the slot of position
+ * context_lens[s] - 1 of sequence s, or < 0 for none), the usual layout of a decode step.
+ *
+ * Defined by: the write and decode definitions above (vasteelab.pages.dev
+ * "PagedAttentionとは？", section "PagedAttentionはAttention kernelとmemory managerの
+ * 組み合わせである").
+ *
+ * The warp of the decode kernel that reads a sequence's last positions encodes its new
+ * token as pkv_reshape_and_cache would, stores it to its slot and uses it directly, so
+ * no separate write kernel runs and the decode waits for none.  A token whose slot is
+ * not its sequence's position L - 1 is stored only (as the two-call form would, provided
+ * no sequence reads another sequence's new slot in the same step — which a correct block
+ * manager never lets happen).  Where the library would run the CUDA-core decode kernel,
+ * the call runs the write and the decode as two kernels instead.  Arguments and errors as
+ * for pkv_decode_step; num_tokens != num_seqs is PKV_ERR_INVALID_ARG.
+ */
+pkv_status pkv_decode_append(const pkv_tensor* out, const pkv_tensor* query, const pkv_tensor* key,
+                             const pkv_tensor* value, const pkv_tensor* slot_mapping,
+                             const pkv_tensor* key_cache, const pkv_tensor* value_cache,
+                             const pkv_tensor* block_tables, const pkv_tensor* context_lens,
+                             int32_t num_kv_heads, float scale, int32_t block_size,
+                             int32_t max_blocks_per_seq, int32_t sliding_window, pkv_stream stream);
 
 /*
  * pkv_paged_attention_decode_window — decode attention of a sliding-window layer:
@@ -352,6 +380,11 @@ int32_t pkv_abi_version(void);
  * PKV_OPT_DYNAMIC_CHUNK (tensor-core kernel): fewest 16-token stages per run-time unit
  * (1 to 64, default 4).  Neither option changes which values are computed, only which
  * warp computes them (and so the rounding order of split rows).
+ * PKV_OPT_FUSED_APPEND (pkv_decode_append): 0 = automatic (the write inside the decode
+ * kernel for a 16-bit cache; for an 8-bit cache, whose kernel is bound by instruction
+ * issue, the write as its own launch with the decode depending on it), 1 = always the
+ * separate write, 2 = always inside the decode kernel (when the tensor-core kernel
+ * runs).  The cache bytes and outputs are the same either way.
  * pkv_set_option returns PKV_ERR_INVALID_ARG for an unknown option or a bad value.
  */
 typedef enum pkv_option {
@@ -360,7 +393,8 @@ typedef enum pkv_option {
   PKV_OPT_DRY_RUN = 2,
   PKV_OPT_DECODE_KERNEL = 3,
   PKV_OPT_DYNAMIC_SHARE = 4,
-  PKV_OPT_DYNAMIC_CHUNK = 5
+  PKV_OPT_DYNAMIC_CHUNK = 5,
+  PKV_OPT_FUSED_APPEND = 6
 } pkv_option;
 
 pkv_status pkv_set_option(int32_t option, int64_t value);

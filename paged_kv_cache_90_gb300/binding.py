@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
                 4: "PKV_ERR_DEVICE_CHECK"}
 DEVERR = {"table_entry": 0x1, "slot": 0x2, "copy_pair": 0x4, "context_len": 0x8, "timeout": 0x10}
 OPTIONS = {"partition_tokens": 0, "debug_sync": 1, "dry_run": 2, "decode_kernel": 3,
-           "dynamic_share": 4, "dynamic_chunk": 5}
+           "dynamic_share": 4, "dynamic_chunk": 5, "fused_append": 6}
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float8_e4m3fn: 2, torch.int32: 3, torch.int64: 4}
 
 
@@ -64,13 +64,14 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
         lib.pkv_decode_step.argtypes = [d, d, d, d, d, d, d, d, d, i32, f32, i32, i32, i32, vp]
         lib.pkv_reshape_and_cache_amax.argtypes = [d, d, d, d, d, vp, vp, vp]
         lib.pkv_paged_attention_prefill.argtypes = [d, d, d, d, d, d, d, i32, f32, i32, i32, vp]
+        lib.pkv_decode_append.argtypes = [d, d, d, d, d, d, d, d, d, i32, f32, i32, i32, i32, vp]
         lib.pkv_paged_attention_decode_window.argtypes = [d, d, d, d, d, d, i32, f32, i32, i32, i32, vp]
         lib.pkv_noalloc_scratch_bytes.restype = i64
         lib.pkv_noalloc_scratch_bytes.argtypes = []
         for fn in ("pkv_paged_attention_decode", "pkv_paged_attention_decode_noalloc",
                    "pkv_reshape_and_cache", "pkv_decode_step", "pkv_copy_blocks",
                    "pkv_paged_attention_decode_window", "pkv_reshape_and_cache_amax",
-                   "pkv_paged_attention_prefill",
+                   "pkv_paged_attention_prefill", "pkv_decode_append",
                    "pkv_set_option", "pkv_reserve_workspace", "pkv_read_device_errors"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.pkv_last_error.restype = ctypes.c_char_p
@@ -163,6 +164,22 @@ def decode_step(out, query, key, value, slot_mapping, key_cache, value_cache, bl
              describe(block_tables), describe(context_lens)]
     _check(lib.pkv_decode_step(*[ctypes.byref(x) for x in descs], int(num_kv_heads), float(scale),
                                int(block_size), int(max_blocks_per_seq), int(sliding_window), _stream(stream)))
+    return out
+
+
+def decode_append(out, query, key, value, slot_mapping, key_cache, value_cache, block_tables, context_lens,
+                  num_kv_heads: int, scale: float, block_size: int, max_blocks_per_seq: int,
+                  k_scale: float = 1.0, v_scale: float = 1.0, stream=None, sliding_window: int = 0,
+                  k_head_scales=None, v_head_scales=None) -> torch.Tensor:
+    """decode_step with the cache write inside the decode kernel: token s of ``key`` /
+    ``value`` must be sequence s's newest token (its slot the position
+    context_lens[s] - 1).  Returns ``out``."""
+    lib = load_library()
+    descs = [describe(out), describe(query), describe(key), describe(value), describe(slot_mapping),
+             describe(key_cache, k_scale, k_head_scales), describe(value_cache, v_scale, v_head_scales),
+             describe(block_tables), describe(context_lens)]
+    _check(lib.pkv_decode_append(*[ctypes.byref(x) for x in descs], int(num_kv_heads), float(scale),
+                                 int(block_size), int(max_blocks_per_seq), int(sliding_window), _stream(stream)))
     return out
 
 

@@ -93,21 +93,6 @@ __global__ void __launch_bounds__(kWriteThreads) cache_write_copy_kernel(const C
   }
 }
 
-// Eight source values -> eight e4m3 codes: x / scale in IEEE binary32 (correctly
-// rounded division), then round-to-nearest-even with saturation to +-448.
-__device__ __forceinline__ uint2 quantize8(const float* x, float scale) {
-  uint32_t w[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float2 a = make_float2(__fdiv_rn(x[4 * i + 0], scale), __fdiv_rn(x[4 * i + 1], scale));
-    const float2 b = make_float2(__fdiv_rn(x[4 * i + 2], scale), __fdiv_rn(x[4 * i + 3], scale));
-    const uint32_t lo = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
-    const uint32_t hi = __nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E4M3);
-    w[i] = (lo & 0xffffu) | (hi << 16);
-  }
-  return make_uint2(w[0], w[1]);
-}
-
 template <typename Src>
 __device__ __forceinline__ void load8(const unsigned char* p, float* f);
 template <>
@@ -145,8 +130,8 @@ __global__ void __launch_bounds__(kWriteThreads) cache_write_e4m3_kernel(const C
     load8<Src>(static_cast<const unsigned char*>(p.value) + src, xv);
     const float ks = p.k_head_scales ? __ldg(p.k_head_scales + h) : p.k_scale;
     const float vs = p.v_head_scales ? __ldg(p.v_head_scales + h) : p.v_scale;
-    *reinterpret_cast<uint2*>(static_cast<unsigned char*>(p.key_cache) + dst) = quantize8(xk, ks);
-    *reinterpret_cast<uint2*>(static_cast<unsigned char*>(p.value_cache) + dst) = quantize8(xv, vs);
+    *reinterpret_cast<uint2*>(static_cast<unsigned char*>(p.key_cache) + dst) = e4m3_quantize8(xk, DivRn(ks));
+    *reinterpret_cast<uint2*>(static_cast<unsigned char*>(p.value_cache) + dst) = e4m3_quantize8(xv, DivRn(vs));
     if (p.k_amax || p.v_amax) {
       AmaxAcc ak, av;
 #pragma unroll

@@ -91,7 +91,7 @@ cudaError_t launch_tpl(const DecodeParams& p, cudaStream_t stream) {
   cudaError_t e = cached_cache_map(&mk, p.key_cache, p, box_rows);
   if (e != cudaSuccess) return e;
   if ((e = cached_cache_map(&mv, p.value_cache, p, box_rows)) != cudaSuccess) return e;
-  const size_t smem = C::smem_bytes(p.num_seqs);
+  const size_t smem = C::smem_bytes(p.num_seqs, p.fused_append);
   auto kern = mma::paged_decode_mma_kernel<KV, D, G>;
   // raise the kernel's shared-memory limit only when a launch needs more than before
   static size_t smem_set[kMapCacheDevices] = {};
@@ -312,11 +312,11 @@ __global__ void __launch_bounds__(kMergeThreads) merge_split_rows_kernel(const D
 }
 
 template <typename KV, int D>
-size_t smem_for(int G, int S) {
+size_t smem_for(int G, int S, bool fused_append) {
   switch (G) {
-    case 4: return mma::Cfg<KV, D, 4>::smem_bytes(S);
-    case 8: return mma::Cfg<KV, D, 8>::smem_bytes(S);
-    case 16: return mma::Cfg<KV, D, 16>::smem_bytes(S);
+    case 4: return mma::Cfg<KV, D, 4>::smem_bytes(S, fused_append);
+    case 8: return mma::Cfg<KV, D, 8>::smem_bytes(S, fused_append);
+    case 16: return mma::Cfg<KV, D, 16>::smem_bytes(S, fused_append);
     default: return 0;
   }
 }
@@ -384,6 +384,18 @@ int mma_heads_per_item(int group) {
   return 0;
 }
 
+static size_t mma_smem_bytes(const DecodeParams& p, int G, bool fused_append) {
+  if (p.kv_dtype == kBF16 && p.head_dim == 128) return smem_for<BF16, 128>(G, p.num_seqs, fused_append);
+  if (p.kv_dtype == kBF16 && p.head_dim == 64) return smem_for<BF16, 64>(G, p.num_seqs, fused_append);
+  if (p.kv_dtype == kE4M3 && p.head_dim == 128) return smem_for<E4M3, 128>(G, p.num_seqs, fused_append);
+  return 0;
+}
+
+bool mma_fused_append_fits(const DecodeParams& p) {
+  const size_t smem = mma_smem_bytes(p, mma_heads_per_item(p.group), true);
+  return smem > 0 && smem <= 227 * 1024;
+}
+
 bool mma_decode_supported(const DecodeParams& p) {
   const int G = mma_heads_per_item(p.group);
   if (G == 0 || p.q_dtype != kBF16 || p.out_dtype != kBF16) return false;
@@ -396,11 +408,8 @@ bool mma_decode_supported(const DecodeParams& p) {
   // the flattened (sequence, head group, token) space must fit in 31 bits
   const int64_t max_ctx = int64_t(p.max_blocks_per_seq) * p.block_size;
   if (int64_t(p.num_seqs) * (max_ctx + 16) * (p.num_heads / G) >= (int64_t(1) << 31)) return false;
-  size_t smem = 0;
-  if (p.kv_dtype == kBF16 && p.head_dim == 128) smem = smem_for<BF16, 128>(G, p.num_seqs);
-  else if (p.kv_dtype == kBF16 && p.head_dim == 64) smem = smem_for<BF16, 64>(G, p.num_seqs);
-  else if (p.kv_dtype == kE4M3 && p.head_dim == 128) smem = smem_for<E4M3, 128>(G, p.num_seqs);
-  else return false;
+  const size_t smem = mma_smem_bytes(p, G, false);
+  if (smem == 0) return false;
   // the merge kernel's offsets and per-row lists fit the default 48 KB with its 20 KB
   // of static shared memory
   if (p.grid < 1 || merge_smem_bytes(p.num_seqs, G, p.num_heads, p.grid) > 26 * 1024) return false;

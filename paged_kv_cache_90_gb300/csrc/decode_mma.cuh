@@ -131,16 +131,25 @@ struct Cfg {
   static_assert(G == 4 || G == 8 || G == 16, "heads per item");
   static_assert(kRawTile % 1024 == 0 || kRawRowBytes == 64, "tiles are whole swizzle atoms");
   static constexpr size_t kWarpBytes = size_t(kStages) * kStageBytes + kVConv;
-  // from the 1024-aligned base: cum[S+1] ints | lens[S] ints | mbarriers | unit tags of
-  // the ring slots | per-warp rings
+  // fused append: a ring slot's copy of the appended token's K and V rows (as given:
+  // f32 or bf16 for an 8-bit cache, the cache's type otherwise), V at the half
+  static constexpr int kAppendBytes = 2 * D * (kFp8 ? 4 : KV::bytes);
+  // from the 1024-aligned base: cum[S+1] ints | lens[S] ints | mbarriers | per ring
+  // slot its unit and the table entry of its row's newest position | per-warp rings |
+  // (fused append) per-warp staged tokens
   __host__ __device__ static size_t bar_offset(int num_seqs) { return ((2 * size_t(num_seqs) + 1) * 4 + 7) / 8 * 8; }
   __host__ __device__ static size_t tag_offset(int num_seqs) {
     return bar_offset(num_seqs) + size_t(kWarps) * kStages * 8;
   }
   __host__ __device__ static size_t ring_offset(int num_seqs) {
-    return (tag_offset(num_seqs) + size_t(kWarps) * kStages * 4 + 1023) / 1024 * 1024;
+    return (tag_offset(num_seqs) + size_t(kWarps) * kStages * 8 + 1023) / 1024 * 1024;
   }
-  static size_t smem_bytes(int num_seqs) { return ring_offset(num_seqs) + kWarps * kWarpBytes + 1024; }
+  __host__ __device__ static size_t append_offset(int num_seqs) {
+    return ring_offset(num_seqs) + kWarps * kWarpBytes;
+  }
+  static size_t smem_bytes(int num_seqs, bool fused_append) {
+    return append_offset(num_seqs) + (fused_append ? size_t(kWarps) * kStages * kAppendBytes : 0) + 1024;
+  }
 };
 
 // Position in the flattened (sequence, head tile, stage) order.  cum[s] is the first
@@ -175,6 +184,8 @@ __device__ __forceinline__ int row_base(int L, int window, int block_size) {
 // be shorter).  `share` / 1024 of the stages go to the run-time units; CH grows beyond
 // `chunk` when that would make more than `nd_max` of them.  Unit indices grow with
 // position, so (unit + row) names a distinct partial slot for every (unit, row) pair.
+// (Run-time units have a fixed cost, a block-table load and a copy latency before their
+// first stage streams, so runs shrinking towards the end lengthen the step.)
 struct WorkSplit {
   int GW, NS, NSs, q, rmd, CH, ND;
   __device__ WorkSplit(int ns, int gw, int share, int chunk, int nd_max) : GW(gw), NS(ns) {
@@ -292,7 +303,10 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
   const int GW = gridDim.x * kWarps;
   const int gw = blockIdx.x * kWarps + warp;
   const WorkSplit split(T / kST, GW, p.dyn_share, p.dyn_chunk, p.dyn_units_max);
-  int* tags = reinterpret_cast<int*>(smem + C::tag_offset(S)) + warp * C::kStages;
+  int* tags = reinterpret_cast<int*>(smem + C::tag_offset(S)) + warp * 2 * C::kStages;
+  int* tail_blk = tags + C::kStages;   // per slot: table entry holding the row's position L - 1
+  unsigned char* abase = smem + C::append_offset(S) + size_t(warp) * C::kStages * C::kAppendBytes;
+  const int aeb = p.new_dtype == kF32 ? 4 : 2;  // bytes of an appended element as given
 
   // cursor at the first stage of unit u
   auto unit_cursor = [&](int u) {
@@ -346,6 +360,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
     }
   };
   int wcur0 = 0, wcur1 = 0, wnext0 = 0, wnext1 = 0;
+  int64_t pend_slot = -1;     // lane j: slot of the token appended in ring slot j
 
   // ---- producer ------------------------------------------------------------------
   // Units are issued in the order static unit, then claimed ones.  A claim is sent
@@ -401,7 +416,13 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
     unsigned char* sb = wbase + size_t(islot) * C::kStageBytes;
     const int tok = icur.base + icur.t0;  // the stage's first token in the context
     const int nbox = (two_boxes && tok + 8 < icur.L) ? 2 : 1;
-    if (lane == 0) mbar_arrive_expect_tx(&bars[islot], uint32_t(kOpsPerBox * nbox) * box_bytes);
+    // fused append: the row's last stage also brings the sequence's new K and V rows
+    // (two bulk copies on the same barrier); its slot is loaded into a register of
+    // lane `islot`, read when the stage is consumed
+    const bool app = p.fused_append && icur.t0 + kST >= icur.rl;
+    const uint32_t arow = uint32_t(D * aeb);
+    if (lane == 0)
+      mbar_arrive_expect_tx(&bars[islot], uint32_t(kOpsPerBox * nbox) * box_bytes + (app ? 2u * arow : 0u));
     if (lane < kOpsPerBox * nbox) {  // one copy per lane
       int blk = op_b == 0 ? e0 : e1;
       if (blk < 0 || int64_t(blk) >= p.num_blocks) {
@@ -409,6 +430,15 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
         blk = 0;
       }
       tma_load_4d(sb + op_off, op_map, 64 * op_h, tok & (bs - 1), icur.kvh, blk, &bars[islot], stream_policy);
+    } else if (app && lane >= 30) {
+      const bool isv = lane == 31;
+      const unsigned char* src = static_cast<const unsigned char*>(isv ? p.new_value : p.new_key) +
+                                 (int64_t(icur.s) * p.nk_stride_t + int64_t(icur.kvh) * p.nk_stride_h) * aeb;
+      bulk_copy_g2s(abase + islot * C::kAppendBytes + (isv ? C::kAppendBytes / 2 : 0), src, arow, &bars[islot]);
+    }
+    if (app) {
+      if (lane == islot) pend_slot = p.slot_mapping[icur.s];
+      tail_blk[islot] = ((icur.L - 1) >> bs_shift) == (tok >> bs_shift) ? e0 : e1;
     }
     cursor_next(icur, geo);
     ++issued;
@@ -540,6 +570,68 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
     const int ctok = cc.base + cc.t0;                     // the stage's first token in the context
     const int nvalid = cc.L - ctok < kST ? cc.L - ctok : kST;
     const int lo_valid = window_start(cc.L, p.sliding_window) - ctok;  // > 0: window starts inside
+
+    // fused append: the row's last stage holds the sequence's newest position L - 1,
+    // where this call's new token goes.  Encode it as the cache write would, store it
+    // to its slot and put it into the tile just copied (which holds the slot's old
+    // bytes).  A token whose slot is not that position is only stored.
+    if (p.fused_append && cc.t0 + kST >= cc.rl) {
+      const int64_t slot_w = __shfl_sync(0xffffffffu, pend_slot, slot);
+      if (slot_w >= 0) {
+        if (slot_w >= p.num_blocks * int64_t(bs)) {
+          if (lane == 0) raise_device_error(p.err, kErrSlot);
+        } else {
+          const int r = nvalid - 1;                        // row of position L - 1 in the stage
+          const int64_t here = int64_t(tail_blk[slot]) * bs + ((cc.L - 1) & (bs - 1));
+          const bool patch = slot_w == here;
+          const int64_t crow = (slot_w >> bs_shift) * p.cs_block + int64_t(cc.kvh) * p.cs_head +
+                               (slot_w & (bs - 1)) * D;   // cache element of the slot's row
+          const unsigned char* stg = abase + slot * C::kAppendBytes;
+          if constexpr (C::kFp8) {
+            // lanes 0-15: K, 16-31: V; 8 codes (d = 8c .. 8c + 7) each
+            const bool isv = lane >= 16;
+            const int c = lane & 15;
+            const unsigned char* src = stg + (isv ? C::kAppendBytes / 2 : 0) + 8 * c * aeb;
+            float x[8];
+            if (aeb == 4) {
+              const float4 f0 = *reinterpret_cast<const float4*>(src);
+              const float4 f1 = *reinterpret_cast<const float4*>(src + 16);
+              x[0] = f0.x; x[1] = f0.y; x[2] = f0.z; x[3] = f0.w;
+              x[4] = f1.x; x[5] = f1.y; x[6] = f1.z; x[7] = f1.w;
+            } else {
+              const uint4 w = *reinterpret_cast<const uint4*>(src);
+              const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                x[2 * k] = bf16_lo_to_f32(ww[k]);
+                x[2 * k + 1] = bf16_hi_to_f32(ww[k]);
+              }
+            }
+            const float* hs = isv ? p.v_head_scales : p.k_head_scales;
+            const float sc = hs ? __ldg(hs + cc.kvh) : (isv ? p.append_v_scale : p.append_k_scale);
+            const uint2 codes = e4m3_quantize8(x, DivRn(sc));
+            unsigned char* cache = static_cast<unsigned char*>(const_cast<void*>(isv ? p.value_cache : p.key_cache));
+            *reinterpret_cast<uint2*>(cache + crow + 8 * c) = codes;
+            if (patch)
+              *reinterpret_cast<uint2*>((isv ? vt : sb) + r * 128 + (((c >> 1) ^ (r & 7)) << 4) + 8 * (c & 1)) = codes;
+          } else {
+            // lanes 0-15: K, 16-31: V; 8 values (16 bytes) each, D / 8 chunks per tensor
+            const int c = lane & 15;
+            if (c < D / 8) {
+              const uint4 v = *reinterpret_cast<const uint4*>(stg + (lane & 16 ? C::kAppendBytes / 2 : 0) + 16 * c);
+              unsigned char* cache =
+                  static_cast<unsigned char*>(const_cast<void*>(lane & 16 ? p.value_cache : p.key_cache));
+              *reinterpret_cast<uint4*>(cache + crow * 2 + 16 * c) = v;
+              const int h = c >> 3, cj = c & 7;
+              if (patch)
+                *reinterpret_cast<uint4*>((lane & 16 ? vt : sb) + size_t(h) * kST * 128 + r * 128 + ((cj ^ (r & 7)) << 4)) = v;
+            }
+          }
+          fence_proxy_async_smem();  // the slot is refilled by a later copy
+          __syncwarp();
+        }
+      }
+    }
 
     // values as 16-bit operand rows (8-bit cache: convert; rows past the context: zero)
     const unsigned char* vop = vt;

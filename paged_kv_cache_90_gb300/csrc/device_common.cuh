@@ -115,6 +115,53 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// x / s in IEEE binary32, correctly rounded to nearest even, without a division per
+// value.  y = RN(1/s) comes from the correctly rounded reciprocal; q0 = RN(x * y) is
+// within a few ulps of x / s.  Markstein's correction (P. Markstein, "IA-64 and
+// Elementary Functions", 2000; Muller et al., "Handbook of Floating-Point Arithmetic",
+// division by Newton-Raphson iteration) forms the remainder r = x - s * q exactly with
+// one FMA and returns RN(q + r * y): the first step brings q within half an ulp plus a
+// hair, the second is correctly rounded by Markstein's theorem (y within half an ulp
+// of 1/s, q within one ulp of x / s).  The theorem needs exact remainders and no
+// underflow: |x| in [2^-100, 2^100] and |s| in [2^-20, 2^20] keep every quantity
+// normal; other operands (zeros, infinities, NaN, extreme values) take the division.
+struct DivRn {
+  float s, y;
+  bool fast;
+  __device__ __forceinline__ explicit DivRn(float scale) : s(scale) {
+    const float as = fabsf(scale);
+    fast = as >= 0x1p-20f && as <= 0x1p20f;
+    y = fast ? __frcp_rn(scale) : 0.f;
+  }
+  __device__ __forceinline__ float operator()(float x) const {
+    const float ax = fabsf(x);
+    if (fast && ax >= 0x1p-100f && ax <= 0x1p100f) {
+      float q = __fmul_rn(x, y);
+      float r = __fmaf_rn(-s, q, x);
+      q = __fmaf_rn(r, y, q);
+      r = __fmaf_rn(-s, q, x);
+      return __fmaf_rn(r, y, q);
+    }
+    return __fdiv_rn(x, s);
+  }
+};
+
+// Eight source values -> eight e4m3 codes: x / scale in IEEE binary32 (correctly
+// rounded), then round-to-nearest-even with saturation to +-448.  The cache write and
+// the decode kernel's fused append both encode with this.
+__device__ __forceinline__ uint2 e4m3_quantize8(const float* x, const DivRn& div) {
+  uint32_t w[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float2 a = make_float2(div(x[4 * i + 0]), div(x[4 * i + 1]));
+    const float2 b = make_float2(div(x[4 * i + 2]), div(x[4 * i + 3]));
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(a, __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(b, __NV_SATFINITE, __NV_E4M3);
+    w[i] = (lo & 0xffffu) | (hi << 16);
+  }
+  return make_uint2(w[0], w[1]);
+}
+
 // ---- mbarrier + bulk async copy (inline PTX) -------------------------------------
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

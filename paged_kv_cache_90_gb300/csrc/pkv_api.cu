@@ -26,6 +26,7 @@ std::atomic<int64_t> g_opt_dry_run{0};
 std::atomic<int64_t> g_opt_decode_kernel{0};
 std::atomic<int64_t> g_opt_dynamic_share{-1};
 std::atomic<int64_t> g_opt_dynamic_chunk{4};
+std::atomic<int64_t> g_opt_fused_append{0};
 
 thread_local std::string t_last_error;
 
@@ -472,6 +473,10 @@ pkv_status pkv_set_option(int32_t option, int64_t value) {
       if (value < 1 || value > 64) return fail(PKV_ERR_INVALID_ARG, "dynamic chunk is 1 to 64 stages");
       g_opt_dynamic_chunk = value;
       return PKV_OK;
+    case PKV_OPT_FUSED_APPEND:
+      if (value < 0 || value > 2) return fail(PKV_ERR_INVALID_ARG, "fused append is 0, 1 or 2");
+      g_opt_fused_append = value;
+      return PKV_OK;
     default:
       return fail(PKV_ERR_INVALID_ARG, "unknown option %d", option);
   }
@@ -485,6 +490,7 @@ int64_t pkv_get_option(int32_t option) {
     case PKV_OPT_DECODE_KERNEL: return g_opt_decode_kernel.load();
     case PKV_OPT_DYNAMIC_SHARE: return g_opt_dynamic_share.load();
     case PKV_OPT_DYNAMIC_CHUNK: return g_opt_dynamic_chunk.load();
+    case PKV_OPT_FUSED_APPEND: return g_opt_fused_append.load();
     default: return -1;
   }
 }
@@ -716,6 +722,56 @@ pkv_status pkv_decode_step(const pkv_tensor* out, const pkv_tensor* query, const
   }
   if (no_decode) return PKV_OK;
   return finish_call(s, launch_decode(p, cs), cs, "decode_step");
+}
+
+pkv_status pkv_decode_append(const pkv_tensor* out, const pkv_tensor* query, const pkv_tensor* key,
+                             const pkv_tensor* value, const pkv_tensor* slot_mapping, const pkv_tensor* key_cache,
+                             const pkv_tensor* value_cache, const pkv_tensor* block_tables,
+                             const pkv_tensor* context_lens, int32_t num_kv_heads, float scale, int32_t block_size,
+                             int32_t max_blocks_per_seq, int32_t sliding_window, pkv_stream stream) {
+  CacheWriteParams wp;
+  bool no_write = false, no_decode = false;
+  pkv_status st = reshape_prepare(key, value, key_cache, value_cache, slot_mapping, &wp, &no_write);
+  if (st) return st;
+  DecodeParams p;
+  size_t ws_bytes = 0;
+  st = decode_prepare(out, query, key_cache, value_cache, block_tables, context_lens, num_kv_heads, scale,
+                      block_size, max_blocks_per_seq, sliding_window, &p, &ws_bytes, &no_decode);
+  if (st) return st;
+  if (key->shape[0] != query->shape[0])
+    return fail(PKV_ERR_INVALID_ARG, "decode_append takes one new token per sequence (key.shape[0] == num_seqs)");
+  if (g_opt_dry_run.load()) return PKV_OK;
+  DeviceState* s;
+  if ((st = device_state(&s))) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (!no_decode && ws_bytes) {
+    if ((st = ensure_workspace(s, ws_bytes, cs))) return st;
+    decode_set_workspace(&p, s->ws);
+  }
+  const int64_t mode = g_opt_fused_append.load();
+  const bool fused = mode == 2 || (mode == 0 && p.kv_dtype != kE4M3);
+  if (no_decode || p.kernel != 1 || !fused || !mma_fused_append_fits(p)) {
+    // the CUDA-core kernel has no fused write (and very many sequences leave no room
+    // for the staged tokens); an 8-bit cache's kernel is bound by instruction issue and
+    // the warps holding many sequence ends would fall behind: the write, then the
+    // decode as in decode_step
+    if (!no_write) {
+      cudaError_t e = launch_reshape_and_cache(wp, cs);
+      if (e != cudaSuccess || no_decode) return finish_call(s, e, cs, "decode_append (cache write)");
+      p.overlap_prologue = p.kernel == 1;
+    }
+    return no_decode ? PKV_OK : finish_call(s, launch_decode(p, cs), cs, "decode_append");
+  }
+  p.fused_append = !no_write;
+  p.new_key = wp.key;
+  p.new_value = wp.value;
+  p.new_dtype = wp.src_dtype;
+  p.nk_stride_t = wp.src_stride_t;
+  p.nk_stride_h = wp.src_stride_h;
+  p.slot_mapping = wp.slot_mapping;
+  p.append_k_scale = wp.k_scale;
+  p.append_v_scale = wp.v_scale;
+  return finish_call(s, launch_decode(p, cs), cs, "decode_append");
 }
 
 pkv_status pkv_copy_blocks(const pkv_tensor* cache, const pkv_tensor* src_dst_pairs, pkv_stream stream) {

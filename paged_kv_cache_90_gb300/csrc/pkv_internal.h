@@ -79,6 +79,15 @@ struct DecodeParams {
   const float* k_head_scales;  // e4m3 cache: [Hk] per-head scales (or null)
   const float* v_head_scales;
   int sliding_window;        // attend to the last W positions only (0: all)
+  // fused append (tensor-core kernel): token s of new_key / new_value is sequence s's
+  // newest token, written to slot_mapping[s] by the warp that reads that position
+  bool fused_append;
+  const void* new_key;
+  const void* new_value;
+  int new_dtype;             // kF32 / kBF16 (same as the cache, or any for an e4m3 cache)
+  int64_t nk_stride_t, nk_stride_h;
+  const int64_t* slot_mapping;
+  float append_k_scale, append_v_scale;  // e4m3 cache without per-head scales
   const int32_t* query_start_loc;  // prefill: [S + 1] packed query rows of each sequence
   int num_tokens;            // prefill: packed query rows
   int partition_tokens;      // multiple of 256
@@ -131,6 +140,8 @@ pkv_status set_error(pkv_status st, const char* msg);
 // group size (0 = unsupported), whether it handles a call, and its launch.
 int mma_heads_per_item(int group);
 bool mma_decode_supported(const DecodeParams& p);
+// whether the call's shared memory still fits with the fused append's staged tokens
+bool mma_fused_append_fits(const DecodeParams& p);
 constexpr int kMmaWarps = 8;  // warps per thread block of the tensor-core kernel
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream);
 // Prefill (prefill_mma.cuh, launched from decode_mma.cu): whether it handles a call,

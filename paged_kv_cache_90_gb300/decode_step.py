@@ -53,10 +53,11 @@ class DeviceWorkload:
         self.out = torch.empty(s, hq, d, dtype=w.q_dtype, device=self.device)
 
     def run_step(self, i: int, out: Optional[torch.Tensor] = None, stream=None,
-                 step: Optional[DeviceStep] = None, joint: bool = True) -> torch.Tensor:
+                 step: Optional[DeviceStep] = None, joint="fused") -> torch.Tensor:
         """Run step ``i`` (or the given device-resident inputs) on the current
-        stream; returns the decode output tensor.  ``joint`` issues the cache write and
-        the decode as one decode_step call, otherwise as two calls."""
+        stream; returns the decode output tensor.  ``joint``: "fused" issues the step as
+        one decode_append call (the write inside the decode kernel; one new token per
+        sequence), True as one decode_step call, False as a write and a decode call."""
         st = step if step is not None else self.steps[i]
         out = self.out if out is None else out
         run_decode_step(self.w, self.key_cache, self.value_cache, st, out, stream, joint,
@@ -65,7 +66,7 @@ class DeviceWorkload:
 
 
 def run_decode_step(w: Workload, key_cache, value_cache, st: DeviceStep, out, stream=None,
-                    joint: bool = True, k_head_scales=None, v_head_scales=None) -> None:
+                    joint="fused", k_head_scales=None, v_head_scales=None) -> None:
     if st.cow_pairs.numel():
         binding.copy_blocks(key_cache, st.cow_pairs, stream)
         binding.copy_blocks(value_cache, st.cow_pairs, stream)
@@ -76,6 +77,12 @@ def run_decode_step(w: Workload, key_cache, value_cache, st: DeviceStep, out, st
         binding.paged_attention_prefill(out, st.query, key_cache, value_cache, st.block_tables, st.context_lens,
                                         st.query_start_loc, w.num_kv_heads, w.scale, w.block_size,
                                         w.max_blocks_per_seq, stream)
+        return
+    if joint == "fused" and st.slot_mapping.numel() == st.query.shape[0]:
+        binding.decode_append(out, st.query, st.new_key, st.new_value, st.slot_mapping, key_cache, value_cache,
+                              st.block_tables, st.context_lens, w.num_kv_heads, w.scale, w.block_size,
+                              w.max_blocks_per_seq, w.k_scale, w.v_scale, stream, w.sliding_window,
+                              k_head_scales, v_head_scales)
         return
     if joint:
         binding.decode_step(out, st.query, st.new_key, st.new_value, st.slot_mapping, key_cache, value_cache,

@@ -77,6 +77,10 @@ def test_decode_step_validation(dry):
     empty = torch.zeros(0, 2, 128, dtype=torch.bfloat16)
     assert _status(binding.decode_step, **args(key=empty, value=empty,
                                                slot_mapping=torch.zeros(0, dtype=torch.int64))) == 0
+    assert _status(binding.decode_append, **args()) == 0                        # one token per sequence
+    two = torch.zeros(2, 2, 128, dtype=torch.bfloat16)
+    assert _status(binding.decode_append, **args(key=two, value=two,
+                                                 slot_mapping=torch.arange(2, dtype=torch.int64))) == 1
 
 
 def test_head_scales_and_amax_validation(dry):
@@ -195,7 +199,8 @@ def test_options_and_workspace_size(lib):
     assert binding.decode_workspace_bytes(0, 32, 8, 128, 16, 2048) == 0
     assert binding.decode_workspace_bytes(8, 32, 5, 128, 16, 2048) == 0
     assert binding.decode_workspace_bytes(8, 6, 2, 128, 16, 16) == 0     # 3 heads per KV head: no tensor path
-    for name, bad in (("dynamic_share", 1025), ("dynamic_share", -2), ("dynamic_chunk", 0), ("dynamic_chunk", 65)):
+    for name, bad in (("dynamic_share", 1025), ("dynamic_share", -2), ("dynamic_chunk", 0), ("dynamic_chunk", 65),
+                      ("fused_append", -1), ("fused_append", 3)):
         with pytest.raises(binding.PkvError):
             binding.set_option(name, bad)
     assert binding.get_option("dynamic_share") == -1     # automatic
@@ -203,6 +208,7 @@ def test_options_and_workspace_size(lib):
     assert binding.get_option("dynamic_share") == 512
     binding.set_option("dynamic_share", -1)
     assert binding.get_option("dynamic_chunk") == 4
+    assert binding.get_option("fused_append") == 0       # automatic
     with pytest.raises(KeyError):
         binding.set_option("nope", 1)
     assert lib.pkv_set_option(99, 0) == 1

@@ -5,6 +5,7 @@ tightly, within the final output rounding (2^-8 relative for a bf16 output)."""
 import os
 
 import pytest
+import numpy as np
 import torch
 
 import oracle
@@ -323,6 +324,37 @@ def test_sliding_window_full(kv, kernel):
     check_workload(wl.sliding_window_decode(kv_dtype=kv))
 
 
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_fused_append_writes_only_where_told(kv):
+    """A token with slot -1 writes nothing; a token whose slot is not its sequence's
+    newest position is stored there (the decode then reads the cache as it was), exactly
+    as the write-then-decode calls do."""
+    w = wl.llama3_8b_decode(seed=62, num_seqs=6, len_range=(20, 300), kv_dtype=kv)
+    st = w.steps[0]
+    st.slot_mapping = st.slot_mapping.clone()
+    st.slot_mapping[1] = -1
+    # sequence 3's token goes to an unused slot (never read in this step)
+    used = set()
+    for r, L in zip(st.block_tables.tolist(), st.context_lens.tolist()):
+        for p in range(L):
+            used.add(r[p // w.block_size] * w.block_size + p % w.block_size)
+    st.slot_mapping[3] = next(x for x in range(w.num_blocks * w.block_size) if x not in used)
+    runs = {}
+    for joint in ("fused", False):
+        dw = DeviceWorkload(w)
+        binding.set_option("fused_append", 2)   # the write inside the kernel for both cache types
+        try:
+            o = dw.run_step(0, out=torch.empty_like(dw.out), joint=joint).clone()
+        finally:
+            binding.set_option("fused_append", 0)
+        torch.cuda.synchronize()
+        runs[joint] = (o, dw.key_cache.clone(), dw.value_cache.clone())
+    assert binding.read_device_errors() == 0
+    assert torch.equal(runs["fused"][0], runs[False][0])
+    assert torch.equal(raw(runs["fused"][1]), raw(runs[False][1]))
+    assert torch.equal(raw(runs["fused"][2]), raw(runs[False][2]))
+
+
 def test_window_covering_every_context_is_the_plain_decode(kernel):
     """A window no shorter than any context gives the plain decode's bits."""
     w = wl.llama3_8b_decode(seed=61, num_seqs=8, len_range=(1, 900))
@@ -444,6 +476,64 @@ def test_cache_write_bit_exact(src, dst):
     assert binding.read_device_errors() == 0
 
 
+def _e4m3_boundary_values(scale: float, n: int, g) -> torch.Tensor:
+    """n binary32 values x whose quotients x / scale sit on, next to and between the
+    rounding midpoints of the e4m3 codes (both signs), plus zeros, infinities, values
+    past saturation, tiny and huge magnitudes, and random ones."""
+    mags = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8)).tolist()   # 0 .. 448
+    q = []
+    for a, b in zip(mags, mags[1:]):
+        mid = np.float32((a + b) / 2)
+        q += [mid, np.nextafter(mid, np.float32(np.inf)), np.nextafter(mid, np.float32(0))]
+    q = np.array(q, dtype=np.float64)
+    x = np.concatenate([q * scale, -q * scale]).astype(np.float32)   # quotient ~ midpoint after rounding x
+    special = np.array([0.0, -0.0, np.inf, -np.inf, 449.0 * scale, -1e4 * scale, 2.0 ** -110, -(2.0 ** 101),
+                        1e-30, 3e38], dtype=np.float32)
+    rnd = (torch.randn(n, generator=g, dtype=torch.float64) * 100 * scale).numpy().astype(np.float32)
+    return torch.from_numpy(np.concatenate([x, special, rnd])[:n].copy())
+
+
+@pytest.mark.parametrize("path", ["write", "fused"])
+def test_e4m3_encode_rounding_boundaries(path):
+    """The 8-bit encode (x / scale in binary32, then the nearest e4m3 code) is bit exact
+    where the quotient sits on or next to a rounding midpoint, for scales inside and
+    outside the reciprocal-based division's range, in the cache write and in the fused
+    append."""
+    g = torch.Generator().manual_seed(71)
+    scales = [0.02, 1 / 3, 0.0173, 1.0, 7.3, 1e-7, 3e6, 2.0 ** -20]
+    hk, d, S = len(scales), 128, 8
+    w = wl.variable_length_decode("rounding", 72, [33, 17, 64, 5, 48, 16, 90, 2], 4 * hk, hk, d, 16, "e4m3",
+                                  head_spread=1.0)
+    st = w.steps[0]
+    w.k_head_scales = torch.tensor(scales, dtype=torch.float32)
+    w.v_head_scales = torch.tensor(scales[::-1], dtype=torch.float32)
+    key = torch.stack([_e4m3_boundary_values(sc, S * d, g).view(S, d) for sc in scales], dim=1)
+    value = torch.stack([_e4m3_boundary_values(sc, S * d, g).view(S, d) for sc in scales[::-1]], dim=1)
+    perm = torch.randperm(S * d, generator=g)                        # mix the lanes that see each case
+    key = key.permute(0, 2, 1).reshape(S * d, hk)[perm].reshape(S, d, hk).permute(0, 2, 1).contiguous()
+    st.new_key, st.new_value = key, value.contiguous()
+    rk, rv = w.key_cache.clone(), w.value_cache.clone()
+    oracle.reshape_and_cache(key, st.new_value, rk, rv, st.slot_mapping, k_head_scales=w.k_head_scales,
+                             v_head_scales=w.v_head_scales)
+    dw = DeviceWorkload(w)
+    dst = dw.steps[0]
+    if path == "write":
+        binding.reshape_and_cache(dst.new_key, dst.new_value, dw.key_cache, dw.value_cache, dst.slot_mapping,
+                                  k_head_scales=dw.k_head_scales, v_head_scales=dw.v_head_scales)
+    else:
+        binding.set_option("decode_kernel", 2)
+        binding.set_option("fused_append", 2)
+        try:
+            dw.run_step(0, joint="fused")
+        finally:
+            binding.set_option("decode_kernel", 0)
+            binding.set_option("fused_append", 0)
+    torch.cuda.synchronize()
+    assert binding.read_device_errors() == 0
+    assert torch.equal(raw(dw.key_cache.cpu()), raw(rk))
+    assert torch.equal(raw(dw.value_cache.cpu()), raw(rv))
+
+
 def test_copy_blocks_bit_exact():
     g = torch.Generator().manual_seed(80)
     cache = torch.randn(40, 8, 16, 128, generator=g).to(torch.bfloat16)
@@ -496,34 +586,47 @@ def test_launch_count_and_determinism(kernel):
     w = wl.llama3_8b_decode(seed=99, num_seqs=4, len_range=(600, 1500))
     dw = DeviceWorkload(w)
     n0 = binding.launch_count()
-    a = dw.run_step(0, out=torch.empty_like(dw.out)).clone()
-    b = dw.run_step(0, out=torch.empty_like(dw.out)).clone()   # same slot rewritten with the same data
+    a = dw.run_step(0, out=torch.empty_like(dw.out), joint=False).clone()
+    b = dw.run_step(0, out=torch.empty_like(dw.out), joint=False).clone()   # same slot, same data
     torch.cuda.synchronize()
     # write + decode main kernel + merge of split contexts
     assert binding.launch_count() - n0 == 2 * 3
     assert torch.equal(a, b)
+    # the fused append folds the write into the tensor-core kernel; the CUDA-core
+    # kernel keeps the separate write
+    n0 = binding.launch_count()
+    c = dw.run_step(0, out=torch.empty_like(dw.out), joint="fused").clone()
+    torch.cuda.synchronize()
+    assert binding.launch_count() - n0 == (2 if kernel == "tensor" else 3)
+    assert torch.equal(a, c)
 
 
 @pytest.mark.parametrize("case", ["llama3", "cb_e4m3_bs8", "cow"])
 def test_decode_step_equals_write_then_decode(case, kernel):
-    """The joint call gives the same bytes as the write and the decode issued as two
-    calls: outputs and both caches, step after step."""
+    """The joint call and the fused append give the same bytes as the write and the
+    decode issued as two calls: outputs and both caches, step after step."""
     make = {"llama3": lambda: wl.llama3_8b_decode(seed=41, num_seqs=12, len_range=(1, 1500), poison=True),
             "cb_e4m3_bs8": lambda: wl.continuous_batching(seed=42, block_size=8, kv_dtype="e4m3", num_seqs=40,
                                                           num_steps=3, median=300, cap=3000, poison=True),
             "cow": lambda: wl.shared_prefix_cow(num_groups=4, prefix_blocks=8, suffix_range=(16, 120), poison=True)}
     w = make[case]()
     runs = {}
-    for joint in (True, False):
+    for joint in ("fused", "forced", True, False):
         dw = DeviceWorkload(w)
-        outs = [dw.run_step(i, out=torch.empty_like(dw.out), joint=joint).clone() for i in range(len(w.steps))]
+        binding.set_option("fused_append", 2 if joint == "forced" else 0)
+        try:
+            outs = [dw.run_step(i, out=torch.empty_like(dw.out), joint="fused" if joint == "forced" else joint).clone()
+                    for i in range(len(w.steps))]
+        finally:
+            binding.set_option("fused_append", 0)
         torch.cuda.synchronize()
         runs[joint] = (outs, dw.key_cache.clone(), dw.value_cache.clone())
     assert binding.read_device_errors() == 0
-    for a, b in zip(runs[True][0], runs[False][0]):
-        assert torch.equal(a, b)
-    assert torch.equal(raw(runs[True][1]), raw(runs[False][1]))
-    assert torch.equal(raw(runs[True][2]), raw(runs[False][2]))
+    for joint in ("fused", "forced", True):
+        for a, b in zip(runs[joint][0], runs[False][0]):
+            assert torch.equal(a, b), joint
+        assert torch.equal(raw(runs[joint][1]), raw(runs[False][1])), joint
+        assert torch.equal(raw(runs[joint][2]), raw(runs[False][2])), joint
 
 
 def test_workspace_reuse_across_shapes_and_kernels():
