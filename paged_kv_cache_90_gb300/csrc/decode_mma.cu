@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "decode_mma.cuh"
+#include "merge.cuh"
 #include "prefill_mma.cuh"
 
 namespace pkv {
@@ -119,65 +120,29 @@ cudaError_t launch_tpl(const DecodeParams& p, cudaStream_t stream) {
 }
 
 // Merge of rows split across units of work.  A persistent grid; block b owns rows b,
-// b + grid, ...  Before it waits for the main kernel's results (context_lens is an input
-// the main kernel does not write, so this overlaps the main kernel's last SMs), each
-// block rebuilds the flattened offsets of the sequences and, for each row it owns, the
-// first and last unit of work holding a part of it (the same split of stages the main
-// kernel used); rows inside one unit are skipped.  A thread covers one (head, 8 output
-// columns) of a row and folds parts online (running max; four parts' loads in flight
-// before their folds).  Rows of a few parts take one group of such threads each; a row
-// of many parts (a long context cut into run-time units) takes the whole block, its
-// groups folding every groups-th part and the first group folding their results from
-// shared memory.  A block packs its rows of many parts: `ways` groups per row, the
-// fewest that fold its largest such row in one round of loads, several rows at once.
+// b + grid, ...
+// Before it waits for the main kernel's results (context_lens is an input the main
+// kernel does not write, so this overlaps the main kernel's last SMs), each block
+// rebuilds the flattened offsets of the sequences and, for each row it owns, the first
+// and last unit of work holding a part of it (the same split of stages the main kernel
+// used); then it folds the parts (merge.cuh).
 constexpr int kMergeThreads = 512;
-constexpr int kMergeCols = 8;        // output columns per thread
-constexpr int kMergeLightParts = 8;  // rows of more parts take a whole block
-struct MergeAcc {
-  float M = -INFINITY, den = 0.f;
-  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = make_float4(0.f, 0.f, 0.f, 0.f);
-  // fold a part with max m, sum l and normalised output (va, vb) = o / l
-  __device__ void fold(float m, float l, const float4& va, const float4& vb) {
-    if (m == -INFINITY) return;
-    const float M2 = fmaxf(M, m);
-    const float x = fast_exp2(M - M2), y = l * fast_exp2(m - M2);
-    den = den * x + y;
-    a.x = a.x * x + y * va.x;
-    a.y = a.y * x + y * va.y;
-    a.z = a.z * x + y * va.z;
-    a.w = a.w * x + y * va.w;
-    b.x = b.x * x + y * vb.x;
-    b.y = b.y * x + y * vb.y;
-    b.z = b.z * x + y * vb.z;
-    b.w = b.w * x + y * vb.w;
-    M = M2;
-  }
-};
 
-// Rows a merge block owns, and its dynamic shared memory: offsets, then the first and
-// last unit of each owned row and the list of its rows of many parts.
-__host__ __device__ inline int merge_rows_per_block(int rows, int grid) { return (rows + grid - 1) / grid; }
+// Dynamic shared memory of the merge kernel: offsets, then its merge scratch.
+__host__ __device__ inline size_t merge_cum_bytes(int num_seqs) { return ((size_t(num_seqs) + 1) * sizeof(int) + 15) / 16 * 16; }
 inline size_t merge_smem_bytes(int num_seqs, int heads_per_item, int num_heads, int grid) {
   const int rows = num_seqs * (num_heads / heads_per_item);
-  return (size_t(num_seqs) + 1 + 3 * size_t(merge_rows_per_block(rows, grid))) * sizeof(int);
+  return merge_cum_bytes(num_seqs) + merge::Scratch<kMergeThreads>::bytes(merge::rows_per_block(rows, grid));
 }
 
 __global__ void __launch_bounds__(kMergeThreads) merge_split_rows_kernel(const DecodeParams p) {
-  extern __shared__ int cum[];  // [S + 1], then first[nk], last[nk], heavy[nk]
-  __shared__ float4 sh_a[kMergeThreads], sh_b[kMergeThreads];
-  __shared__ float2 sh_md[kMergeThreads];
+  extern __shared__ __align__(16) unsigned char merge_smem[];
+  int* cum = reinterpret_cast<int*>(merge_smem);  // [S + 1]
   __shared__ int warp_tot[kMergeThreads / 32];
-  __shared__ int n_heavy, max_parts;
-  const int S = p.num_seqs, G = p.heads_per_item, D = p.head_dim;
-  const int tiles = p.num_heads / G, tiles_per_kv = p.group / G;
+  const int S = p.num_seqs, G = p.heads_per_item;
+  const int tiles = p.num_heads / G;
   const int max_ctx = p.max_blocks_per_seq * p.block_size;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rows = S * tiles;
-  const int nk = (rows - int(blockIdx.x) + int(gridDim.x) - 1) / int(gridDim.x);  // rows of this block
-  int* first = cum + S + 1;
-  int* last = first + merge_rows_per_block(rows, gridDim.x);
-  int* heavy = last + merge_rows_per_block(rows, gridDim.x);
-  if (tid == 0) n_heavy = max_parts = 0;
   {  // cum[s] = sum over earlier sequences of (context padded to 16) x tiles
     const int per = (S + kMergeThreads - 1) / kMergeThreads;
     const int s0 = tid * per;
@@ -207,108 +172,12 @@ __global__ void __launch_bounds__(kMergeThreads) merge_split_rows_kernel(const D
   }
   const int T = cum[S];
   const mma::WorkSplit split(T / mma::kST, p.grid * kMmaWarps, p.dyn_share, p.dyn_chunk, p.dyn_units_max);
-  for (int k = tid; k < nk; k += kMergeThreads) {
-    const int row = blockIdx.x + k * gridDim.x;
-    const int s = row / tiles, tile = row - s * tiles;
-    const int rl = (cum[s + 1] - cum[s]) / tiles;
-    int wf = 0, wl = 0;
-    if (rl > 0) {
-      const int row_start = cum[s] + tile * rl;
-      wf = split.owner(row_start / mma::kST);
-      wl = split.owner((row_start + rl) / mma::kST - 1);
-    }
-    first[k] = wf;
-    last[k] = wl;
-    if (wl - wf >= kMergeLightParts) {
-      heavy[atomicAdd(&n_heavy, 1)] = k;
-      atomicMax(&max_parts, wl - wf + 1);
-    }
-  }
-  __syncthreads();
-  const int cols = G * D / kMergeCols;  // threads per group
-  const int groups = kMergeThreads / cols;
-  int ways = 1;
-  while (ways < groups && 4 * ways < max_parts) ways *= 2;
-  const int grp = tid / cols, i = tid % cols;
-  const int hr = i / (D / kMergeCols), d = (i % (D / kMergeCols)) * kMergeCols;
-
-  // fold parts wf + j, wf + j + ways, ... of a row
-  auto fold_parts = [&](MergeAcc& acc, int row, int wf, int wl, int j, int ways) {
-    for (int w0 = wf + j; w0 <= wl; w0 += 4 * ways) {
-      float pm[4], pl[4];
-      float4 pa[4], pb[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int w = w0 + k * ways;
-        pm[k] = -INFINITY;
-        if (w <= wl && split.len(w) > 0) {  // skip an empty static unit between two parts
-          const int64_t pr = int64_t(w + row) * G + hr;
-          const float4* po = reinterpret_cast<const float4*>(p.part_o + pr * D + d);
-          pm[k] = p.part_m[pr];
-          pl[k] = p.part_l[pr];
-          pa[k] = po[0];
-          pb[k] = po[1];
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc.fold(pm[k], pl[k], pa[k], pb[k]);
-    }
-  };
-  auto write_row = [&](const MergeAcc& acc, int row) {
-    const int s = row / tiles, tile = row - s * tiles;
-    const float inv = acc.den > 0.f ? 1.f / acc.den : 0.f;
-    const int h0 = (tile / tiles_per_kv) * p.group + (tile % tiles_per_kv) * G;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + int64_t(s) * p.out_stride_s +
-                         int64_t(h0 + hr) * p.out_stride_h + d;
-    __nv_bfloat162 r[4] = {__floats2bfloat162_rn(acc.a.x * inv, acc.a.y * inv),
-                           __floats2bfloat162_rn(acc.a.z * inv, acc.a.w * inv),
-                           __floats2bfloat162_rn(acc.b.x * inv, acc.b.y * inv),
-                           __floats2bfloat162_rn(acc.b.z * inv, acc.b.w * inv)};
-    *reinterpret_cast<uint4*>(out) = *reinterpret_cast<const uint4*>(r);
-  };
-
+  const merge::Scratch<kMergeThreads> sc = merge::Scratch<kMergeThreads>::carve(
+      merge_smem + merge_cum_bytes(S), merge::rows_per_block(S * tiles, gridDim.x));
+  merge::plan<kMergeThreads>(p, cum, split, sc, blockIdx.x, gridDim.x);
   asm volatile("griddepcontrol.wait;" ::: "memory");  // every partial of the main kernel is visible
   if (T == 0) return;
-  // rows of a few parts: one group each
-  for (int k = grp; k < nk; k += groups) {
-    const int wf = first[k], wl = last[k];
-    if (wf == wl || wl - wf >= kMergeLightParts) continue;
-    const int row = blockIdx.x + k * gridDim.x;
-    MergeAcc acc;
-    fold_parts(acc, row, wf, wl, 0, 1);
-    write_row(acc, row);
-  }
-  // rows of many parts: `ways` groups each, groups / ways rows at a time
-  const int per_pass = groups / ways, slot = grp / ways, j = grp % ways;
-  for (int base = 0; base < n_heavy; base += per_pass) {
-    const int h = base + slot;
-    int row = -1;
-    MergeAcc acc;
-    if (h < n_heavy) {
-      const int k = heavy[h];
-      row = blockIdx.x + k * gridDim.x;
-      fold_parts(acc, row, first[k], last[k], j, ways);
-    }
-    // a group's (M, den, a|b) is the fold of its parts: den = sum l 2^(m-M), a|b the
-    // same weights times o/l, so it folds like a part with m = M, l = den, o/l = a|b / den
-    sh_a[tid] = acc.a;
-    sh_b[tid] = acc.b;
-    sh_md[tid] = make_float2(acc.M, acc.den);
-    __syncthreads();
-    if (j == 0 && row >= 0) {
-      MergeAcc tot;
-      for (int q = 0; q < ways; ++q) {
-        const float2 md = sh_md[tid + q * cols];
-        if (md.y == 0.f) continue;
-        const float inv = 1.f / md.y;
-        const float4 va = sh_a[tid + q * cols], vb = sh_b[tid + q * cols];
-        tot.fold(md.x, md.y, make_float4(va.x * inv, va.y * inv, va.z * inv, va.w * inv),
-                 make_float4(vb.x * inv, vb.y * inv, vb.z * inv, vb.w * inv));
-      }
-      write_row(tot, row);
-    }
-    __syncthreads();
-  }
+  merge::fold<kMergeThreads>(p, split, sc, blockIdx.x, gridDim.x);
 }
 
 template <typename KV, int D>
@@ -410,9 +279,8 @@ bool mma_decode_supported(const DecodeParams& p) {
   if (int64_t(p.num_seqs) * (max_ctx + 16) * (p.num_heads / G) >= (int64_t(1) << 31)) return false;
   const size_t smem = mma_smem_bytes(p, G, false);
   if (smem == 0) return false;
-  // the merge kernel's offsets and per-row lists fit the default 48 KB with its 20 KB
-  // of static shared memory
-  if (p.grid < 1 || merge_smem_bytes(p.num_seqs, G, p.num_heads, p.grid) > 26 * 1024) return false;
+  // the merge kernel's offsets and scratch fit the default 48 KB
+  if (p.grid < 1 || merge_smem_bytes(p.num_seqs, G, p.num_heads, p.grid) > 46 * 1024) return false;
   return smem > 0 && smem <= 227 * 1024;
 }
 

@@ -18,9 +18,9 @@
 // same rate (on this part some take ~20% longer for the same bytes), and the run-time
 // units let the faster ones take up the slack.  A row that spans several units leaves
 // one partial (m, l, o/l) per unit in a slot fixed by the unit's index, whichever warp
-// ran it, and a small second kernel merges them with the log-sum-exp rule; the main
-// kernel holds no cross-warp synchronisation beyond the claims (a GPU-scope release
-// while the SM streams hundreds of KB cost up to 25 us per warp).
+// ran it, and a small second kernel merges them with the log-sum-exp rule (merge.cuh);
+// the main kernel holds no cross-warp synchronisation beyond the claims (a GPU-scope
+// release while the SM streams hundreds of KB cost up to 25 us per warp).
 //
 // Per warp: lane 0 streams K and V tiles of its stages with TMA tensor copies (128-byte
 // swizzle, so ldmatrix reads are bank-conflict free) into a 3-deep ring of stages, one
@@ -852,6 +852,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
       atomicExch(p.work_ctr + 1, 0);
     }
   }
+
 }
 
 }  // namespace mma

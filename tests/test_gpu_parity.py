@@ -680,6 +680,22 @@ def test_tensor_kernel_work_split_settings(share, chunk, work_split):
     assert torch.equal(runs[0], runs[1]) and torch.equal(runs[0], runs[2])
 
 
+def test_merge_of_rows_of_many_parts(work_split):
+    """Rows cut into many parts (a long context in one-stage run-time units, rows of
+    many sequences folded side by side in one merge block): the merge matches the
+    oracle and launches in a row give identical bits."""
+    work_split(1024, 1)
+    check_workload(wl.long_context(num_seqs=2, context_len=20000))
+    check_workload(wl.continuous_batching(block_size=16, kv_dtype="e4m3", num_seqs=40, num_steps=2,
+                                          median=300, cap=3000, poison=True))
+    w = wl.llama3_8b_decode(seed=33, num_seqs=64, len_range=(100, 2048))
+    dw = DeviceWorkload(w)
+    runs = [dw.run_step(0, out=torch.empty_like(dw.out)).clone() for _ in range(5)]
+    torch.cuda.synchronize()
+    assert binding.read_device_errors() == 0
+    assert all(torch.equal(runs[0], r) for r in runs[1:])
+
+
 def test_tensor_kernel_all_claimed_full_size(work_split):
     """Every stage claimed at run time, more units than the cap allows at one stage
     each (the kernel widens them): the full Llama-3-8B-shaped batch."""
