@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "decode_mma.cuh"
+#include "decode_mma_launch.cuh"
 #include "merge.cuh"
 #include "prefill_mma.cuh"
 
@@ -54,70 +55,11 @@ struct MapCacheEntry {
   int64_t key[7] = {};
   CUtensorMap map;
 };
-constexpr int kMapCacheDevices = 64, kMapCacheSlots = 4;
+constexpr int kMapCacheSlots = 4;
 MapCacheEntry g_map_cache[kMapCacheDevices][kMapCacheSlots];
 int g_map_cache_next[kMapCacheDevices];
 std::mutex g_map_mutex;
 
-cudaError_t cached_cache_map(CUtensorMap* out, const void* base, const DecodeParams& p, int box_rows) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMapCacheDevices) return make_cache_map(out, base, p, box_rows);
-  const int64_t key[7] = {p.kv_dtype, p.head_dim, p.block_size, p.num_kv_heads, p.num_blocks, p.cs_head,
-                          p.cs_block * 64 + box_rows};
-  std::lock_guard<std::mutex> lock(g_map_mutex);
-  for (auto& e : g_map_cache[dev]) {
-    if (e.base == base && std::equal(key, key + 7, e.key)) {
-      *out = e.map;
-      return cudaSuccess;
-    }
-  }
-  MapCacheEntry& e = g_map_cache[dev][g_map_cache_next[dev]];
-  cudaError_t r = make_cache_map(&e.map, base, p, box_rows);
-  if (r != cudaSuccess) {
-    e.base = nullptr;
-    return r;
-  }
-  e.base = base;
-  std::copy(key, key + 7, e.key);
-  g_map_cache_next[dev] = (g_map_cache_next[dev] + 1) % kMapCacheSlots;
-  *out = e.map;
-  return cudaSuccess;
-}
-
-template <typename KV, int D, int G>
-cudaError_t launch_tpl(const DecodeParams& p, cudaStream_t stream) {
-  using C = mma::Cfg<KV, D, G>;
-  const int box_rows = p.block_size < mma::kST ? p.block_size : mma::kST;
-  CUtensorMap mk, mv;
-  cudaError_t e = cached_cache_map(&mk, p.key_cache, p, box_rows);
-  if (e != cudaSuccess) return e;
-  if ((e = cached_cache_map(&mv, p.value_cache, p, box_rows)) != cudaSuccess) return e;
-  const size_t smem = C::smem_bytes(p.num_seqs, p.fused_append);
-  auto kern = mma::paged_decode_mma_kernel<KV, D, G>;
-  // raise the kernel's shared-memory limit only when a launch needs more than before
-  static size_t smem_set[kMapCacheDevices] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= kMapCacheDevices || smem > smem_set[dev]) {
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) != cudaSuccess)
-      return e;
-    if (dev >= 0 && dev < kMapCacheDevices) smem_set[dev] = smem;
-  }
-  static_assert(mma::kWarps == kMmaWarps, "warps per block");
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(p.grid));
-  cfg.blockDim = dim3(unsigned(mma::kThreads));
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = p.overlap_prologue ? 1 : 0;
-  e = cudaLaunchKernelEx(&cfg, kern, mk, mv, p);
-  note_launch();
-  return e != cudaSuccess ? e : cudaGetLastError();
-}
 
 // Merge of rows split across units of work.  A persistent grid; block b owns rows b,
 // b + grid, ...
@@ -225,6 +167,32 @@ int prefill_heads_per_block(int group) {
 
 }  // namespace
 
+// Tensor map of a cache pool, from a small per-device cache of recent ones.
+cudaError_t cached_cache_map(CUtensorMap* out, const void* base, const DecodeParams& p, int box_rows) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMapCacheDevices) return make_cache_map(out, base, p, box_rows);
+  const int64_t key[7] = {p.kv_dtype, p.head_dim, p.block_size, p.num_kv_heads, p.num_blocks, p.cs_head,
+                          p.cs_block * 64 + box_rows};
+  std::lock_guard<std::mutex> lock(g_map_mutex);
+  for (auto& e : g_map_cache[dev]) {
+    if (e.base == base && std::equal(key, key + 7, e.key)) {
+      *out = e.map;
+      return cudaSuccess;
+    }
+  }
+  MapCacheEntry& e = g_map_cache[dev][g_map_cache_next[dev]];
+  cudaError_t r = make_cache_map(&e.map, base, p, box_rows);
+  if (r != cudaSuccess) {
+    e.base = nullptr;
+    return r;
+  }
+  e.base = base;
+  std::copy(key, key + 7, e.key);
+  g_map_cache_next[dev] = (g_map_cache_next[dev] + 1) % kMapCacheSlots;
+  *out = e.map;
+  return cudaSuccess;
+}
+
 bool prefill_supported(const DecodeParams& p) {
   if (p.q_dtype != kBF16 || p.out_dtype != kBF16 || p.kv_dtype != kBF16) return false;
   if (!(p.head_dim == 64 || p.head_dim == 128)) return false;
@@ -285,18 +253,7 @@ bool mma_decode_supported(const DecodeParams& p) {
 }
 
 cudaError_t launch_decode_mma_main(const DecodeParams& p, cudaStream_t stream) {
-  const int G = p.heads_per_item;
-#define PKV_MMA_CASE(KVT, DD, GG) \
-  if (G == GG) return launch_tpl<KVT, DD, GG>(p, stream);
-  if (p.kv_dtype == kBF16 && p.head_dim == 128) {
-    PKV_MMA_CASE(BF16, 128, 4) PKV_MMA_CASE(BF16, 128, 8) PKV_MMA_CASE(BF16, 128, 16)
-  } else if (p.kv_dtype == kBF16 && p.head_dim == 64) {
-    PKV_MMA_CASE(BF16, 64, 4) PKV_MMA_CASE(BF16, 64, 8) PKV_MMA_CASE(BF16, 64, 16)
-  } else if (p.kv_dtype == kE4M3 && p.head_dim == 128) {
-    PKV_MMA_CASE(E4M3, 128, 4) PKV_MMA_CASE(E4M3, 128, 8) PKV_MMA_CASE(E4M3, 128, 16)
-  }
-#undef PKV_MMA_CASE
-  return cudaErrorInvalidValue;
+  return p.fused_append ? launch_decode_mma_main_append(p, stream) : launch_main<false>(p, stream);
 }
 
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream) {

@@ -231,7 +231,10 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const Geometry& q) {
   }
 }
 
-template <typename KV, int D, int G>
+// kAppend: the fused append (the new token of every sequence stored and patched into
+// the stage that holds its position); a separate instantiation, so that plain decode
+// calls carry none of its code.
+template <typename KV, int D, int G, bool kAppend>
 __global__ void __launch_bounds__(kThreads, 1)
 paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                         const DecodeParams p) {
@@ -306,7 +309,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
   int* tags = reinterpret_cast<int*>(smem + C::tag_offset(S)) + warp * 2 * C::kStages;
   int* tail_blk = tags + C::kStages;   // per slot: table entry holding the row's position L - 1
   unsigned char* abase = smem + C::append_offset(S) + size_t(warp) * C::kStages * C::kAppendBytes;
-  const int aeb = p.new_dtype == kF32 ? 4 : 2;  // bytes of an appended element as given
+  const int aeb = kAppend && p.new_dtype == kF32 ? 4 : 2;  // bytes of an appended element as given
 
   // cursor at the first stage of unit u
   auto unit_cursor = [&](int u) {
@@ -419,7 +422,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
     // fused append: the row's last stage also brings the sequence's new K and V rows
     // (two bulk copies on the same barrier); its slot is loaded into a register of
     // lane `islot`, read when the stage is consumed
-    const bool app = p.fused_append && icur.t0 + kST >= icur.rl;
+    const bool app = kAppend && icur.t0 + kST >= icur.rl;
     const uint32_t arow = uint32_t(D * aeb);
     if (lane == 0)
       mbar_arrive_expect_tx(&bars[islot], uint32_t(kOpsPerBox * nbox) * box_bytes + (app ? 2u * arow : 0u));
@@ -575,7 +578,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
     // where this call's new token goes.  Encode it as the cache write would, store it
     // to its slot and put it into the tile just copied (which holds the slot's old
     // bytes).  A token whose slot is not that position is only stored.
-    if (p.fused_append && cc.t0 + kST >= cc.rl) {
+    if (kAppend && cc.t0 + kST >= cc.rl) {
       const int64_t slot_w = __shfl_sync(0xffffffffu, pend_slot, slot);
       if (slot_w >= 0) {
         if (slot_w >= p.num_blocks * int64_t(bs)) {
