@@ -499,6 +499,8 @@ def run_gpu(args, world, rank, local):
     except Exception:
         l2_bytes = 129 << 20
     joint = STEP_MODES[args.step_mode]
+    if args.step_mode == "fused":
+        binding.set_option("fused_append", 2)   # the write inside the decode kernel
     step0_bytes = decode_bytes(w, w.steps[0])
     back_to_back = step0_bytes > 2 * l2_bytes and not any(st.cow_pairs.numel() for st in w.steps)
     for i in range(args.warmup):
@@ -672,9 +674,10 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle CPU time")
     ap.add_argument("--decode-kernel", choices=["auto", "tensor", "core"], default="auto",
                     help="decode kernel: chosen by the library, tensor-core, or CUDA-core")
-    ap.add_argument("--step-mode", choices=sorted(STEP_MODES), default="fused",
-                    help="how a decode step's cache write is issued: fused into the decode kernel, "
-                         "joint (write + dependent decode launch in one call), or split (two calls)")
+    ap.add_argument("--step-mode", choices=sorted(STEP_MODES), default="joint",
+                    help="how a decode step's cache write is issued: joint (write + dependent decode "
+                         "launch in one call), fused (the write inside the decode kernel), or split "
+                         "(two calls)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("at least 3 warm-up steps")

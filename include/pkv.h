@@ -380,11 +380,12 @@ int32_t pkv_abi_version(void);
  * PKV_OPT_DYNAMIC_CHUNK (tensor-core kernel): fewest 16-token stages per run-time unit
  * (1 to 64, default 4).  Neither option changes which values are computed, only which
  * warp computes them (and so the rounding order of split rows).
- * PKV_OPT_FUSED_APPEND (pkv_decode_append): 0 = automatic (the write inside the decode
- * kernel for a 16-bit cache; for an 8-bit cache, whose kernel is bound by instruction
- * issue, the write as its own launch with the decode depending on it), 1 = always the
- * separate write, 2 = always inside the decode kernel (when the tensor-core kernel
- * runs).  The cache bytes and outputs are the same either way.
+ * PKV_OPT_FUSED_APPEND (pkv_decode_append): 0 = automatic, 1 = the write as a kernel of
+ * its own with the decode kernel launched as its programmatic dependent (as in
+ * pkv_decode_step), 2 = the write inside the tensor-core decode kernel.  Automatic is
+ * 1: on GB300 the small write kernel runs while the decode kernel prepares, whereas the
+ * in-kernel write lengthens the warps that hold sequence ends.  The cache bytes and
+ * outputs are the same either way.
  * pkv_set_option returns PKV_ERR_INVALID_ARG for an unknown option or a bad value.
  */
 typedef enum pkv_option {

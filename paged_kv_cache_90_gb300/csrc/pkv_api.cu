@@ -748,13 +748,14 @@ pkv_status pkv_decode_append(const pkv_tensor* out, const pkv_tensor* query, con
     if ((st = ensure_workspace(s, ws_bytes, cs))) return st;
     decode_set_workspace(&p, s->ws);
   }
-  const int64_t mode = g_opt_fused_append.load();
-  const bool fused = mode == 2 || (mode == 0 && p.kv_dtype != kE4M3);
+  // Automatic: the write, then the decode launched as its programmatic dependent (as in
+  // decode_step).  Measured on GB300 that is faster than the write inside the decode
+  // kernel for both cache types: the small write kernel runs while the decode kernel
+  // prepares, whereas the in-kernel append sits on the critical path of the warps
+  // that hold sequence ends.  The CUDA-core kernel has no fused write, and very many
+  // sequences leave no room for the staged tokens.
+  const bool fused = g_opt_fused_append.load() == 2;
   if (no_decode || p.kernel != 1 || !fused || !mma_fused_append_fits(p)) {
-    // the CUDA-core kernel has no fused write (and very many sequences leave no room
-    // for the staged tokens); an 8-bit cache's kernel is bound by instruction issue and
-    // the warps holding many sequence ends would fall behind: the write, then the
-    // decode as in decode_step
     if (!no_write) {
       cudaError_t e = launch_reshape_and_cache(wp, cs);
       if (e != cudaSuccess || no_decode) return finish_call(s, e, cs, "decode_append (cache write)");

@@ -53,7 +53,7 @@ class DeviceWorkload:
         self.out = torch.empty(s, hq, d, dtype=w.q_dtype, device=self.device)
 
     def run_step(self, i: int, out: Optional[torch.Tensor] = None, stream=None,
-                 step: Optional[DeviceStep] = None, joint="fused") -> torch.Tensor:
+                 step: Optional[DeviceStep] = None, joint=True) -> torch.Tensor:
         """Run step ``i`` (or the given device-resident inputs) on the current
         stream; returns the decode output tensor.  ``joint``: "fused" issues the step as
         one decode_append call (the write inside the decode kernel; one new token per
@@ -66,7 +66,7 @@ class DeviceWorkload:
 
 
 def run_decode_step(w: Workload, key_cache, value_cache, st: DeviceStep, out, stream=None,
-                    joint="fused", k_head_scales=None, v_head_scales=None) -> None:
+                    joint=True, k_head_scales=None, v_head_scales=None) -> None:
     if st.cow_pairs.numel():
         binding.copy_blocks(key_cache, st.cow_pairs, stream)
         binding.copy_blocks(value_cache, st.cow_pairs, stream)

@@ -592,11 +592,15 @@ def test_launch_count_and_determinism(kernel):
     # write + decode main kernel + merge of split contexts
     assert binding.launch_count() - n0 == 2 * 3
     assert torch.equal(a, b)
-    # the fused append folds the write into the tensor-core kernel; the CUDA-core
-    # kernel keeps the separate write
-    n0 = binding.launch_count()
-    c = dw.run_step(0, out=torch.empty_like(dw.out), joint="fused").clone()
-    torch.cuda.synchronize()
+    # the fused append, forced, folds the write into the tensor-core kernel; the
+    # CUDA-core kernel keeps the separate write
+    binding.set_option("fused_append", 2)
+    try:
+        n0 = binding.launch_count()
+        c = dw.run_step(0, out=torch.empty_like(dw.out), joint="fused").clone()
+        torch.cuda.synchronize()
+    finally:
+        binding.set_option("fused_append", 0)
     assert binding.launch_count() - n0 == (2 if kernel == "tensor" else 3)
     assert torch.equal(a, c)
 
