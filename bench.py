@@ -48,8 +48,8 @@ from paged_kv_cache_90_gb300.decode_step import DeviceStep, DeviceWorkload, run_
 METRIC = "paged decode attention: effective KV-read GB/s (% of HBM peak), µs/step"
 UNIT = "GB/s"
 L2_FLUSH_BYTES = 256 << 20
-DECODE_SOURCES = ["decode_core.cuh", "decode_mma.cuh", "decode_mma.cu", "decode_dispatch.cu", "device_common.cuh",
-                  "pkv_internal.h"]
+DECODE_SOURCES = ["decode_core.cuh", "decode_mma.cuh", "decode_mma.cu", "decode_mma_launch.cuh", "merge.cuh",
+                  "decode_dispatch.cu", "device_common.cuh", "pkv_internal.h"]
 
 
 # ---- workloads -----------------------------------------------------------------------
