@@ -516,7 +516,12 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
 
   while (true) {
     while (issued - consumed < uint32_t(C::kStages)) {  // keep the ring full
-      if (icur.left == 0 && !next_unit()) break;
+      if (icur.left == 0) {
+        if (!next_unit()) break;
+        // a new unit's table window is on its way: consume a stage while it loads
+        // (unless the ring is empty) rather than wait for it here
+        if (issued != consumed) break;
+      }
       issue_stage();
     }
     if (consumed == issued) break;  // nothing in flight and nothing left to claim
