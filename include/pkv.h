@@ -15,8 +15,8 @@
  *                                last W positions; blocks before them never read);
  *   pkv_paged_attention_prefill  causal attention of a prompt's (or a prompt chunk's)
  *                                new tokens over the cache;
- *   pkv_decode_append            a decode step whose cache write happens inside the
- *                                decode kernel (one new token per sequence).
+ *   pkv_decode_append            a decode step of one new token per sequence whose
+ *                                cache write can run inside the decode kernel.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -144,18 +144,20 @@ pkv_status pkv_paged_attention_decode(const pkv_tensor* out, const pkv_tensor* q
                                       int32_t max_blocks_per_seq, pkv_stream stream);
 
 /*
- * pkv_decode_append — one decode step with the cache write fused into the decode
+ * pkv_decode_append — one decode step whose cache write can be fused into the decode
  * kernel: the same results as pkv_decode_step when token s of key / value is sequence
  * s's newest token (num_tokens == num_seqs, slot_mapping[s] the slot of position
  * context_lens[s] - 1 of sequence s, or < 0 for none), the usual layout of a decode step.
+ * With PKV_OPT_FUSED_APPEND = 2 the write runs inside the decode kernel as described
+ * below; by default (measured faster on GB300) it runs as in pkv_decode_step.
  *
  * Defined by: the write and decode definitions above (vasteelab.pages.dev
  * "PagedAttentionとは？", section "PagedAttentionはAttention kernelとmemory managerの
  * 組み合わせである").
  *
- * The warp of the decode kernel that reads a sequence's last positions encodes its new
- * token as pkv_reshape_and_cache would, stores it to its slot and uses it directly, so
- * no separate write kernel runs and the decode waits for none.  A token whose slot is
+ * Fused, the warp of the decode kernel that reads a sequence's last positions encodes
+ * its new token as pkv_reshape_and_cache would, stores it to its slot and uses it
+ * directly, so no separate write kernel runs and the decode waits for none.  A token whose slot is
  * not its sequence's position L - 1 is stored only (as the two-call form would, provided
  * no sequence reads another sequence's new slot in the same step — which a correct block
  * manager never lets happen).  Where the library would run the CUDA-core decode kernel,

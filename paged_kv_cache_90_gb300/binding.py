@@ -171,9 +171,10 @@ def decode_append(out, query, key, value, slot_mapping, key_cache, value_cache, 
                   num_kv_heads: int, scale: float, block_size: int, max_blocks_per_seq: int,
                   k_scale: float = 1.0, v_scale: float = 1.0, stream=None, sliding_window: int = 0,
                   k_head_scales=None, v_head_scales=None) -> torch.Tensor:
-    """decode_step with the cache write inside the decode kernel: token s of ``key`` /
-    ``value`` must be sequence s's newest token (its slot the position
-    context_lens[s] - 1).  Returns ``out``."""
+    """decode_step for one new token per sequence (token s of ``key`` / ``value`` is
+    sequence s's newest, its slot the position context_lens[s] - 1); with the
+    ``fused_append`` option at 2 the write runs inside the decode kernel.  Returns
+    ``out``."""
     lib = load_library()
     descs = [describe(out), describe(query), describe(key), describe(value), describe(slot_mapping),
              describe(key_cache, k_scale, k_head_scales), describe(value_cache, v_scale, v_head_scales),

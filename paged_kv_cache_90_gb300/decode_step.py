@@ -56,8 +56,9 @@ class DeviceWorkload:
                  step: Optional[DeviceStep] = None, joint=True) -> torch.Tensor:
         """Run step ``i`` (or the given device-resident inputs) on the current
         stream; returns the decode output tensor.  ``joint``: "fused" issues the step as
-        one decode_append call (the write inside the decode kernel; one new token per
-        sequence), True as one decode_step call, False as a write and a decode call."""
+        one decode_append call (one new token per sequence; the write inside the decode
+        kernel when the fused_append option is 2), True (the default) as one
+        decode_step call, False as a write and a decode call."""
         st = step if step is not None else self.steps[i]
         out = self.out if out is None else out
         run_decode_step(self.w, self.key_cache, self.value_cache, st, out, stream, joint,
