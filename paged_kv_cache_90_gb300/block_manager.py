@@ -25,10 +25,16 @@ What it follows:
   in place.
 * Finished sequences return their blocks to the pool (ya.zerocoder.ru
   "Что такое PagedAttention", section "Учебная трасса: рост последовательности").
+* Prefix caching on top of the pool (:class:`PrefixCache`): a full block is identified
+  by the hash of its parent block's identity, the tokens it holds and the request's
+  model conditions (adapter id, multimodal input hashes), so a later prompt that starts
+  with the same tokens under the same conditions reuses the blocks instead of computing
+  them again (vasteelab.pages.dev "PagedAttentionとは？", section "Prefix Cachingとの違い").
 """
 from __future__ import annotations
 
-from collections import deque
+import hashlib
+from collections import OrderedDict, deque
 from dataclasses import dataclass, field
 from typing import Iterable, List, Optional, Sequence, Tuple
 
@@ -205,15 +211,17 @@ class BlockManager:
         return len(s.blocks) * self.bs - s.length
 
     # -- structural checks -------------------------------------------------
-    def check_structure(self) -> None:
+    def check_structure(self, held: Iterable[int] = ()) -> None:
         """Structural correctness: every table entry is an allocated block (or, in a
         leading run, a block released after it left a sliding window), each
         sequence's table covers its tokens exactly, reference counts equal the number
-        of table entries pointing at each block, and no free block is referenced
-        (ya.zerocoder.ru, section "Учебная трасса: рост последовательности": the
-        table references existing blocks, reference counts balance, frees leave
-        nothing dangling)."""
+        of table entries pointing at each block plus the references ``held`` by other
+        owners (a prefix cache), and no free block is referenced (ya.zerocoder.ru,
+        section "Учебная трасса: рост последовательности": the table references
+        existing blocks, reference counts balance, frees leave nothing dangling)."""
         counts = [0] * self.alloc.num_blocks
+        for b in held:
+            counts[b] += 1
         for sid, s in self.seqs.items():
             if len(s.blocks) != blocks_needed(s.length, self.bs):
                 raise AssertionError(f"sequence {sid}: {len(s.blocks)} blocks for {s.length} tokens")
@@ -251,3 +259,93 @@ def validate_cow_pairs(pairs: Sequence[Tuple[int, int]], num_blocks: int) -> Non
             raise ValueError(f"pair ({s}, {d}) outside the pool")
         if d in srcs:
             raise ValueError(f"block {d} is both a source and a destination")
+
+
+class PrefixCache:
+    """Reuse of full blocks computed for earlier prompts, over a :class:`BlockManager`.
+
+    A full block's identity is a hash chained from its parent's: H(parent identity,
+    the block's tokens, the request's extra keys such as an adapter id or multimodal
+    input hashes).  Equal identities mean equal tokens at equal positions under equal
+    conditions, hence equal keys and values, so the block can be shared.  Only full
+    blocks are identified (a partial block still grows).  The cache keeps one reference
+    to every block it identifies, so a block outlives the sequences that computed it
+    until :meth:`evict` drops it (least recently used first, and only blocks no
+    sequence holds).  Blocks are identified when their prompt is added: the cache write
+    of that step puts their keys and values in place before any later attention reads
+    them.
+    """
+
+    def __init__(self, manager: BlockManager):
+        self.mgr = manager
+        self.by_hash: "OrderedDict[bytes, int]" = OrderedDict()  # identity -> block, oldest use first
+
+    @staticmethod
+    def block_hash(parent: Optional[bytes], tokens: Sequence[int], extra: Sequence = ()) -> bytes:
+        h = hashlib.sha256()
+        h.update(parent if parent is not None else bytes(32))
+        h.update(len(tokens).to_bytes(4, "little"))
+        for t in tokens:
+            h.update(int(t).to_bytes(8, "little", signed=True))
+        h.update(repr(tuple(extra)).encode())
+        return h.digest()
+
+    def add_prompt(self, seq_id, tokens: Sequence[int], extra: Sequence = ()) -> Tuple[List[int], int]:
+        """Register ``seq_id`` with a prompt.  Its longest run of leading full blocks
+        whose identities are cached is shared (reference counts go up); blocks are
+        reserved for the rest, and the new full blocks are identified.  At least the
+        last token is always computed (a prompt cached whole gives back its last block
+        and computes it again).  Returns (slots of the tokens still to compute, in
+        position order, number of cached tokens)."""
+        mgr, bs = self.mgr, self.mgr.bs
+        if seq_id in mgr.seqs:
+            raise ValueError(f"sequence {seq_id} exists")
+        tokens = list(tokens)
+        nfull = len(tokens) // bs
+        ids, parent = [], None
+        for i in range(nfull):
+            parent = self.block_hash(parent, tokens[i * bs:(i + 1) * bs], extra)
+            ids.append(parent)
+        reused = []
+        for h in ids:
+            b = self.by_hash.get(h)
+            if b is None:
+                break
+            reused.append(b)
+        if reused and len(reused) * bs == len(tokens):
+            reused.pop()
+        for i, b in enumerate(reused):
+            mgr.alloc.incref(b)
+            self.by_hash.move_to_end(ids[i])
+        cached = len(reused) * bs
+        mgr.seqs[seq_id] = SequenceBlocks(blocks=list(reused), length=cached)
+        slots = []
+        for _ in range(len(tokens) - cached):
+            slot, pair = mgr.append_token(seq_id)
+            assert pair is None  # new tokens go to fresh blocks: reused blocks are full
+            slots.append(slot)
+        blocks = mgr.seqs[seq_id].blocks
+        for i in range(len(reused), nfull):
+            if ids[i] not in self.by_hash:
+                self.by_hash[ids[i]] = blocks[i]
+                mgr.alloc.incref(blocks[i])  # the cache's own reference
+        return slots, cached
+
+    def held(self) -> List[int]:
+        """The blocks the cache holds a reference to."""
+        return list(self.by_hash.values())
+
+    def evict(self, n: int) -> int:
+        """Drop up to ``n`` identified blocks that no sequence holds, least recently
+        used first, returning them to the pool; returns how many were dropped."""
+        dropped = 0
+        for h in list(self.by_hash):
+            if dropped >= n:
+                break
+            b = self.by_hash[h]
+            if self.mgr.alloc.refcount[b] == 1:
+                del self.by_hash[h]
+                self.mgr.alloc.decref(b)
+                dropped += 1
+        return dropped
+

@@ -181,3 +181,74 @@ def test_release_outside_window():
     mgr.check_structure()
     mgr.free_sequence("a")
     mgr.check_structure()
+
+
+# ---- prefix caching --------------------------------------------------------------
+
+def _kv_of(tokens, pos):
+    """Stand-in for a layer's key at a position: a function of the prefix it sees
+    (the token and everything before it), as a model's keys are."""
+    return hash((tuple(tokens[:pos + 1]),)) & 0xFFFFFFFF
+
+
+def _pool_with_cache(num_blocks=64, bs=16):
+    from paged_kv_cache_90_gb300.block_manager import PrefixCache
+    mgr = BlockManager(BlockAllocator(num_blocks, bs, free_order=list(reversed(range(num_blocks)))))
+    return mgr, PrefixCache(mgr)
+
+
+def test_prefix_cache_shares_full_blocks_of_a_common_prefix():
+    """Two prompts with a common 32-token prefix at 16 tokens per block: the second
+    shares both full blocks and computes only its own 9 tokens; the tables agree on
+    the shared blocks and every slot the second prompt reads holds its own keys."""
+    mgr, pc = _pool_with_cache()
+    a = list(range(100, 140))                       # 40 tokens: blocks 0, 1 full, 2 partial
+    b = a[:32] + list(range(500, 509))              # 41 tokens
+    pool = {}
+    slots, cached = pc.add_prompt("a", a)
+    assert cached == 0 and len(slots) == 40
+    for pos, sl in enumerate(slots):
+        pool[sl] = _kv_of(a, pos)
+    slots, cached = pc.add_prompt("b", b)
+    assert cached == 32 and len(slots) == 9
+    for i, sl in enumerate(slots):
+        pool[sl] = _kv_of(b, 32 + i)
+    assert mgr.seqs["b"].blocks[:2] == mgr.seqs["a"].blocks[:2]
+    assert mgr.seqs["b"].blocks[2] != mgr.seqs["a"].blocks[2]
+    for pos in range(len(b)):                       # what attention gathers through b's table
+        assert pool[mgr.seqs["b"].slot(pos, 16)] == _kv_of(b, pos)
+    mgr.check_structure(held=pc.held())
+
+
+def test_prefix_cache_identity_is_chained_and_conditioned():
+    mgr, pc = _pool_with_cache()
+    a = list(range(48))
+    pc.add_prompt("a", a)
+    assert pc.add_prompt("lora", a + [7], extra=("adapter", 3))[1] == 0   # other conditions
+    c = list(a)
+    c[3] = 999                                                            # block 0 differs
+    assert pc.add_prompt("c", c + [7])[1] == 0                            # so no later block matches
+    d = list(a)
+    d[20] = 999                                                           # block 1 differs
+    assert pc.add_prompt("d", d + [7])[1] == 16
+    assert pc.add_prompt("e", a[:40])[1] == 32                            # partial last block: never shared
+    assert pc.add_prompt("f", a)[1] == 32                                 # cached whole: the last block is recomputed
+    assert mgr.seqs["f"].blocks[2] != mgr.seqs["a"].blocks[2]
+    mgr.check_structure(held=pc.held())
+
+
+def test_prefix_cache_outlives_sequences_until_evicted():
+    mgr, pc = _pool_with_cache(num_blocks=8)
+    a = list(range(40))
+    pc.add_prompt("a", a)                            # 3 blocks, 2 identified
+    mgr.free_sequence("a")
+    assert mgr.alloc.num_free == 6                   # the cache still holds the 2 full blocks
+    mgr.check_structure(held=pc.held())
+    assert pc.add_prompt("b", a)[1] == 32            # a later request finds them
+    assert pc.evict(10) == 0                         # b holds them: nothing to drop
+    mgr.free_sequence("b")
+    assert pc.evict(1) == 1 and mgr.alloc.num_free == 7   # least recently used first
+    assert pc.evict(10) == 1 and mgr.alloc.num_free == 8
+    assert pc.held() == []
+    mgr.check_structure()
+    assert pc.add_prompt("c", a)[1] == 0
