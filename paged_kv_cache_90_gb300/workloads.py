@@ -25,7 +25,7 @@ from typing import List, Optional, Sequence
 
 import torch
 
-from .block_manager import BlockAllocator, BlockManager, blocks_needed, validate_cow_pairs
+from .block_manager import BlockAllocator, BlockManager, PrefixCache, blocks_needed, validate_cow_pairs
 
 DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}
 DTYPE_NAMES = {v: k for k, v in DTYPES.items()}
@@ -445,6 +445,64 @@ def chunked_prefill(seed: int = 7, prefix_lens: Sequence[int] = (0, 0, 512, 1536
                    num_kv_heads, head_dim, block_size, nb, mb, kc, vc, ks, vs, [step])
 
 
+def prefix_cached_prefill(seed: int = 10, system_len: int = 700, suffix_lens: Sequence[int] = (90, 1, 300, 17, 64),
+                          num_heads: int = 32, num_kv_heads: int = 8, head_dim: int = 128, block_size: int = 16,
+                          kv_dtype: str = "bf16", poison: bool = False) -> Workload:
+    """Prompts that share a system prompt, through the prefix cache: an earlier request
+    computed the system prompt (its K/V are in the pool, its full blocks identified, the
+    request gone), then each prompt (system prompt + its own suffix) shares the cached
+    full blocks and prefills only the rest — one chunked-prefill step whose sequences
+    all read the same physical prefix blocks."""
+    g = torch.Generator().manual_seed(seed)
+    suffix = [int(x) for x in suffix_lens]
+    if min(suffix) < 1 or system_len < 1:
+        raise ValueError("a system prompt and at least one suffix token per prompt")
+    vocab = 32000
+    system = torch.randint(0, vocab, (system_len,), generator=g).tolist()
+    prompts = [system + torch.randint(0, vocab, (n,), generator=g).tolist() for n in suffix]
+    need = blocks_needed(system_len + 1, block_size) + sum(blocks_needed(len(t), block_size) for t in prompts)
+    nb = need + 8
+    perm = torch.randperm(nb, generator=g).tolist()
+    mgr = BlockManager(BlockAllocator(nb, block_size, perm))
+    cache = PrefixCache(mgr)
+    cache.add_prompt("earlier", system + [0])   # computed before this step; its K/V are the pool's
+    kc, vc, ks, vs, _, _ = _make_pool(nb, num_kv_heads, block_size, head_dim, kv_dtype, g)
+    mgr.free_sequence("earlier")                # the cache keeps its full blocks
+    seq_ids = list(range(len(prompts)))
+    slots, chunk = [], []
+    for sid, t in zip(seq_ids, prompts):
+        sl, cached = cache.add_prompt(sid, t)
+        slots += sl
+        chunk.append(len(t) - cached)
+    mgr.check_structure(held=cache.held())
+    if poison:
+        # the step writes the new tokens' slots; the shared prefix blocks hold the
+        # earlier request's K/V; everything else unused is NaN
+        occ = _occupied_slots(mgr)
+        new = torch.tensor(slots, dtype=torch.int64)
+        keep = occ[~torch.isin(occ, new)]
+        _poison(kc, keep)
+        _poison(vc, keep)
+    mb = max(blocks_needed(len(t), block_size) for t in prompts)
+    tq = sum(chunk)
+    src = torch.bfloat16 if kv_dtype == "e4m3" else DTYPES[kv_dtype]
+    q_dtype = torch.float32 if kv_dtype == "f32" else torch.bfloat16
+    qsl = [0]
+    for c in chunk:
+        qsl.append(qsl[-1] + c)
+    step = DecodeStep(
+        query=_randn((tq, num_heads, head_dim), q_dtype, g),
+        new_key=_randn((tq, num_kv_heads, head_dim), src, g),
+        new_value=_randn((tq, num_kv_heads, head_dim), src, g),
+        slot_mapping=torch.tensor(slots, dtype=torch.int64),
+        block_tables=torch.tensor(mgr.block_table_rows(seq_ids, mb), dtype=torch.int32).view(len(seq_ids), mb),
+        context_lens=torch.tensor([len(t) for t in prompts], dtype=torch.int32),
+        cow_pairs=torch.zeros(0, 2, dtype=torch.int64),
+        query_start_loc=torch.tensor(qsl, dtype=torch.int32))
+    return _finish(f"prefix_cached_prefill_s{len(prompts)}_sys{system_len}_bs{block_size}_{kv_dtype}", seed,
+                   num_heads, num_kv_heads, head_dim, block_size, nb, mb, kc, vc, ks, vs, [step])
+
+
 WORKLOADS = {
     "tiny": tiny,
     "llama3_8b_decode": llama3_8b_decode,
@@ -453,4 +511,5 @@ WORKLOADS = {
     "continuous_batching": continuous_batching,
     "sliding_window": sliding_window_decode,
     "chunked_prefill": chunked_prefill,
+    "prefix_cached_prefill": prefix_cached_prefill,
 }

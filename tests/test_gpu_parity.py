@@ -734,3 +734,12 @@ def test_tensor_core_kernel_rejects_what_it_cannot_run():
         assert ei.value.status == 2
     finally:
         binding.set_option("decode_kernel", 0)
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_prefill_over_prefix_cached_blocks(bs):
+    """Prompts sharing a system prompt's cached blocks through the prefix cache: every
+    sequence of the step reads the same physical prefix blocks and prefills its own
+    suffix (unused slots NaN)."""
+    check_workload(wl.prefix_cached_prefill(seed=20 + bs, system_len=300, suffix_lens=(40, 1, 129, 16, 7),
+                                            block_size=bs, poison=True))

@@ -630,3 +630,33 @@ def test_prefill_first_token_of_a_prompt_returns_its_value():
         for h in range(4):
             v = _gather(vc, st.block_tables[s], h // 2, 1, 4)[0].double()
             assert torch.equal(out[q0, h], v)
+
+
+def test_prefix_cached_prefill_equals_private_copies():
+    """Prompts that share a system prompt's cached blocks (the prefix cache's tables)
+    give, bit for bit, the prefill of tables whose blocks were first copied into
+    private blocks; the shared blocks are really shared."""
+    w = wl.prefix_cached_prefill(seed=12, system_len=70, suffix_lens=(9, 1, 33, 16), num_heads=8,
+                                 num_kv_heads=2, head_dim=64, block_size=16, poison=True)
+    kc, vc = _materialize(w)
+    st = w.steps[0]
+    shared = oracle.paged_attention_prefill(st.query, kc, vc, st.block_tables, st.context_lens,
+                                            st.query_start_loc, w.scale)
+    assert torch.isfinite(shared).all()
+    s = st.block_tables.shape[0]
+    nblk = [-(-int(L) // w.block_size) for L in st.context_lens]
+    kp = torch.full((sum(nblk),) + tuple(kc.shape[1:]), float("nan"), dtype=kc.dtype)
+    vp = torch.full_like(kp, float("nan"))
+    bt = torch.full((s, st.block_tables.shape[1]), -1, dtype=torch.int32)
+    nxt = 0
+    for i in range(s):
+        for j in range(nblk[i]):
+            src = int(st.block_tables[i, j])
+            kp[nxt], vp[nxt] = kc[src], vc[src]
+            bt[i, j] = nxt
+            nxt += 1
+    private = oracle.paged_attention_prefill(st.query, kp, vp, bt, st.context_lens, st.query_start_loc, w.scale)
+    assert torch.equal(shared, private)
+    assert len(set(st.block_tables[:, :4].flatten().tolist())) == 4   # 64 cached tokens: 4 shared blocks
+    qsl = st.query_start_loc.tolist()
+    assert [qsl[i + 1] - qsl[i] for i in range(s)] == [70 + n - 64 for n in (9, 1, 33, 16)]
