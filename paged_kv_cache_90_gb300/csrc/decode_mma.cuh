@@ -29,8 +29,13 @@
 // only moved (and the accumulators rescaled) when a row's max grows by more than 2^8,
 // so the rescale is skipped in the steady state.
 //
-// An 8-bit cache is read the same way; its codes become f16 exactly (e4m3 -> f16), the
-// scores use f16 MMAs, and each stage's values are converted to an f16 staging tile.
+// An 8-bit cache is read the same way; its codes become f16 exactly (e4m3 -> f16) in
+// registers and the MMAs are f16.  The value step needs pairs of consecutive tokens per
+// column, which the token-major tile does not hold: the score columns are ordered so
+// that a thread's P fragment covers four consecutive tokens, and each thread reads one
+// 32-bit word (four columns) per token row and regroups the bytes into token pairs per
+// column with byte permutes; the output columns come out permuted and are written back
+// in place.
 #pragma once
 
 #include <cuda.h>
@@ -123,7 +128,7 @@ struct Cfg {
   static constexpr int kRawTile = kST * kRawRowBytes;      // K (or V) bytes of a stage, as stored
   static constexpr int kStages = (kFp8 || D == 64) ? 4 : 3;
   static constexpr int kStageBytes = 2 * kRawTile;         // K then V
-  static constexpr int kVConv = kFp8 ? kST * D * 2 : 0;    // per-warp f16 copy of a stage's V
+  static constexpr int kVConv = 0;                         // (no staging tile: 8-bit V is widened in registers)
   static constexpr int kRows = G > 8 ? 2 : 1;              // real MMA rows per thread (g, g+8)
   static constexpr int kNT = D / 8;                        // output n-tiles
   static constexpr int kKS = D / 16;                       // k-steps of the score MMA
@@ -248,7 +253,6 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
   const int g = lane >> 2, c4 = lane & 3;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::bar_offset(S)) + warp * C::kStages;
   unsigned char* wbase = smem + C::ring_offset(S) + size_t(warp) * C::kWarpBytes;
-  unsigned char* vconv = wbase + size_t(C::kStages) * C::kStageBytes;   // 8-bit caches only
 
   const int max_ctx = p.max_blocks_per_seq * p.block_size;
   const int tiles = p.num_heads / G;
@@ -484,16 +488,11 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
 #pragma unroll
   for (int i = 0; i < C::kKS / 2; ++i)
     koff[i] = uint32_t((i / 2) * kST * 128 + (lane & 7) * 128 + ((((i % 2) * 4 + (lane >> 3)) ^ (lane & 7)) << 4));
-  constexpr int kVOff = C::kFp8 ? C::kNT / 2 : 4;
-  uint32_t voff[kVOff];        // V: pair of n-tiles (per half for an 8-bit cache)
+  uint32_t voff[4];            // V (16-bit cache): pair of n-tiles
   {
     const int vrow = ((lane >> 3) & 1) * 8 + (lane & 7);
 #pragma unroll
-    for (int i = 0; i < kVOff; ++i) {
-      const int h = C::kFp8 ? i / 4 : 0;
-      const int key = C::kFp8 ? ((lane & 7) ^ h) : (lane & 7);
-      voff[i] = uint32_t(h * kST * 128 + vrow * 128 + (((2 * (i % 4) + (lane >> 4)) ^ key) << 4));
-    }
+    for (int i = 0; i < 4; ++i) voff[i] = uint32_t(vrow * 128 + (((2 * i + (lane >> 4)) ^ (lane & 7)) << 4));
   }
 
   // ---- consumer ----------------------------------------------------------------------
@@ -641,32 +640,8 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
       }
     }
 
-    // values as 16-bit operand rows (8-bit cache: convert; rows past the context: zero)
-    const unsigned char* vop = vt;
-    if constexpr (C::kFp8) {
-      // 16 rows x 8 chunks of 16 codes; lanes 0-7 take one row, so reads are conflict
-      // free; the second half uses a different XOR key so the stores are too
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = i * 4 + (lane >> 3), j = lane & 7;
-        uint4 raw = make_uint4(0, 0, 0, 0);
-        if (r < nvalid) raw = *reinterpret_cast<const uint4*>(vt + r * 128 + ((j ^ (r & 7)) << 4));
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t h16[8];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          h16[2 * q] = e4m3x2_to_f16x2(w[q]);
-          h16[2 * q + 1] = e4m3x2_to_f16x2(w[q] >> 16);
-        }
-        const int hf = j >> 2, key = (r & 7) ^ hf;
-        unsigned char* rowp = vconv + size_t(hf) * kST * 128 + r * 128;
-        const int c0 = 2 * (j & 3);
-        *reinterpret_cast<uint4*>(rowp + ((c0 ^ key) << 4)) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
-        *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ key) << 4)) = make_uint4(h16[4], h16[5], h16[6], h16[7]);
-      }
-      __syncwarp();
-      vop = vconv;
-    } else if (nvalid < kST) {
+    // 16-bit values: rows past the context zeroed (the 8-bit path zeroes them in registers)
+    if (!C::kFp8 && nvalid < kST) {
       const int per_half = (kST - nvalid) * 8;  // 16-byte pieces per half
       for (int i = lane; i < per_half * C::kHalves; i += 32) {
         const int h = i / per_half, rem = i - h * per_half;
@@ -688,7 +663,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
       if constexpr (C::kFp8) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          const int row = nt * 8 + g;
+          const int row = 4 * (g >> 1) + (g & 1) + 2 * nt;  // token of score column nt * 8 + g
 #pragma unroll
           for (int kk = 0; kk < C::kKS; ++kk) {
             const uint32_t w = *reinterpret_cast<const uint32_t*>(kt + row * 128 + ((kk ^ (row & 7)) << 4) + 4 * c4);
@@ -728,7 +703,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int t = nt * 8 + 2 * c4 + e;
+            const int t = C::kFp8 ? 4 * c4 + e + 2 * nt : nt * 8 + 2 * c4 + e;  // the column's token
             if (t >= nvalid || t < lo_valid) s[nt][2 * rr + e] = -INFINITY;
           }
       }
@@ -775,15 +750,37 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
       const uint32_t a2 = pack2(s[1][0], s[1][1], C::kF16);
       const uint32_t a1 = C::kRows > 1 ? pack2(s[0][2], s[0][3], C::kF16) : 0u;
       const uint32_t a3 = C::kRows > 1 ? pack2(s[1][2], s[1][3], C::kF16) : 0u;
-      const uint32_t vbase = smem_addr(vop);
+      if constexpr (C::kFp8) {
+        // tokens 4 c4 .. 4 c4 + 3 (P's k slots 2 c4, 2 c4 + 1, 2 c4 + 8, 2 c4 + 9) at
+        // columns d = 32 m + 4 g + i: one 32-bit word per token row and m, transposed
+        // by byte permutes into token pairs per column and widened to f16 in registers;
+        // n-tile 4 m + i of o holds columns 32 m + 4 n + i
 #pragma unroll
-      for (int n = 0; n < C::kNT; n += 2) {
-        const int i = n / 2;
-        const uint32_t addr = C::kFp8 ? vbase + voff[i] : vbase + voff[i % 4] + (i / 4) * kST * 128;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(addr, b0, b1, b2, b3);
-        mma16816<C::kF16>(o[n], a0, a1, a2, a3, b0, b1);
-        mma16816<C::kF16>(o[n + 1], a0, a1, a2, a3, b2, b3);
+        for (int m = 0; m < 4; ++m) {
+          uint32_t wv[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int r = 4 * c4 + t, b = 32 * m + 4 * g;
+            wv[t] = r < nvalid ? *reinterpret_cast<const uint32_t*>(vt + r * 128 + (((b >> 4) ^ (r & 7)) << 4) + (b & 15))
+                               : 0u;
+          }
+          const uint32_t x01 = __byte_perm(wv[0], wv[1], 0x5140), x23 = __byte_perm(wv[0], wv[1], 0x7362);
+          const uint32_t y01 = __byte_perm(wv[2], wv[3], 0x5140), y23 = __byte_perm(wv[2], wv[3], 0x7362);
+          mma16816<true>(o[4 * m], a0, a1, a2, a3, e4m3x2_to_f16x2(x01), e4m3x2_to_f16x2(y01));
+          mma16816<true>(o[4 * m + 1], a0, a1, a2, a3, e4m3x2_to_f16x2(x01 >> 16), e4m3x2_to_f16x2(y01 >> 16));
+          mma16816<true>(o[4 * m + 2], a0, a1, a2, a3, e4m3x2_to_f16x2(x23), e4m3x2_to_f16x2(y23));
+          mma16816<true>(o[4 * m + 3], a0, a1, a2, a3, e4m3x2_to_f16x2(x23 >> 16), e4m3x2_to_f16x2(y23 >> 16));
+        }
+      } else {
+        const uint32_t vbase = smem_addr(vt);
+#pragma unroll
+        for (int n = 0; n < C::kNT; n += 2) {
+          const int i = n / 2;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vbase + voff[i % 4] + (i / 4) * kST * 128, b0, b1, b2, b3);
+          mma16816<false>(o[n], a0, a1, a2, a3, b0, b1);
+          mma16816<false>(o[n + 1], a0, a1, a2, a3, b2, b3);
+        }
       }
     }
     __syncwarp();
@@ -812,10 +809,22 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
           if (hr < G) {
             const float inv = l_run[rr] > 0.f ? vsc / l_run[rr] : 0.f;
             __nv_bfloat16* out = outs + int64_t(h0 + hr) * p.out_stride_h;
+            if constexpr (C::kFp8) {  // n-tile 4 m + i, column 2 c4 + e: d = 32 m + 8 c4 + 4 e + i
 #pragma unroll
-            for (int n = 0; n < C::kNT; ++n)
-              *reinterpret_cast<__nv_bfloat162*>(out + n * 8 + 2 * c4) =
-                  __floats2bfloat162_rn(o[n][2 * rr] * inv, o[n][2 * rr + 1] * inv);
+              for (int m = 0; m < 4; ++m)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const __nv_bfloat162 lo = __floats2bfloat162_rn(o[4 * m][2 * rr + e] * inv, o[4 * m + 1][2 * rr + e] * inv);
+                  const __nv_bfloat162 hi = __floats2bfloat162_rn(o[4 * m + 2][2 * rr + e] * inv, o[4 * m + 3][2 * rr + e] * inv);
+                  *reinterpret_cast<uint2*>(out + 32 * m + 8 * c4 + 4 * e) =
+                      make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+                }
+            } else {
+#pragma unroll
+              for (int n = 0; n < C::kNT; ++n)
+                *reinterpret_cast<__nv_bfloat162*>(out + n * 8 + 2 * c4) =
+                    __floats2bfloat162_rn(o[n][2 * rr] * inv, o[n][2 * rr + 1] * inv);
+            }
           }
         }
       } else {
@@ -827,10 +836,20 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
             const int64_t pr = int64_t(slot_id) * G + hr;
             const float inv = l_run[rr] > 0.f ? vsc / l_run[rr] : 0.f;
             float* po = p.part_o + pr * D;
+            if constexpr (C::kFp8) {
 #pragma unroll
-            for (int n = 0; n < C::kNT; ++n)
-              *reinterpret_cast<float2*>(po + n * 8 + 2 * c4) =
-                  make_float2(o[n][2 * rr] * inv, o[n][2 * rr + 1] * inv);
+              for (int m = 0; m < 4; ++m)
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                  *reinterpret_cast<float4*>(po + 32 * m + 8 * c4 + 4 * e) =
+                      make_float4(o[4 * m][2 * rr + e] * inv, o[4 * m + 1][2 * rr + e] * inv,
+                                  o[4 * m + 2][2 * rr + e] * inv, o[4 * m + 3][2 * rr + e] * inv);
+            } else {
+#pragma unroll
+              for (int n = 0; n < C::kNT; ++n)
+                *reinterpret_cast<float2*>(po + n * 8 + 2 * c4) =
+                    make_float2(o[n][2 * rr] * inv, o[n][2 * rr + 1] * inv);
+            }
             if (c4 == 0) {
               p.part_m[pr] = m_ref[rr];
               p.part_l[pr] = l_run[rr];
