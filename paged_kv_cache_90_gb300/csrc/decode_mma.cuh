@@ -470,8 +470,9 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
 #pragma unroll
         for (int kk = 0; kk < C::kKS; ++kk) {
           if constexpr (C::kFp8) {
-            // k index 2c, 2c+1, 2c+8, 2c+9 <-> d = 16kk + 4c + {0,1,2,3} (matches the K reads)
-            const uint2 w = __ldg(reinterpret_cast<const uint2*>(q + 16 * kk + 4 * c4));
+            // k index 2c, 2c+1, 2c+8, 2c+9 <-> d = 32c + 4kk + {0,1,2,3} (matches the K reads:
+            // a thread's 32 columns of a key row are two adjacent 16-byte chunks)
+            const uint2 w = __ldg(reinterpret_cast<const uint2*>(q + 32 * c4 + 4 * kk));
             qa[kk][0 + rr] = bf16x2_to_f16x2(w.x);
             qa[kk][2 + rr] = bf16x2_to_f16x2(w.y);
           } else {
@@ -664,12 +665,13 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           const int row = 4 * (g >> 1) + (g & 1) + 2 * nt;  // token of score column nt * 8 + g
+          const uint4 ka = *reinterpret_cast<const uint4*>(kt + row * 128 + (((2 * c4) ^ (row & 7)) << 4));
+          const uint4 kb = *reinterpret_cast<const uint4*>(kt + row * 128 + (((2 * c4 + 1) ^ (row & 7)) << 4));
+          const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
-          for (int kk = 0; kk < C::kKS; ++kk) {
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(kt + row * 128 + ((kk ^ (row & 7)) << 4) + 4 * c4);
+          for (int kk = 0; kk < C::kKS; ++kk)
             mma16816<true>(kk & 1 ? s2[nt] : s[nt], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3],
-                           e4m3x2_to_f16x2(w), e4m3x2_to_f16x2(w >> 16));
-          }
+                           e4m3x2_to_f16x2(kw[kk]), e4m3x2_to_f16x2(kw[kk] >> 16));
         }
       } else {
         const uint32_t kbase = smem_addr(kt);
