@@ -743,3 +743,42 @@ def test_prefill_over_prefix_cached_blocks(bs):
     suffix (unused slots NaN)."""
     check_workload(wl.prefix_cached_prefill(seed=20 + bs, system_len=300, suffix_lens=(40, 1, 129, 16, 7),
                                             block_size=bs, poison=True))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_largest_batch_of_the_tensor_core_kernel(kv, kernel):
+    """4096 sequences (the most the tensor-core kernel takes: its per-sequence offsets
+    fill shared memory) of 1 to 40 tokens, unused slots NaN; steps as write + decode,
+    joint, and with the in-kernel append forced (which falls back to two launches when
+    its staged tokens no longer fit)."""
+    w = wl.variable_length_decode(f"max_batch_{kv}", 73, torch.randint(1, 41, (4096,),
+                                  generator=torch.Generator().manual_seed(73)).tolist(),
+                                  32, 8, 128, 16, kv, poison=True)
+    check_workload(w)
+    runs = {}
+    for mode in ("joint", "forced"):
+        dw = DeviceWorkload(w)
+        binding.set_option("fused_append", 2 if mode == "forced" else 0)
+        try:
+            runs[mode] = dw.run_step(0, out=torch.empty_like(dw.out), joint="fused" if mode == "forced" else True).clone()
+        finally:
+            binding.set_option("fused_append", 0)
+        torch.cuda.synchronize()
+    assert binding.read_device_errors() == 0
+    assert torch.equal(runs["joint"], runs["forced"])
+
+
+def test_one_sequence_past_the_tensor_core_kernels_batch_limit():
+    """4097 sequences: the library runs the CUDA-core kernel on its own, and refuses the
+    forced tensor-core kernel with PKV_ERR_UNSUPPORTED."""
+    lens = [1 + (i % 23) for i in range(4097)]
+    w = wl.variable_length_decode("past_max_batch", 74, lens, 32, 8, 128, 16, "bf16", poison=True)
+    check_workload(w)
+    dw = DeviceWorkload(w)
+    binding.set_option("decode_kernel", 2)
+    try:
+        with pytest.raises(binding.PkvError) as ei:
+            dw.run_step(0)
+        assert ei.value.status == 2
+    finally:
+        binding.set_option("decode_kernel", 0)
