@@ -782,3 +782,31 @@ def test_one_sequence_past_the_tensor_core_kernels_batch_limit():
         assert ei.value.status == 2
     finally:
         binding.set_option("decode_kernel", 0)
+
+
+@pytest.mark.parametrize("draw", range(12))
+def test_random_configurations(draw):
+    """Seeded random draws over the supported space: GQA group, head_dim, block size,
+    cache dtype, window, per-head scales, batch size and a length mix with very short
+    and block-edge contexts; two decode steps each, all against the oracle (the default
+    kernel choice, so both decode kernels meet draws they take)."""
+    g = torch.Generator().manual_seed(1000 + draw)
+    pick = lambda xs: xs[int(torch.randint(0, len(xs), (1,), generator=g))]
+    hk = pick([1, 2, 4, 8])
+    group = pick([1, 3, 4, 8, 16])
+    d = pick([64, 128])
+    bs = pick([2, 4, 8, 16, 32])
+    kv = pick(["bf16", "bf16", "e4m3", "f32"])
+    if kv == "e4m3" and d == 64 and bs < 8:
+        bs = 16
+    q = "f32" if kv == "f32" else "bf16"
+    n = int(torch.randint(1, 48, (1,), generator=g))
+    lens = torch.randint(1, 900, (n,), generator=g).tolist()
+    lens[0] = 1
+    if n > 1:
+        lens[1] = bs * int(torch.randint(1, 20, (1,), generator=g))   # ends on a block edge
+    window = pick([0, 0, 0, 17, 256]) if kv != "f32" else 0
+    spread = 2.0 if (kv == "e4m3" and draw % 2) else 0.0
+    w = wl.variable_length_decode(f"random_{draw}", 2000 + draw, lens, hk * group, hk, d, bs, kv, q_dtype=q,
+                                  num_steps=2, poison=True, window=window, head_spread=spread)
+    check_workload(w)
