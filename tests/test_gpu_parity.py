@@ -810,3 +810,36 @@ def test_random_configurations(draw):
     w = wl.variable_length_decode(f"random_{draw}", 2000 + draw, lens, hk * group, hk, d, bs, kv, q_dtype=q,
                                   num_steps=2, poison=True, window=window, head_spread=spread)
     check_workload(w)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_decode_step_replayed_from_a_cuda_graph(kv):
+    """A decode step (cache write, then the decode launched as its programmatic
+    dependent, then the merge) captured into a CUDA graph after the workspace was
+    reserved, and replayed: the same cache bytes and outputs as the eager step."""
+    w = wl.continuous_batching(seed=77, num_seqs=48, num_steps=1, median=300, cap=4000, kv_dtype=kv, poison=True)
+    st = w.steps[0]
+    eager = DeviceWorkload(w)
+    ref = eager.run_step(0, out=torch.empty_like(eager.out)).clone()
+    torch.cuda.synchronize()
+    binding.reserve_workspace(binding.decode_workspace_bytes(w.num_seqs, st.query.shape[1], w.num_kv_heads,
+                                                             w.head_dim, w.block_size, w.max_blocks_per_seq))
+    dw = DeviceWorkload(w)
+    out = torch.empty_like(dw.out)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):                 # warm-up outside the capture
+        dw.run_step(0, out=out)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    out.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        dw.run_step(0, out=out)
+    for _ in range(3):                            # the step rewrites the same slots with the same bytes
+        graph.replay()
+    torch.cuda.synchronize()
+    assert binding.read_device_errors() == 0
+    assert torch.equal(out, ref)
+    assert torch.equal(raw(dw.key_cache), raw(eager.key_cache))
+    assert torch.equal(raw(dw.value_cache), raw(eager.value_cache))
