@@ -52,6 +52,9 @@ struct DeviceState {
   int num_sms = 0;
   void* ws = nullptr;           // decode workspace
   size_t ws_bytes = 0;
+  // Held from a workspace check to the end of the launch that uses the workspace, so
+  // a growth on one host thread cannot free a buffer another thread is queueing work on.
+  std::mutex ws_use;
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
@@ -75,9 +78,9 @@ pkv_status device_state(DeviceState** out) {
 }
 
 // Grow the current device's workspace to `bytes` (synchronises the device first so no
-// queued kernel still uses the old buffer; refused during stream capture).
+// queued kernel still uses the old buffer; refused during stream capture).  The caller
+// holds s->ws_use.
 pkv_status ensure_workspace(DeviceState* s, size_t bytes, cudaStream_t stream) {
-  std::lock_guard<std::mutex> lock(g_dev_mutex);
   if (bytes <= s->ws_bytes) return PKV_OK;
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   cudaError_t ce = cudaStreamIsCapturing(stream, &cs);
@@ -527,6 +530,7 @@ pkv_status pkv_reserve_workspace(int64_t bytes) {
   DeviceState* s;
   pkv_status st = device_state(&s);
   if (st) return st;
+  std::lock_guard<std::mutex> use(s->ws_use);
   return ensure_workspace(s, size_t(bytes), nullptr);
 }
 
@@ -576,7 +580,9 @@ pkv_status pkv_paged_attention_decode_window(const pkv_tensor* out, const pkv_te
   DeviceState* s;
   if ((st = device_state(&s))) return st;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  std::unique_lock<std::mutex> use(s->ws_use, std::defer_lock);
   if (ws_bytes) {
+    use.lock();
     if ((st = ensure_workspace(s, ws_bytes, cs))) return st;
     decode_set_workspace(&p, s->ws);
   }
@@ -709,7 +715,9 @@ pkv_status pkv_decode_step(const pkv_tensor* out, const pkv_tensor* query, const
   DeviceState* s;
   if ((st = device_state(&s))) return st;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (!no_decode && ws_bytes) {  // growth synchronises: before the write is queued
+  std::unique_lock<std::mutex> use(s->ws_use, std::defer_lock);
+  if (!no_decode && ws_bytes) {  // growth synchronises the device: before the write is queued
+    use.lock();
     if ((st = ensure_workspace(s, ws_bytes, cs))) return st;
     decode_set_workspace(&p, s->ws);
   }
@@ -744,7 +752,9 @@ pkv_status pkv_decode_append(const pkv_tensor* out, const pkv_tensor* query, con
   DeviceState* s;
   if ((st = device_state(&s))) return st;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  std::unique_lock<std::mutex> use(s->ws_use, std::defer_lock);
   if (!no_decode && ws_bytes) {
+    use.lock();
     if ((st = ensure_workspace(s, ws_bytes, cs))) return st;
     decode_set_workspace(&p, s->ws);
   }
