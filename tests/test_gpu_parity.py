@@ -843,3 +843,59 @@ def test_decode_step_replayed_from_a_cuda_graph(kv):
     assert torch.equal(out, ref)
     assert torch.equal(raw(dw.key_cache), raw(eager.key_cache))
     assert torch.equal(raw(dw.value_cache), raw(eager.value_cache))
+
+
+_THREADED_CHILD = r"""
+import sys, threading, torch
+from paged_kv_cache_90_gb300 import binding
+from paged_kv_cache_90_gb300.decode_step import DeviceWorkload
+from paged_kv_cache_90_gb300 import workloads as wl
+sys.path.insert(0, sys.argv[2])
+from test_gpu_parity import threaded_cases
+binding.load_library()
+stream = torch.cuda.Stream()
+outs, errors = {}, []
+def run(t):
+    try:
+        with torch.cuda.stream(stream):
+            for key, w in threaded_cases(t):
+                dw = DeviceWorkload(w)
+                out = dw.run_step(0, out=torch.empty_like(dw.out))
+                stream.synchronize()
+                outs[key] = out.cpu()
+    except Exception as e:            # reported by the parent
+        errors.append(repr(e))
+threads = [threading.Thread(target=run, args=(t,)) for t in range(4)]
+for th in threads: th.start()
+for th in threads: th.join()
+assert not errors, errors
+assert binding.read_device_errors() == 0
+torch.save(outs, sys.argv[1])
+"""
+
+
+def threaded_cases(t):
+    """Thread t's decodes, growing in size, so that the threads grow the (initially
+    empty) workspace while the others queue work."""
+    return [((t, j), wl.llama3_8b_decode(seed=600 + 10 * t + j, num_seqs=n, len_range=(1, 1200 + 400 * t)))
+            for j, n in enumerate((4, 24, 64))]
+
+
+def test_host_threads_share_one_workspace(tmp_path):
+    """Four host threads queue decodes of growing size on one stream in a fresh process
+    (so the workspace grows while other threads queue work): every output matches the
+    oracle and no device check fires."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    path = tmp_path / "outs.pt"
+    r = subprocess.run([sys.executable, "-c", _THREADED_CHILD, str(path), os.path.join(root, "tests")],
+                       cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+    outs = torch.load(path)
+    for t in range(4):
+        for key, w in threaded_cases(t):
+            kc, vc = w.key_cache.clone(), w.value_cache.clone()
+            ref = oracle.run_workload_step(w, 0, kc, vc, THREADS)
+            wabs = weighted_abs_values(w, w.steps[0], kc, vc)
+            assert_decode_close(outs[key].double(), ref, w, wabs)
