@@ -356,14 +356,7 @@ def run_prefill_gpu(args, world, rank, local, w, dw, dev, flush_l2, barrier):
     clocks.stop()
     pre_ms = sum(a.elapsed_time(c) for a, c in ev[:pre_steps]) / pre_steps
     flops = prefill_flops(w, w.steps[0])
-    my = torch.tensor([total_ms, float(flops * args.steps)], dtype=torch.float64)
-    if world > 1:
-        import torch.distributed as dist
-        t_ = my.to(dev)
-        dist.all_reduce(t_[:1], op=dist.ReduceOp.MAX)
-        dist.all_reduce(t_[1:], op=dist.ReduceOp.SUM)
-        my = t_.cpu()
-    max_ms, all_flops = float(my[0]), float(my[1])
+    (max_ms,), (all_flops,) = reduce_over_ranks(world, dev, [total_ms], [flops * args.steps])
     value = all_flops / (max_ms * 1e-3) / 1e12
     # end to end: step inputs from pinned host memory, output back
     fields = ("query", "new_key", "new_value", "slot_mapping", "block_tables", "context_lens", "cow_pairs",
@@ -383,7 +376,8 @@ def run_prefill_gpu(args, world, rank, local, w, dw, dev, flush_l2, barrier):
         c.synchronize()
         if k >= 3:
             e_ms += a.elapsed_time(c)
-    e2e = flops * e_steps / (e_ms * 1e-3) / 1e12
+    (e_ms,), (e2e_flops, launches) = reduce_over_ranks(world, dev, [e_ms], [flops * e_steps, launches])
+    e2e = e2e_flops / (e_ms * 1e-3) / 1e12
     if rank != 0:
         return 0
     try:
@@ -417,6 +411,21 @@ def run_prefill_gpu(args, world, rank, local, w, dw, dev, flush_l2, barrier):
 
 
 # ---- the two arms --------------------------------------------------------------------
+
+def reduce_over_ranks(world, dev, maxes, sums):
+    """Whole-job figures of a run on `world` ranks: the max over ranks of each entry of
+    `maxes` (times) and the sum of each entry of `sums` (work done, launches); every
+    rank calls it at the same point.  One rank: the values as given."""
+    maxes, sums = [float(x) for x in maxes], [float(x) for x in sums]
+    if world == 1:
+        return maxes, sums
+    import torch.distributed as dist
+    m = torch.tensor(maxes, dtype=torch.float64, device=dev)
+    t = torch.tensor(sums, dtype=torch.float64, device=dev)
+    dist.all_reduce(m, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return m.cpu().tolist(), t.cpu().tolist()
+
 
 def init_dist(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -595,17 +604,8 @@ def run_gpu(args, world, rank, local):
 
     bytes_steps = [step_bytes(w, w.steps[k % nsteps]) for k in range(args.steps)]
     dec_bytes = [float(statistics.mean(decode_bytes(w, w.steps[k % nsteps]) for k in range(dec_steps)))]
-    my_time = torch.tensor([total_ms], dtype=torch.float64)
-    my_bytes = torch.tensor([float(sum(bytes_steps))], dtype=torch.float64)
-    if world > 1:
-        import torch.distributed as dist
-        t_ = my_time.to(dev)
-        b_ = my_bytes.to(dev)
-        dist.all_reduce(t_, op=dist.ReduceOp.MAX)
-        dist.all_reduce(b_, op=dist.ReduceOp.SUM)
-        my_time, my_bytes = t_.cpu(), b_.cpu()
-    max_ms = float(my_time[0])
-    value = float(my_bytes[0]) / (max_ms * 1e-3) / 1e9
+    (max_ms,), (all_bytes,) = reduce_over_ranks(world, dev, [total_ms], [sum(bytes_steps)])
+    value = all_bytes / (max_ms * 1e-3) / 1e9
 
     # ---- end to end through the public API from pinned host buffers (e2e) ----
     fields = ("query", "new_key", "new_value", "slot_mapping", "block_tables", "context_lens", "cow_pairs")
@@ -635,6 +635,7 @@ def run_gpu(args, world, rank, local):
         c.synchronize()
         e_ms += a.elapsed_time(c)
     e2e_bytes = sum(step_bytes(w, w.steps[k % nsteps]) for k in range(e2e_steps))
+    (e_ms,), (e2e_bytes, launches) = reduce_over_ranks(world, dev, [e_ms], [e2e_bytes, launches])
     e2e_value = e2e_bytes / (e_ms * 1e-3) / 1e9
 
     if rank != 0:
