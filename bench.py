@@ -157,6 +157,13 @@ def profiled_traffic(workload: str):
     return int(m_tr.group(1))
 
 
+def smi_index(local: int) -> int:
+    """nvidia-smi's index of this rank's GPU: entry `local` of CUDA_VISIBLE_DEVICES when
+    that lists indices, else `local` itself."""
+    vis = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")]
+    return int(vis[local]) if local < len(vis) and vis[local].isdigit() else local
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling while the timed region runs."""
 
@@ -321,8 +328,7 @@ def run_prefill_gpu(args, world, rank, local, w, dw, dev, flush_l2, barrier):
         flush_l2()
         dw.run_step(0)
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
-                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local)
+    clocks = ClockSampler(smi_index(local))
     clocks.start()
     time.sleep(0.3)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -537,8 +543,7 @@ def run_gpu(args, world, rank, local):
         flush_l2()
         dw.run_step(i % nsteps, joint=joint)
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
-                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local)
+    clocks = ClockSampler(smi_index(local))
     clocks.start()
     time.sleep(0.3)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),

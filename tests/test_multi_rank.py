@@ -87,3 +87,13 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["steps"] == 2
     assert line["value"] > 0 and line["e2e"]["value"] == line["value"]
     assert line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_clock_sampling_follows_the_rank_gpu(monkeypatch):
+    b = _bench()
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "4,5,6,7")
+    assert [b.smi_index(r) for r in range(4)] == [4, 5, 6, 7]
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "GPU-aaaa,GPU-bbbb")
+    assert b.smi_index(1) == 1
+    monkeypatch.delenv("CUDA_VISIBLE_DEVICES")
+    assert b.smi_index(2) == 2
