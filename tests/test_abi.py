@@ -212,3 +212,105 @@ def test_options_and_workspace_size(lib):
     with pytest.raises(KeyError):
         binding.set_option("nope", 1)
     assert lib.pkv_set_option(99, 0) == 1
+
+
+def _raw_decode(lib, descs, num_kv_heads=2, scale=0.1, block_size=16, mb=4):
+    ptrs = [None if d is None else ctypes.byref(d) for d in descs]
+    return lib.pkv_paged_attention_decode(*ptrs, num_kv_heads, scale, block_size, mb, None)
+
+
+def test_descriptor_checks(dry):
+    """Malformed descriptors fail with INVALID_ARG (or UNSUPPORTED for a known but
+    unsupported dtype) and a message naming the argument, before anything is queued."""
+    lib = binding.load_library()
+    a = _decode_args()
+    names = ("out", "query", "key_cache", "value_cache", "block_tables", "context_lens")
+
+    def descs():
+        return [binding.describe(a[n]) for n in names]
+
+    assert _raw_decode(lib, descs()) == 0
+    for i, n in enumerate(names):
+        d = descs()
+        d[i] = None                                           # null descriptor
+        assert _raw_decode(lib, d) == 1 and n.encode() in lib.pkv_last_error()
+        d = descs()
+        d[i].data = None                                      # null data pointer
+        assert _raw_decode(lib, d) == 1 and n.encode() in lib.pkv_last_error()
+        d = descs()
+        d[i].dtype = 17                                       # unknown dtype code
+        assert _raw_decode(lib, d) == 1 and b"unknown dtype" in lib.pkv_last_error()
+        d = descs()
+        d[i].ndim = d[i].ndim + 1 if d[i].ndim < 4 else 3     # wrong rank
+        assert _raw_decode(lib, d) == 1
+        d = descs()
+        d[i].shape[0] = -1                                    # negative size
+        assert _raw_decode(lib, d) == 1
+    d = descs()
+    d[2].stride[2] = 256                                      # (bs, D) tile not contiguous
+    assert _raw_decode(lib, d) == 1 and b"tile" in lib.pkv_last_error()
+    d = descs()
+    d[1].stride[2] = 2                                        # query's last dim strided
+    assert _raw_decode(lib, d) == 1 and b"contiguous" in lib.pkv_last_error()
+    d = descs()
+    d[4].dtype = 4                                            # int64 block table: known, unsupported
+    assert _raw_decode(lib, d) == 2
+
+
+def test_window_prefill_and_noalloc_validation(dry):
+    a = _decode_args()
+    assert _status(binding.paged_attention_decode, **a, sliding_window=64) == 0
+    assert _status(binding.paged_attention_decode, **a, sliding_window=-1) == 1
+    assert _status(binding.paged_attention_decode_noalloc, **a) == 0
+    b = dict(a)
+    b["num_kv_heads"] = 3
+    assert _status(binding.paged_attention_decode_noalloc, **b) == 1
+    # prefill: 5 packed new tokens of 3 sequences
+    T = 5
+    q = torch.zeros(T, 8, 128, dtype=torch.bfloat16)
+    p = dict(out=torch.empty_like(q), query=q, key_cache=a["key_cache"], value_cache=a["value_cache"],
+             block_tables=a["block_tables"], context_lens=torch.full((3,), 8, dtype=torch.int32),
+             query_start_loc=torch.tensor([0, 2, 4, 5], dtype=torch.int32), num_kv_heads=2, scale=0.1,
+             block_size=16, max_blocks_per_seq=4)
+    # the prefill kernel needs the driver's tensor-map encoder: without a GPU driver a
+    # valid call passes every argument check and then reports UNSUPPORTED
+    assert _status(binding.paged_attention_prefill, **p) in ((0,) if torch.cuda.is_available() else (0, 2))
+    assert _status(binding.paged_attention_prefill, **dict(p, query_start_loc=torch.tensor([0, 2, 5], dtype=torch.int32))) == 1
+    f = torch.zeros(T, 8, 128, dtype=torch.float32)
+    assert _status(binding.paged_attention_prefill, **dict(p, query=f, out=torch.empty_like(f))) == 2
+
+
+def test_workspace_errors_and_empty_pool(dry):
+    lib = binding.load_library()
+    assert lib.pkv_reserve_workspace(ctypes.c_int64(-1)) == 1
+    assert lib.pkv_read_device_errors(None) == 1 and b"null" in lib.pkv_last_error()
+    a = _decode_args(NB=0)                                   # a pool of no blocks
+    assert _status(binding.paged_attention_decode, **a) == 1 and b"no block" in lib.pkv_last_error()
+
+
+def test_last_error_is_per_thread(dry):
+    """pkv_last_error() is the calling thread's message: another thread's failure does
+    not replace it."""
+    import threading
+    lib = binding.load_library()
+    a = _decode_args()
+    a["num_kv_heads"] = 3
+    with pytest.raises(binding.PkvError):
+        binding.paged_attention_decode(**a)
+    mine = lib.pkv_last_error()
+    assert b"num_kv_heads" in mine
+    theirs = []
+
+    def other():
+        b = _decode_args()
+        b["scale"] = float("nan")
+        try:
+            binding.paged_attention_decode(**b)
+        except binding.PkvError:
+            pass
+        theirs.append(lib.pkv_last_error())
+    t = threading.Thread(target=other)
+    t.start()
+    t.join()
+    assert b"scale" in theirs[0]
+    assert lib.pkv_last_error() == mine
