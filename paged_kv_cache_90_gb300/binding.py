@@ -118,6 +118,26 @@ def describe(t: torch.Tensor, scale: float = 1.0, head_scales: Optional[torch.Te
     return d
 
 
+# Descriptors the call wrappers pass, by everything a descriptor holds (address, dtype,
+# shape, strides, scale, per-head scales): a serving loop passes the same tensors every
+# step, and building a descriptor costs several microseconds of Python.  The cached
+# objects never leave this module, so nothing mutates them.
+_DESC_CACHE: dict = {}
+_DESC_CACHE_MAX = 4096
+
+
+def _ref(t: torch.Tensor, scale: float = 1.0, head_scales: Optional[torch.Tensor] = None):
+    hs = None if head_scales is None else (head_scales.data_ptr(), head_scales.dtype, head_scales.device,
+                                             head_scales.stride())
+    key = (t.data_ptr(), t.dtype, t.device, t.shape, t.stride(), float(scale), hs)
+    r = _DESC_CACHE.get(key)
+    if r is None:
+        if len(_DESC_CACHE) >= _DESC_CACHE_MAX:
+            _DESC_CACHE.clear()
+        r = _DESC_CACHE[key] = ctypes.byref(describe(t, scale, head_scales))
+    return r
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         if not torch.cuda.is_available():
@@ -138,15 +158,14 @@ def paged_attention_decode(out, query, key_cache, value_cache, block_tables, con
     (pkv_paged_attention_decode_window).  ``k_head_scales`` / ``v_head_scales``: one
     scale per KV head of an 8-bit cache (device float32), instead of k_scale / v_scale."""
     lib = load_library()
-    descs = [describe(out), describe(query), describe(key_cache, k_scale, k_head_scales),
-             describe(value_cache, v_scale, v_head_scales), describe(block_tables), describe(context_lens)]
-    args = [ctypes.byref(x) for x in descs]
+    descs = [_ref(out), _ref(query), _ref(key_cache, k_scale, k_head_scales),
+             _ref(value_cache, v_scale, v_head_scales), _ref(block_tables), _ref(context_lens)]
     if sliding_window:
-        _check(lib.pkv_paged_attention_decode_window(*args, int(num_kv_heads), float(scale), int(block_size),
+        _check(lib.pkv_paged_attention_decode_window(*descs, int(num_kv_heads), float(scale), int(block_size),
                                                      int(max_blocks_per_seq), int(sliding_window),
                                                      _stream(stream)))
     else:
-        _check(lib.pkv_paged_attention_decode(*args, int(num_kv_heads), float(scale), int(block_size),
+        _check(lib.pkv_paged_attention_decode(*descs, int(num_kv_heads), float(scale), int(block_size),
                                               int(max_blocks_per_seq), _stream(stream)))
     return out
 
@@ -159,10 +178,10 @@ def decode_step(out, query, key, value, slot_mapping, key_cache, value_cache, bl
     and decode into ``out`` (returned): the results of reshape_and_cache followed by
     paged_attention_decode, with the decode's preparation overlapping the write."""
     lib = load_library()
-    descs = [describe(out), describe(query), describe(key), describe(value), describe(slot_mapping),
-             describe(key_cache, k_scale, k_head_scales), describe(value_cache, v_scale, v_head_scales),
-             describe(block_tables), describe(context_lens)]
-    _check(lib.pkv_decode_step(*[ctypes.byref(x) for x in descs], int(num_kv_heads), float(scale),
+    descs = [_ref(out), _ref(query), _ref(key), _ref(value), _ref(slot_mapping),
+             _ref(key_cache, k_scale, k_head_scales), _ref(value_cache, v_scale, v_head_scales),
+             _ref(block_tables), _ref(context_lens)]
+    _check(lib.pkv_decode_step(*descs, int(num_kv_heads), float(scale),
                                int(block_size), int(max_blocks_per_seq), int(sliding_window), _stream(stream)))
     return out
 
@@ -176,10 +195,10 @@ def decode_append(out, query, key, value, slot_mapping, key_cache, value_cache, 
     ``fused_append`` option at 2 the write runs inside the decode kernel.  Returns
     ``out``."""
     lib = load_library()
-    descs = [describe(out), describe(query), describe(key), describe(value), describe(slot_mapping),
-             describe(key_cache, k_scale, k_head_scales), describe(value_cache, v_scale, v_head_scales),
-             describe(block_tables), describe(context_lens)]
-    _check(lib.pkv_decode_append(*[ctypes.byref(x) for x in descs], int(num_kv_heads), float(scale),
+    descs = [_ref(out), _ref(query), _ref(key), _ref(value), _ref(slot_mapping),
+             _ref(key_cache, k_scale, k_head_scales), _ref(value_cache, v_scale, v_head_scales),
+             _ref(block_tables), _ref(context_lens)]
+    _check(lib.pkv_decode_append(*descs, int(num_kv_heads), float(scale),
                                  int(block_size), int(max_blocks_per_seq), int(sliding_window), _stream(stream)))
     return out
 
@@ -191,9 +210,9 @@ def paged_attention_prefill(out, query, key_cache, value_cache, block_tables, co
     query_start_loc[s] .. query_start_loc[s+1]-1, the last of its context_lens[s]
     cached positions) over the paged cache, into ``out`` (returned)."""
     lib = load_library()
-    descs = [describe(out), describe(query), describe(key_cache), describe(value_cache), describe(block_tables),
-             describe(context_lens), describe(query_start_loc)]
-    _check(lib.pkv_paged_attention_prefill(*[ctypes.byref(x) for x in descs], int(num_kv_heads), float(scale),
+    descs = [_ref(out), _ref(query), _ref(key_cache), _ref(value_cache), _ref(block_tables),
+             _ref(context_lens), _ref(query_start_loc)]
+    _check(lib.pkv_paged_attention_prefill(*descs, int(num_kv_heads), float(scale),
                                            int(block_size), int(max_blocks_per_seq), _stream(stream)))
     return out
 
@@ -208,9 +227,9 @@ def paged_attention_decode_noalloc(out, query, key_cache, value_cache, block_tab
     an allocation synchronise the device).  Calls on one device share that scratch,
     so calls on unordered streams must not overlap."""
     lib = load_library()
-    descs = [describe(out), describe(query), describe(key_cache, k_scale),
-             describe(value_cache, v_scale), describe(block_tables), describe(context_lens)]
-    _check(lib.pkv_paged_attention_decode_noalloc(*[ctypes.byref(x) for x in descs],
+    descs = [_ref(out), _ref(query), _ref(key_cache, k_scale),
+             _ref(value_cache, v_scale), _ref(block_tables), _ref(context_lens)]
+    _check(lib.pkv_paged_attention_decode_noalloc(*descs,
                                                   int(num_kv_heads), float(scale), int(block_size),
                                                   int(max_blocks_per_seq), _stream(stream)))
     return out
@@ -227,16 +246,15 @@ def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, k_scale:
     ``v_amax`` (device float32 [Hk], starting >= 0) are raised to the largest |x|
     written per KV head (pkv_reshape_and_cache_amax)."""
     lib = load_library()
-    descs = [describe(key), describe(value), describe(key_cache, k_scale, k_head_scales),
-             describe(value_cache, v_scale, v_head_scales), describe(slot_mapping)]
-    args = [ctypes.byref(x) for x in descs]
+    descs = [_ref(key), _ref(value), _ref(key_cache, k_scale, k_head_scales),
+             _ref(value_cache, v_scale, v_head_scales), _ref(slot_mapping)]
     if k_amax is None and v_amax is None:
-        _check(lib.pkv_reshape_and_cache(*args, _stream(stream)))
+        _check(lib.pkv_reshape_and_cache(*descs, _stream(stream)))
         return
     for a in (k_amax, v_amax):
         if a is not None and (a.dtype != torch.float32 or not a.is_contiguous() or a.device != key_cache.device):
             raise ValueError("amax arrays must be contiguous float32 tensors on the cache's device")
-    _check(lib.pkv_reshape_and_cache_amax(*args, None if k_amax is None else ctypes.c_void_p(k_amax.data_ptr()),
+    _check(lib.pkv_reshape_and_cache_amax(*descs, None if k_amax is None else ctypes.c_void_p(k_amax.data_ptr()),
                                           None if v_amax is None else ctypes.c_void_p(v_amax.data_ptr()),
                                           _stream(stream)))
 
@@ -247,8 +265,8 @@ def copy_blocks(cache, src_dst_pairs, stream=None) -> None:
     pairs = src_dst_pairs
     if pairs.numel() == 0:
         pairs = pairs.reshape(0, 2)
-    descs = [describe(cache), describe(pairs)]
-    _check(lib.pkv_copy_blocks(*[ctypes.byref(x) for x in descs], _stream(stream)))
+    descs = [_ref(cache), _ref(pairs)]
+    _check(lib.pkv_copy_blocks(*descs, _stream(stream)))
 
 
 def set_option(name: str, value: int) -> None:

@@ -314,3 +314,25 @@ def test_last_error_is_per_thread(dry):
     t.join()
     assert b"scale" in theirs[0]
     assert lib.pkv_last_error() == mine
+
+
+def test_call_descriptors_are_cached_by_content(lib):
+    """The wrappers' descriptor cache hands out a descriptor equal to a fresh one, keyed
+    by everything a descriptor holds: another view, dtype, scale or per-head scale array
+    gets its own; empty tensors carry no pointer; the cache stays bounded."""
+    def fields(d):
+        return (d.data, d.dtype, d.ndim, tuple(d.shape), tuple(d.stride), d.scale, d.head_scales)
+
+    binding._DESC_CACHE.clear()
+    c = torch.zeros(6, 2, 16, 64, dtype=torch.bfloat16)
+    hs = torch.ones(2, dtype=torch.float32)
+    for t, sc, h in ((c, 1.0, None), (c[1:], 1.0, None), (c.view(torch.float8_e4m3fn)[:, :1], 1.0, None),
+                     (c, 0.5, None), (c.view(torch.float8_e4m3fn)[..., :64], 0.5, hs), (c[:0], 1.0, None)):
+        r = binding._ref(t, sc, h)
+        assert binding._ref(t, sc, h) is r                         # a hit
+        assert fields(r._obj) == fields(binding.describe(t, sc, h))
+    assert len(binding._DESC_CACHE) == 6
+    assert binding._ref(c[:0])._obj.data is None
+    for i in range(binding._DESC_CACHE_MAX + 10):
+        binding._ref(c, float(i))
+    assert len(binding._DESC_CACHE) <= binding._DESC_CACHE_MAX
