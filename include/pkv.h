@@ -40,6 +40,8 @@
  * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream) of the
  *   current device.  Every call is asynchronous and stream-ordered; nothing
  *   synchronises unless the debug-sync option is on.
+ * Empty work.  A call with nothing to compute (no sequence, token, copy pair, query
+ *   head or KV head) checks its arguments and returns PKV_OK without queueing work.
  * Errors.  No call throws or aborts.  Argument problems found on the host return
  *   PKV_ERR_INVALID_ARG or PKV_ERR_UNSUPPORTED before anything is queued; CUDA
  *   launch/runtime failures return PKV_ERR_CUDA.  pkv_last_error() gives the calling

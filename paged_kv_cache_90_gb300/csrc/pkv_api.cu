@@ -278,7 +278,7 @@ pkv_status decode_prepare(const pkv_tensor* out, const pkv_tensor* query, const 
   const int pt = choose_partition_tokens(max_ctx);
   const int64_t parts = (max_ctx + pt - 1) / pt;
   if (parts > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many context partitions; raise the partition size");
-  if (g_opt_dry_run.load() || S == 0) {
+  if (g_opt_dry_run.load() || S == 0 || Hq == 0) {  // no query head: the output has no element
     *nothing_to_do = true;
     return PKV_OK;
   }
@@ -384,7 +384,7 @@ pkv_status reshape_prepare(const pkv_tensor* key, const pkv_tensor* value, const
   if (!aligned16(key->data) || !aligned16(value->data) || (key->stride[0] * eb) % 16 || (key->stride[1] * eb) % 16)
     return fail(PKV_ERR_INVALID_ARG, "key/value base pointers and strides must be multiples of 16 bytes");
   if (T > 0x7fffffff) return fail(PKV_ERR_UNSUPPORTED, "too many tokens in one call");
-  if (g_opt_dry_run.load() || T == 0) {
+  if (g_opt_dry_run.load() || T == 0 || Hk == 0) {  // no KV head: nothing is written
     *nothing_to_do = true;
     return PKV_OK;
   }
@@ -657,7 +657,7 @@ pkv_status pkv_paged_attention_prefill(const pkv_tensor* out, const pkv_tensor* 
     return fail(PKV_ERR_UNSUPPORTED, "prefill needs bf16 queries, outputs and caches, head_dim 64/128, block size "
                 "8/16/32, at most %d table entries per sequence, 16-byte aligned query/out rows",
                 kPrefillMaxTableEntries);
-  if (g_opt_dry_run.load() || S == 0 || T == 0) return PKV_OK;
+  if (g_opt_dry_run.load() || S == 0 || T == 0 || Hq == 0) return PKV_OK;
   DeviceState* ds;
   if ((st = device_state(&ds))) return st;
   p.err = ds->err;
@@ -797,7 +797,7 @@ pkv_status pkv_copy_blocks(const pkv_tensor* cache, const pkv_tensor* src_dst_pa
     return fail(PKV_ERR_UNSUPPORTED, "block_size %lld (supported: 2, 4, 8, 16, 32)", (long long)cache->shape[2]);
   const int64_t n = src_dst_pairs->shape[0];
   if (n > 0x7fffffff || cache->shape[1] > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many pairs or heads");
-  if (g_opt_dry_run.load() || n == 0) return PKV_OK;
+  if (g_opt_dry_run.load() || n == 0 || cache->shape[1] == 0) return PKV_OK;  // (no KV head: no byte to copy)
 
   DeviceState* s;
   if ((st = device_state(&s))) return st;

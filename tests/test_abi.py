@@ -336,3 +336,25 @@ def test_call_descriptors_are_cached_by_content(lib):
     for i in range(binding._DESC_CACHE_MAX + 10):
         binding._ref(c, float(i))
     assert len(binding._DESC_CACHE) <= binding._DESC_CACHE_MAX
+
+
+def test_zero_heads_queue_nothing(lib):
+    """A batch with no query head (decode, prefill) or a pool with no KV head (write,
+    copy) has nothing to compute: the call returns OK before it touches a device (so it
+    succeeds here, where there is none), rather than launching kernels whose tile
+    counts would be zero."""
+    binding.set_option("dry_run", 0)
+    a = _decode_args(Hq=0)
+    assert _status(binding.paged_attention_decode, **a) == 0
+    assert _status(binding.paged_attention_decode, **a, sliding_window=16) == 0
+    q = torch.zeros(5, 0, 128, dtype=torch.bfloat16)
+    assert _status(binding.paged_attention_prefill, out=torch.empty_like(q), query=q, key_cache=a["key_cache"],
+                   value_cache=a["value_cache"], block_tables=a["block_tables"],
+                   context_lens=torch.full((3,), 8, dtype=torch.int32),
+                   query_start_loc=torch.tensor([0, 2, 4, 5], dtype=torch.int32), num_kv_heads=2, scale=0.1,
+                   block_size=16, max_blocks_per_seq=4) in ((0,) if torch.cuda.is_available() else (0, 2))
+    c0 = torch.zeros(10, 0, 16, 128, dtype=torch.bfloat16)
+    k0 = torch.zeros(4, 0, 128, dtype=torch.bfloat16)
+    assert _status(binding.reshape_and_cache, key=k0, value=k0, key_cache=c0, value_cache=c0,
+                   slot_mapping=torch.arange(4, dtype=torch.int64)) == 0
+    assert _status(binding.copy_blocks, cache=c0, src_dst_pairs=torch.tensor([[0, 1]], dtype=torch.int64)) == 0
