@@ -693,7 +693,10 @@ def main():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
-    ap.add_argument("--workload", default="llama3_8b_decode")
+    ap.add_argument("--workload", default="llama3_8b_decode",
+                    help="llama3_8b_decode, long_context[_bs32], shared_prefix_cow, "
+                         "continuous_batching_bs{8,16,32}_{bf16,e4m3}[_headscales], sliding_window[_bs32], "
+                         "chunked_prefill, prefill_<N>x<T>, tiny")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle CPU time")
     ap.add_argument("--decode-kernel", choices=["auto", "tensor", "core"], default="auto",
