@@ -52,6 +52,24 @@ MUTANTS = [
     ("prefill: every row uses the last query", "const int64_t qoff = ((q0 + i) * num_heads + h) * head_dim;",
      "const int64_t qoff = ((q0 + n - 1) * num_heads + h) * head_dim;", 0),
     ("prefill: score scale dropped", "\n          z[j] = scale * acc;", "\n          z[j] = acc;", 0),
+    ("prefill: no causal mask", "int64_t pos = L - n + i;", "int64_t pos = L - 1;", 0),
+    ("prefill: keys scaled by the value scale", "orc_load(key_cache, base + d, kv_dtype) * k_scale;",
+     "orc_load(key_cache, base + d, kv_dtype) * v_scale;", 0),
+    # more decode, format and write mistakes
+    ("decode: keys scaled by the value scale", "orc_load(key_cache, base + d, kv_dtype) * ks;",
+     "orc_load(key_cache, base + d, kv_dtype) * vs;", 0),
+    ("decode: every KV head takes head 0's scale", "k_head_scales ? (double)k_head_scales[k]",
+     "k_head_scales ? (double)k_head_scales[0]", 0),
+    ("decode: window start ignored", "(sliding_window > 0 && Lctx > sliding_window) ? Lctx - sliding_window : 0",
+     "0", 0),
+    ("e4m3: sign dropped on decode", "return sign ? -mag : mag;", "return mag;", 0),
+    ("e4m3: NaN encoded as zero", "if (isnan(y)) return 0x7F;", "if (isnan(y)) return 0x00;", 0),
+    ("bf16: bits taken as the low half", "(uint32_t)bits << 16", "(uint32_t)bits", 0),
+    ("write: value codes stored in the key cache",
+     "((uint8_t*)value_cache)[dst + d] = orc_f32_to_e4m3(yv);", "((uint8_t*)key_cache)[dst + d] = orc_f32_to_e4m3(yv);", 0),
+    ("write: amax forgets a NaN", "if (k_amax && (isnan(ak) || ak > k_amax[h])) k_amax[h] = ak;",
+     "if (k_amax && (ak > k_amax[h])) k_amax[h] = ak;", 0),
+    ("copy: half of each block", "(size_t)block_bytes);", "(size_t)block_bytes / 2);", 0),
 ]
 
 

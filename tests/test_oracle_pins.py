@@ -608,6 +608,34 @@ def test_prefill_equals_causal_sdpa(bs):
         assert torch.allclose(out[qsl[s]:qsl[s + 1]], ref[0].permute(1, 0, 2), rtol=0, atol=1e-12), s
 
 
+def test_prefill_over_an_8bit_cache_equals_causal_sdpa():
+    """An e4m3 cache with separate K and V scales: the oracle's prefill equals torch's
+    causal scaled_dot_product_attention in float64 over the cache decoded by torch's
+    own float8 conversion and scaled (K by its scale, V by its)."""
+    w = _prefill_small(seed=87, prefix=(0, 6, 21), chunk=(5, 12, 3), bs=8, kv="e4m3")
+    assert w.k_scale != w.v_scale
+    kc, vc = _materialize(w)
+    st = w.steps[0]
+    out = oracle.paged_attention_prefill(st.query, kc, vc, st.block_tables, st.context_lens, st.query_start_loc,
+                                         w.scale, w.k_scale, w.v_scale)
+    bs = w.block_size
+
+    def gather8(cache, table, L):      # [Hk, L, D] values; torch cannot index fp8 on the CPU
+        n = -(-L // bs)
+        blocks = cache.view(torch.uint8)[table[:n].long()].view(torch.float8_e4m3fn).double()
+        return blocks.permute(1, 0, 2, 3).reshape(blocks.shape[1], n * bs, -1)[:, :L]
+
+    qsl = st.query_start_loc.tolist()
+    for s, L in enumerate(st.context_lens.tolist()):
+        n = qsl[s + 1] - qsl[s]
+        ks = (gather8(kc, st.block_tables[s], L) * w.k_scale).repeat_interleave(2, dim=0)[None]
+        vs = (gather8(vc, st.block_tables[s], L) * w.v_scale).repeat_interleave(2, dim=0)[None]
+        qs = st.query[qsl[s]:qsl[s + 1]].double().permute(1, 0, 2)[None]
+        mask = torch.arange(L)[None, :] <= (L - n + torch.arange(n))[:, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(qs, ks, vs, attn_mask=mask, scale=w.scale)
+        assert torch.allclose(out[qsl[s]:qsl[s + 1]], ref[0].permute(1, 0, 2), rtol=0, atol=1e-12), s
+
+
 def test_prefill_of_one_token_is_decode():
     """A chunk of one token per sequence is exactly the decode step."""
     w = _prefill_small(seed=84, prefix=(3, 16, 40), chunk=(1, 1, 1))
