@@ -70,6 +70,13 @@ MUTANTS = [
     ("write: amax forgets a NaN", "if (k_amax && (isnan(ak) || ak > k_amax[h])) k_amax[h] = ak;",
      "if (k_amax && (ak > k_amax[h])) k_amax[h] = ak;", 0),
     ("copy: half of each block", "(size_t)block_bytes);", "(size_t)block_bytes / 2);", 0),
+    ("decode: every head uses its group's first query", "const int64_t qoff = (s * num_heads + h) * head_dim;",
+     "const int64_t qoff = (s * num_heads + k * group) * head_dim;", 0),
+    ("decode: every sequence reads sequence 0's table", "block_tables[s * max_blocks_per_seq + j / block_size]",
+     "block_tables[0 * max_blocks_per_seq + j / block_size]", 0),
+    ("e4m3: encoder truncates", "lo = lo + 1;", ";", 0),
+    ("write: value amax read from the keys", "av = fabs(orc_load(value, src + d, src_dtype))",
+     "av = fabs(orc_load(key, src + d, src_dtype))", 0),
 ]
 
 
