@@ -86,6 +86,8 @@ typedef enum pkv_status {
 #define PKV_DEVERR_COPY_PAIR 0x4u    /* copy pair outside [0, num_blocks) */
 #define PKV_DEVERR_CONTEXT_LEN 0x8u  /* context_len < 0 or > max_blocks_per_seq * block_size */
 #define PKV_DEVERR_TIMEOUT 0x10u     /* a bounded wait for an async copy ran out */
+#define PKV_DEVERR_COPY_OVERLAP 0x20u /* copy pairs: a destination repeated or also a source
+                                        (checked only with PKV_OPT_DEBUG_SYNC on) */
 
 typedef struct pkv_tensor {
   void* data;         /* device pointer */
@@ -326,8 +328,12 @@ pkv_status pkv_reshape_and_cache_amax(const pkv_tensor* key, const pkv_tensor* v
  * cache          [num_blocks, num_kv_heads, block_size, head_dim], layout rules above.
  * src_dst_pairs  [num_pairs, 2] int64, contiguous; num_pairs may be 0.
  * Pairs are copied in parallel: destinations must be distinct and no destination may
- * also be a source (the host side cannot check device-resident pairs; breaking this
- * gives an unspecified mix of old and new bytes, never an out-of-bounds access).
+ * also be a source (breaking this gives an unspecified mix of old and new bytes, never
+ * an out-of-bounds access).  The pairs live on the device, so the host cannot check
+ * this; with PKV_OPT_DEBUG_SYNC on, a device kernel compares every pair with every other
+ * before the copy (O(num_pairs^2)) and a clash sets PKV_DEVERR_COPY_OVERLAP, which the
+ * call then reports as PKV_ERR_DEVICE_CHECK.  Pairs outside [0, num_blocks) set
+ * PKV_DEVERR_COPY_PAIR and are skipped.
  */
 pkv_status pkv_copy_blocks(const pkv_tensor* cache, const pkv_tensor* src_dst_pairs,
                            pkv_stream stream);
@@ -351,8 +357,10 @@ pkv_status pkv_copy_blocks(const pkv_tensor* cache, const pkv_tensor* src_dst_pa
  * message and queues nothing.
  * The first call on each device looks up the array's device address (and may load the
  * library's device code there): make it before any stream capture.  All calls on a
- * device share the array, so calls whose GPU work overlaps (unordered streams) race on
- * it; calls ordered on one stream are safe.
+ * device share the array.  Each call clears the array's counter header on its stream
+ * before its kernels run (a memset node, no allocation), so a call does not depend on
+ * how an earlier one ended; but calls whose GPU work overlaps (unordered streams) race
+ * on the array and may return wrong results.  Calls ordered on one stream are safe.
  */
 pkv_status pkv_paged_attention_decode_noalloc(const pkv_tensor* out, const pkv_tensor* query,
                                               const pkv_tensor* key_cache,

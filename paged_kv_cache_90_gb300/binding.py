@@ -21,7 +21,8 @@ LIB_PATH = os.path.join(_HERE, "_build", "libpkv.so")
 PKV_OK = 0
 STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA",
                 4: "PKV_ERR_DEVICE_CHECK"}
-DEVERR = {"table_entry": 0x1, "slot": 0x2, "copy_pair": 0x4, "context_len": 0x8, "timeout": 0x10}
+DEVERR = {"table_entry": 0x1, "slot": 0x2, "copy_pair": 0x4, "context_len": 0x8, "timeout": 0x10,
+          "copy_overlap": 0x20}
 OPTIONS = {"partition_tokens": 0, "debug_sync": 1, "dry_run": 2, "decode_kernel": 3,
            "dynamic_share": 4, "dynamic_chunk": 5, "fused_append": 6}
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float8_e4m3fn: 2, torch.int32: 3, torch.int64: 4}

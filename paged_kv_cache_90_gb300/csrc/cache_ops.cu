@@ -161,6 +161,30 @@ __global__ void __launch_bounds__(kCopyThreads) copy_blocks_kernel(const CopyBlo
   for (int64_t i = threadIdx.x; i < nvec; i += kCopyThreads) d[i] = s[i];
 }
 
+// Precondition of a parallel copy: destinations distinct and never a source.  Thread i
+// compares pair i's destination with every pair's source and with the destinations of
+// the pairs after it (pairs staged through shared memory a tile at a time); a clash sets
+// the overlap bit.  Out-of-range entries are left to the copy kernel's own check.
+constexpr int kCheckThreads = 256;
+__global__ void __launch_bounds__(kCheckThreads) copy_pairs_check_kernel(const CopyBlocksParams p) {
+  __shared__ int64_t src_tile[kCheckThreads], dst_tile[kCheckThreads];
+  const int64_t i = int64_t(blockIdx.x) * kCheckThreads + threadIdx.x;
+  const int64_t my_dst = i < p.num_pairs ? p.pairs[2 * i + 1] : -1;
+  bool clash = false;
+  for (int64_t base = 0; base < p.num_pairs; base += kCheckThreads) {
+    const int64_t j = base + threadIdx.x;
+    src_tile[threadIdx.x] = j < p.num_pairs ? p.pairs[2 * j] : -1;
+    dst_tile[threadIdx.x] = j < p.num_pairs ? p.pairs[2 * j + 1] : -1;
+    __syncthreads();
+    const int n = int(min(int64_t(kCheckThreads), p.num_pairs - base));
+    if (i < p.num_pairs)
+      for (int k = 0; k < n; ++k)
+        clash |= src_tile[k] == my_dst || (base + k > i && dst_tile[k] == my_dst);
+    __syncthreads();
+  }
+  if (clash) raise_device_error(p.err, kErrCopyOverlap);
+}
+
 }  // namespace
 
 cudaError_t launch_reshape_and_cache(const CacheWriteParams& p, cudaStream_t stream) {
@@ -180,6 +204,11 @@ cudaError_t launch_reshape_and_cache(const CacheWriteParams& p, cudaStream_t str
 
 cudaError_t launch_copy_blocks(const CopyBlocksParams& p, cudaStream_t stream) {
   if (p.num_pairs == 0) return cudaSuccess;
+  if (p.check_overlap) {
+    copy_pairs_check_kernel<<<unsigned((p.num_pairs + kCheckThreads - 1) / kCheckThreads), kCheckThreads, 0,
+                              stream>>>(p);
+    note_launch();
+  }
   const dim3 grid(static_cast<unsigned>(p.num_pairs), static_cast<unsigned>(p.num_kv_heads));
   copy_blocks_kernel<<<grid, kCopyThreads, 0, stream>>>(p);
   note_launch();

@@ -17,9 +17,12 @@
 // module there: make that first call before any stream capture.
 //
 // Every call on a device shares the one array and leaves its contents behind.  The
-// kernels write every partial result before reading it, so nothing has to be cleared
-// between calls; but two calls whose work overlaps on the GPU (different streams with
-// no ordering between them) race on the array and may return wrong results.
+// kernels write every partial result before reading it; the array's header holds the
+// counters through which the tensor-core kernel's warps claim work, and each call clears
+// it on its own stream (cudaMemsetAsync, which allocates nothing) before its launch, so
+// a call never depends on how an earlier one ended.  Two calls whose work overlaps on
+// the GPU (different streams with no ordering between them) still race on the array
+// and may return wrong results; calls ordered on one stream do not.
 #include <cstdio>
 #include <mutex>
 
@@ -80,12 +83,16 @@ extern "C" pkv_status pkv_paged_attention_decode_noalloc(
              ws_bytes, kStaticScratchBytes);
     return set_error(PKV_ERR_INVALID_ARG, msg);
   }
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (ws_bytes) {
     void* scratch = nullptr;
     if ((st = static_scratch(&scratch))) return st;
     decode_set_workspace(&p, scratch);
+    // the claim counters start at zero whatever an earlier (possibly overlapping or
+    // aborted) call left behind
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, kWorkspaceHeader, cs);
+    if (e != cudaSuccess) return finish_launch(e, cs, "paged_attention_decode_noalloc (clearing the counters)");
   }
-  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   return finish_launch(launch_decode(p, cs), cs, "paged_attention_decode_noalloc");
 }
 

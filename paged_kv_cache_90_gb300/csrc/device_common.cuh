@@ -21,6 +21,7 @@ constexpr unsigned int kErrSlot = 0x2u;
 constexpr unsigned int kErrCopyPair = 0x4u;
 constexpr unsigned int kErrContextLen = 0x8u;
 constexpr unsigned int kErrTimeout = 0x10u;
+constexpr unsigned int kErrCopyOverlap = 0x20u;
 
 // First attended position of a context of L tokens under a sliding window of W
 // positions (W <= 0: no window).

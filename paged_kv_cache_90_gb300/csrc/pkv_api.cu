@@ -812,6 +812,7 @@ pkv_status pkv_copy_blocks(const pkv_tensor* cache, const pkv_tensor* src_dst_pa
   p.num_pairs = n;
   p.num_blocks = cache->shape[0];
   p.err = s->err;
+  p.check_overlap = g_opt_debug_sync.load() != 0;  // O(pairs^2) device check, debug only
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   return finish_call(s, launch_copy_blocks(p, cs), cs, "copy_blocks");
 }

@@ -53,6 +53,7 @@ struct CopyBlocksParams {
   int64_t num_pairs;
   int64_t num_blocks;
   unsigned int* err;
+  bool check_overlap;        // first check that destinations are distinct and no source
 };
 cudaError_t launch_copy_blocks(const CopyBlocksParams& p, cudaStream_t stream);
 

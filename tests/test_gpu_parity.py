@@ -582,6 +582,43 @@ def test_device_checks_flag_bad_indices():
     assert binding.read_device_errors() == 0
 
 
+def test_copy_blocks_overlap_check_under_debug_sync():
+    """With debug sync on, copy pairs that break the parallel copy's precondition (a
+    destination named twice, or a destination that is also a source) are reported as a
+    device-check failure with the overlap bit; valid pairs still copy bit for bit, and
+    with debug sync off no check runs."""
+    g = torch.Generator().manual_seed(81)
+    cache = torch.randn(24, 4, 16, 64, generator=g).to(torch.bfloat16)
+    d = cache.cuda()
+    assert binding.read_device_errors() == 0
+    binding.set_option("debug_sync", 1)
+    try:
+        for bad in ([[1, 5], [2, 5]], [[1, 2], [2, 3]], [[3, 3]], [[0, 9], [4, 10], [9, 11]]):
+            with pytest.raises(binding.PkvError) as ei:
+                binding.copy_blocks(d, torch.tensor(bad, dtype=torch.int64, device="cuda"))
+            assert ei.value.status == 4 and "0x20" in ei.value.message, ei.value.message
+        assert binding.read_device_errors() == 0          # the failing call cleared the word
+        good = torch.tensor([[1, 12], [2, 13], [1, 14], [23, 0]], dtype=torch.int64)
+        d = cache.cuda()
+        binding.copy_blocks(d, good.cuda())
+        ref = cache.clone()
+        oracle.copy_blocks(ref, good)
+        assert torch.equal(raw(d.cpu()), raw(ref))
+        # many pairs, several tiles of the check, one clash at the far end
+        n = 700
+        many = torch.stack([torch.arange(n), torch.arange(n) + n], 1).to(torch.int64)
+        big = torch.zeros(2 * n + 1, 1, 16, 64, dtype=torch.bfloat16, device="cuda")
+        binding.copy_blocks(big, many.cuda())
+        many[n - 1, 1] = 0                                  # destination 0 is pair 0's source
+        with pytest.raises(binding.PkvError) as ei:
+            binding.copy_blocks(big, many.cuda())
+        assert "0x20" in ei.value.message
+    finally:
+        binding.set_option("debug_sync", 0)
+    binding.copy_blocks(d, torch.tensor([[1, 5], [2, 5]], dtype=torch.int64, device="cuda"))
+    assert binding.read_device_errors() == 0              # not checked without debug sync
+
+
 def test_launch_count_and_determinism(kernel):
     w = wl.llama3_8b_decode(seed=99, num_seqs=4, len_range=(600, 1500))
     dw = DeviceWorkload(w)
