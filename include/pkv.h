@@ -401,6 +401,10 @@ int32_t pkv_abi_version(void);
  * 1: on GB300 the small write kernel runs while the decode kernel prepares, whereas the
  * in-kernel write lengthens the warps that hold sequence ends.  The cache bytes and
  * outputs are the same either way.
+ * PKV_OPT_PREFILL_KERNEL (pkv_paged_attention_prefill): 0 = automatic (the tcgen05
+ * kernel, with its accumulators in tensor memory, whenever it supports the call), 1 =
+ * the mma.sync kernel, 2 = the tcgen05 kernel (PKV_ERR_UNSUPPORTED where it does not
+ * support the call).  Both compute the same attention; rounding orders differ.
  * pkv_set_option returns PKV_ERR_INVALID_ARG for an unknown option or a bad value.
  */
 typedef enum pkv_option {
@@ -410,7 +414,8 @@ typedef enum pkv_option {
   PKV_OPT_DECODE_KERNEL = 3,
   PKV_OPT_DYNAMIC_SHARE = 4,
   PKV_OPT_DYNAMIC_CHUNK = 5,
-  PKV_OPT_FUSED_APPEND = 6
+  PKV_OPT_FUSED_APPEND = 6,
+  PKV_OPT_PREFILL_KERNEL = 7
 } pkv_option;
 
 pkv_status pkv_set_option(int32_t option, int64_t value);

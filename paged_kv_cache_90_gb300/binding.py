@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
 DEVERR = {"table_entry": 0x1, "slot": 0x2, "copy_pair": 0x4, "context_len": 0x8, "timeout": 0x10,
           "copy_overlap": 0x20}
 OPTIONS = {"partition_tokens": 0, "debug_sync": 1, "dry_run": 2, "decode_kernel": 3,
-           "dynamic_share": 4, "dynamic_chunk": 5, "fused_append": 6}
+           "dynamic_share": 4, "dynamic_chunk": 5, "fused_append": 6,
+           "prefill_kernel": 7}
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1, torch.float8_e4m3fn: 2, torch.int32: 3, torch.int64: 4}
 
 

@@ -113,7 +113,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_split_rows_kernel(const D
     __syncthreads();
   }
   const int T = cum[S];
-  const mma::WorkSplit split(T / mma::kST, p.grid * kMmaWarps, p.dyn_share, p.dyn_chunk, p.dyn_units_max);
+  const mma::WorkSplit split(T / mma::kST, p.grid * p.block_warps, p.dyn_share, p.dyn_chunk, p.dyn_units_max);
   const merge::Scratch<kMergeThreads> sc = merge::Scratch<kMergeThreads>::carve(
       merge_smem + merge_cum_bytes(S), merge::rows_per_block(S * tiles, gridDim.x));
   merge::plan<kMergeThreads>(p, cum, split, sc, blockIdx.x, gridDim.x);

@@ -49,8 +49,6 @@
 namespace pkv {
 namespace mma {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
 constexpr int kST = 16;               // tokens per pipeline stage
 constexpr float kRescaleGap = 8.f;    // log2 of the largest weight allowed before rescaling
 
@@ -62,6 +60,14 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+// 8x8 b16 matrix transposed across the warp: the lane holding (row r, columns 2c, 2c+1)
+// receives (row r, columns 2c, 2c+1) of the transpose
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
 }
 
 template <bool kF16>
@@ -123,15 +129,21 @@ template <typename KV, int D, int G>
 struct Cfg {
   static constexpr bool kFp8 = std::is_same<KV, E4M3>::value;
   static constexpr bool kF16 = kFp8;                       // f16 MMAs for an 8-bit cache
+  // warps per block: an 8-bit cache's kernel is bound by instruction issue, and its
+  // smaller register footprint (heads in N) lets 12 warps share an SM
+  static constexpr int kWarps = kFp8 ? 12 : 8;
+  static constexpr int kThreads = kWarps * 32;
   static constexpr int kHalves = D / 64;                   // 128-byte operand rows of 16-bit data
   static constexpr int kRawRowBytes = D * KV::bytes;       // one token row as stored
   static constexpr int kRawTile = kST * kRawRowBytes;      // K (or V) bytes of a stage, as stored
-  static constexpr int kStages = (kFp8 || D == 64) ? 4 : 3;
+  static constexpr int kStages = (!kFp8 && D == 64) ? 4 : 3;
   static constexpr int kStageBytes = 2 * kRawTile;         // K then V
   static constexpr int kVConv = 0;                         // (no staging tile: 8-bit V is widened in registers)
-  static constexpr int kRows = G > 8 ? 2 : 1;              // real MMA rows per thread (g, g+8)
-  static constexpr int kNT = D / 8;                        // output n-tiles
+  static constexpr int kRows = G > 8 ? 2 : 1;              // 16-bit cache: real MMA rows per thread (g, g+8)
+  static constexpr int kNT = D / 8;                        // 16-bit cache: output n-tiles
   static constexpr int kKS = D / 16;                       // k-steps of the score MMA
+  static constexpr int kHT = (G + 7) / 8;                  // 8-bit cache: head tiles (MMA N = 8 heads)
+  static constexpr int kMT = D / 16;                       // 8-bit cache: head_dim tiles of the value MMA
   static_assert(kFp8 ? D == 128 : (D == 64 || D == 128), "head_dim");
   static_assert(G == 4 || G == 8 || G == 16, "heads per item");
   static_assert(kRawTile % 1024 == 0 || kRawRowBytes == 64, "tiles are whole swizzle atoms");
@@ -240,10 +252,11 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const Geometry& q) {
 // the stage that holds its position); a separate instantiation, so that plain decode
 // calls carry none of its code.
 template <typename KV, int D, int G, bool kAppend>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<KV, D, G>::kThreads, 1)
 paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                         const DecodeParams p) {
   using C = Cfg<KV, D, G>;
+  constexpr int kWarps = C::kWarps, kThreads = C::kThreads;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);  // swizzle atoms
   const int S = p.num_seqs;
@@ -455,10 +468,11 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
   };
   if (split.len(gw) > 0) start_unit(gw); else claim();
 
-  // queries of one row as MMA A fragments (rows g and g+8, this lane's k's)
-  auto load_q = [&](int s, int h0, uint32_t (&qa)[C::kKS][4]) {
+  // 16-bit cache: queries of one row as MMA A fragments (rows g and g+8, this lane's k's)
+  constexpr int kQA = C::kFp8 ? 1 : C::kKS;
+  auto load_q = [&](int s, int h0, uint32_t (&qa)[kQA][4]) {
 #pragma unroll
-    for (int kk = 0; kk < C::kKS; ++kk)
+    for (int kk = 0; kk < kQA; ++kk)
 #pragma unroll
       for (int r = 0; r < 4; ++r) qa[kk][r] = 0u;
 #pragma unroll
@@ -468,17 +482,33 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
         const uint16_t* q = static_cast<const uint16_t*>(p.query) + int64_t(s) * p.q_stride_s +
                             int64_t(h0 + row) * p.q_stride_h;
 #pragma unroll
-        for (int kk = 0; kk < C::kKS; ++kk) {
-          if constexpr (C::kFp8) {
-            // k index 2c, 2c+1, 2c+8, 2c+9 <-> d = 32c + 4kk + {0,1,2,3} (matches the K reads:
-            // a thread's 32 columns of a key row are two adjacent 16-byte chunks)
-            const uint2 w = __ldg(reinterpret_cast<const uint2*>(q + 32 * c4 + 4 * kk));
-            qa[kk][0 + rr] = bf16x2_to_f16x2(w.x);
-            qa[kk][2 + rr] = bf16x2_to_f16x2(w.y);
-          } else {
-            qa[kk][0 + rr] = __ldg(reinterpret_cast<const uint32_t*>(q + 16 * kk + 2 * c4));
-            qa[kk][2 + rr] = __ldg(reinterpret_cast<const uint32_t*>(q + 16 * kk + 8 + 2 * c4));
-          }
+        for (int kk = 0; kk < kQA; ++kk) {
+          qa[kk][0 + rr] = __ldg(reinterpret_cast<const uint32_t*>(q + 16 * kk + 2 * c4));
+          qa[kk][2 + rr] = __ldg(reinterpret_cast<const uint32_t*>(q + 16 * kk + 8 + 2 * c4));
+        }
+      }
+    }
+  };
+  // 8-bit cache: queries as the B operand of the score MMAs, head 8 ht + g of the row
+  // (zero past G); k slots 2c, 2c+1 | 2c+8, 2c+9 of k-step kk <-> d = 32c + 4kk + {0,1} |
+  // {2,3}, matching the key reads (a lane's 32 columns of a key row are two 16-byte chunks)
+  constexpr int kQHT = C::kFp8 ? C::kHT : 1, kQKS = C::kFp8 ? C::kKS : 2;
+  auto load_qb = [&](int s, int h0, uint32_t (&qb)[kQHT][kQKS][2]) {
+#pragma unroll
+    for (int ht = 0; ht < kQHT; ++ht) {
+      const int h = 8 * ht + g;
+#pragma unroll
+      for (int kk = 0; kk < kQKS; ++kk) qb[ht][kk][0] = qb[ht][kk][1] = 0u;
+      if (h < G) {
+        const uint16_t* q = static_cast<const uint16_t*>(p.query) + int64_t(s) * p.q_stride_s +
+                            int64_t(h0 + h) * p.q_stride_h;
+#pragma unroll
+        for (int i = 0; i < kQKS / 2; ++i) {
+          const uint4 w = __ldg(reinterpret_cast<const uint4*>(q + 32 * c4 + 8 * i));
+          qb[ht][2 * i][0] = bf16x2_to_f16x2(w.x);
+          qb[ht][2 * i][1] = bf16x2_to_f16x2(w.y);
+          qb[ht][2 * i + 1][0] = bf16x2_to_f16x2(w.z);
+          qb[ht][2 * i + 1][1] = bf16x2_to_f16x2(w.w);
         }
       }
     }
@@ -500,11 +530,19 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
   Cursor cc;
   cc.left = 0;
   int cu = 0;  // unit being consumed
-  uint32_t qa[C::kKS][4], qa_next[C::kKS][4];
   float sl = p.qk_scale_log2;  // score scale (base 2) of the current row's KV head
   float vsc = p.v_scale;       // value scale of the current row's KV head
-  float o[C::kNT][4];
+  // 16-bit cache: query heads in M (padded to 16), tokens in N (scores) and K (values)
+  uint32_t qa[kQA][4], qa_next[kQA][4];
+  float o[C::kFp8 ? 1 : C::kNT][4];
   float m_ref[C::kRows], l_run[C::kRows];
+  // 8-bit cache: tokens (scores) and head_dim (values) in M, query heads in N: S^T = K Q^T,
+  // then O^T += V^T P^T with P^T moved into the B operand by an 8x8 transpose in registers.
+  // A lane holds, per head tile, heads 8 ht + 2 c4 + e (e = 0, 1): scores of tokens g and
+  // g + 8, output columns 16 g + 2 mt (o8[mt][ht][e]) and 16 g + 2 mt + 1 (o8[mt][ht][2 + e]).
+  uint32_t qb[kQHT][kQKS][2], qb_next[kQHT][kQKS][2];
+  float o8[C::kFp8 ? C::kMT : 1][kQHT][4];
+  float m8[kQHT][2], l8[kQHT][2];
   bool first = true, aborted = false;
   int cslot = 0;
   uint32_t cphase = 0;
@@ -536,10 +574,19 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
       if (p.k_head_scales) sl = p.qk_scale_log2 * __ldg(p.k_head_scales + cc.kvh);
       if (p.v_head_scales) vsc = __ldg(p.v_head_scales + cc.kvh);
       if (unit_start) {
-        load_q(cc.s, cc.kvh * p.group + cc.sub * G, qa);
+        if constexpr (C::kFp8) load_qb(cc.s, cc.kvh * p.group + cc.sub * G, qb);
+        else load_q(cc.s, cc.kvh * p.group + cc.sub * G, qa);
+      } else if constexpr (C::kFp8) {
+#pragma unroll
+        for (int ht = 0; ht < kQHT; ++ht)
+#pragma unroll
+          for (int kk = 0; kk < kQKS; ++kk) {
+            qb[ht][kk][0] = qb_next[ht][kk][0];
+            qb[ht][kk][1] = qb_next[ht][kk][1];
+          }
       } else {
 #pragma unroll
-        for (int kk = 0; kk < C::kKS; ++kk)
+        for (int kk = 0; kk < kQA; ++kk)
 #pragma unroll
           for (int r = 0; r < 4; ++r) qa[kk][r] = qa_next[kk][r];
       }
@@ -553,16 +600,33 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
           kvh2 = sub2 = 0;
           do { ++s2; } while (cum[s2 + 1] == cum[s2]);
         }
-        load_q(s2, kvh2 * p.group + sub2 * G, qa_next);
+        if constexpr (C::kFp8) load_qb(s2, kvh2 * p.group + sub2 * G, qb_next);
+        else load_q(s2, kvh2 * p.group + sub2 * G, qa_next);
       }
+      if constexpr (C::kFp8) {
 #pragma unroll
-      for (int n = 0; n < C::kNT; ++n)
+        for (int mt = 0; mt < C::kMT; ++mt)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) o[n][r] = 0.f;
+          for (int ht = 0; ht < kQHT; ++ht)
 #pragma unroll
-      for (int rr = 0; rr < C::kRows; ++rr) {
-        m_ref[rr] = -INFINITY;
-        l_run[rr] = 0.f;
+            for (int r = 0; r < 4; ++r) o8[mt][ht][r] = 0.f;
+#pragma unroll
+        for (int ht = 0; ht < kQHT; ++ht)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            m8[ht][e] = -INFINITY;
+            l8[ht][e] = 0.f;
+          }
+      } else {
+#pragma unroll
+        for (int n = 0; n < C::kNT; ++n)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) o[n][r] = 0.f;
+#pragma unroll
+        for (int rr = 0; rr < C::kRows; ++rr) {
+          m_ref[rr] = -INFINITY;
+          l_run[rr] = 0.f;
+        }
       }
     }
 
@@ -653,6 +717,115 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
       __syncwarp();
     }
 
+    if constexpr (C::kFp8) {
+      // scores S^T = K Q^T: tokens g and g + 8, columns d = 32 c4 .. 32 c4 + 31 (two
+      // 16-byte chunks each), widened to f16 in registers; two chains of k-steps
+      float s[kQHT][4], s2[kQHT][4];
+#pragma unroll
+      for (int ht = 0; ht < kQHT; ++ht)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) s[ht][r] = s2[ht][r] = 0.f;
+      {
+        const uint4 ka0 = *reinterpret_cast<const uint4*>(kt + g * 128 + (((2 * c4) ^ g) << 4));
+        const uint4 ka1 = *reinterpret_cast<const uint4*>(kt + g * 128 + (((2 * c4 + 1) ^ g) << 4));
+        const uint4 kb0 = *reinterpret_cast<const uint4*>(kt + (g + 8) * 128 + (((2 * c4) ^ g) << 4));
+        const uint4 kb1 = *reinterpret_cast<const uint4*>(kt + (g + 8) * 128 + (((2 * c4 + 1) ^ g) << 4));
+        const uint32_t kwa[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
+        const uint32_t kwb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
+#pragma unroll
+        for (int kk = 0; kk < kQKS; ++kk) {
+          const uint32_t a0 = e4m3x2_to_f16x2(kwa[kk]), a2 = e4m3x2_to_f16x2(kwa[kk] >> 16);
+          const uint32_t a1 = e4m3x2_to_f16x2(kwb[kk]), a3 = e4m3x2_to_f16x2(kwb[kk] >> 16);
+#pragma unroll
+          for (int ht = 0; ht < kQHT; ++ht)
+            mma16816<true>(kk & 1 ? s2[ht] : s[ht], a0, a1, a2, a3, qb[ht][kk][0], qb[ht][kk][1]);
+        }
+      }
+      // online softmax in base 2 against a lazily moved reference max; head e of the
+      // lane's pair holds s[ht][e] (token g) and s[ht][2 + e] (token g + 8)
+      bool need = false;
+      float m_new[kQHT][2];
+#pragma unroll
+      for (int ht = 0; ht < kQHT; ++ht) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) s[ht][r] = (s[ht][r] + s2[ht][r]) * sl;
+        if (nvalid < kST || lo_valid > 0) {  // the row's last stage, or the window's first
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int t = g + 8 * (r >> 1);
+            if (t >= nvalid || t < lo_valid) s[ht][r] = -INFINITY;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float mx = fmaxf(s[ht][e], s[ht][2 + e]);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          m_new[ht][e] = m8[ht][e];
+          if (mx > m8[ht][e] + kRescaleGap || m8[ht][e] == -INFINITY) {
+            m_new[ht][e] = mx;
+            need = true;
+          }
+        }
+      }
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int ht = 0; ht < kQHT; ++ht)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float alpha = m_new[ht][e] == m8[ht][e] ? 1.f : fast_exp2(m8[ht][e] - m_new[ht][e]);
+            l8[ht][e] *= alpha;
+#pragma unroll
+            for (int mt = 0; mt < C::kMT; ++mt) {
+              o8[mt][ht][e] *= alpha;
+              o8[mt][ht][2 + e] *= alpha;
+            }
+            m8[ht][e] = m_new[ht][e];
+          }
+      }
+      // weights, and P^T as the value MMA's B operand: the lane's (token, head pair)
+      // words transposed per 8x8 block give (tokens 2 c4, 2 c4 + 1 | + 8, + 9; head g)
+      uint32_t pb[kQHT][2];
+#pragma unroll
+      for (int ht = 0; ht < kQHT; ++ht) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float mu = m8[ht][r & 1] == -INFINITY ? 0.f : m8[ht][r & 1];
+          s[ht][r] = fast_exp2(s[ht][r] - mu);
+        }
+        l8[ht][0] += s[ht][0] + s[ht][2];
+        l8[ht][1] += s[ht][1] + s[ht][3];
+        pb[ht][0] = movmatrix_trans(pack2(s[ht][0], s[ht][1], true));
+        pb[ht][1] = movmatrix_trans(pack2(s[ht][2], s[ht][3], true));
+      }
+      // O^T += V^T P^T: tokens 2 c4, 2 c4 + 1, 2 c4 + 8, 2 c4 + 9 at columns 16 g ..
+      // 16 g + 15 (one 16-byte chunk each, zero past the context); byte permutes pair
+      // the tokens per column, and m-tile mt takes columns 16 g + 2 mt (row g) and
+      // 16 g + 2 mt + 1 (row g + 8)
+      uint4 wv[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int r = 2 * c4 + (t & 1) + 8 * (t >> 1);
+        wv[t] = r < nvalid ? *reinterpret_cast<const uint4*>(vt + r * 128 + ((g ^ (r & 7)) << 4))
+                           : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t x0 = (&wv[0].x)[j], x1 = (&wv[1].x)[j], y0 = (&wv[2].x)[j], y1 = (&wv[3].x)[j];
+        const uint32_t x01 = __byte_perm(x0, x1, 0x5140), x23 = __byte_perm(x0, x1, 0x7362);
+        const uint32_t y01 = __byte_perm(y0, y1, 0x5140), y23 = __byte_perm(y0, y1, 0x7362);
+        const uint32_t a0 = e4m3x2_to_f16x2(x01), a1 = e4m3x2_to_f16x2(x01 >> 16);
+        const uint32_t a2 = e4m3x2_to_f16x2(y01), a3 = e4m3x2_to_f16x2(y01 >> 16);
+        const uint32_t c0 = e4m3x2_to_f16x2(x23), c1 = e4m3x2_to_f16x2(x23 >> 16);
+        const uint32_t c2 = e4m3x2_to_f16x2(y23), c3 = e4m3x2_to_f16x2(y23 >> 16);
+#pragma unroll
+        for (int ht = 0; ht < kQHT; ++ht) {
+          mma16816<true>(o8[2 * j][ht], a0, a1, a2, a3, pb[ht][0], pb[ht][1]);
+          mma16816<true>(o8[2 * j + 1][ht], c0, c1, c2, c3, pb[ht][0], pb[ht][1]);
+        }
+      }
+    } else {
     // scores S = Q K^T for the stage's 16 tokens (2 n-tiles of 8), two chains per tile
     float s[2][4];
     {
@@ -661,30 +834,16 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int r = 0; r < 4; ++r) s[nt][r] = s2[nt][r] = 0.f;
-      if constexpr (C::kFp8) {
+      const uint32_t kbase = smem_addr(kt);
+#pragma unroll
+      for (int i = 0; i < C::kKS / 2; ++i)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          const int row = 4 * (g >> 1) + (g & 1) + 2 * nt;  // token of score column nt * 8 + g
-          const uint4 ka = *reinterpret_cast<const uint4*>(kt + row * 128 + (((2 * c4) ^ (row & 7)) << 4));
-          const uint4 kb = *reinterpret_cast<const uint4*>(kt + row * 128 + (((2 * c4 + 1) ^ (row & 7)) << 4));
-          const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-#pragma unroll
-          for (int kk = 0; kk < C::kKS; ++kk)
-            mma16816<true>(kk & 1 ? s2[nt] : s[nt], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3],
-                           e4m3x2_to_f16x2(kw[kk]), e4m3x2_to_f16x2(kw[kk] >> 16));
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kbase + koff[i] + nt * 1024, b0, b1, b2, b3);
+          mma16816<false>(s[nt], qa[2 * i][0], qa[2 * i][1], qa[2 * i][2], qa[2 * i][3], b0, b1);
+          mma16816<false>(s2[nt], qa[2 * i + 1][0], qa[2 * i + 1][1], qa[2 * i + 1][2], qa[2 * i + 1][3], b2, b3);
         }
-      } else {
-        const uint32_t kbase = smem_addr(kt);
-#pragma unroll
-        for (int i = 0; i < C::kKS / 2; ++i)
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(kbase + koff[i] + nt * 1024, b0, b1, b2, b3);
-            mma16816<false>(s[nt], qa[2 * i][0], qa[2 * i][1], qa[2 * i][2], qa[2 * i][3], b0, b1);
-            mma16816<false>(s2[nt], qa[2 * i + 1][0], qa[2 * i + 1][1], qa[2 * i + 1][2], qa[2 * i + 1][3], b2, b3);
-          }
-      }
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -705,7 +864,7 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int t = C::kFp8 ? 4 * c4 + e + 2 * nt : nt * 8 + 2 * c4 + e;  // the column's token
+            const int t = nt * 8 + 2 * c4 + e;  // the column's token
             if (t >= nvalid || t < lo_valid) s[nt][2 * rr + e] = -INFINITY;
           }
       }
@@ -748,42 +907,20 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
 
     // O += P V over the stage's 16 tokens
     {
-      const uint32_t a0 = pack2(s[0][0], s[0][1], C::kF16);
-      const uint32_t a2 = pack2(s[1][0], s[1][1], C::kF16);
-      const uint32_t a1 = C::kRows > 1 ? pack2(s[0][2], s[0][3], C::kF16) : 0u;
-      const uint32_t a3 = C::kRows > 1 ? pack2(s[1][2], s[1][3], C::kF16) : 0u;
-      if constexpr (C::kFp8) {
-        // tokens 4 c4 .. 4 c4 + 3 (P's k slots 2 c4, 2 c4 + 1, 2 c4 + 8, 2 c4 + 9) at
-        // columns d = 32 m + 4 g + i: one 32-bit word per token row and m, transposed
-        // by byte permutes into token pairs per column and widened to f16 in registers;
-        // n-tile 4 m + i of o holds columns 32 m + 4 n + i
+      const uint32_t a0 = pack2(s[0][0], s[0][1], false);
+      const uint32_t a2 = pack2(s[1][0], s[1][1], false);
+      const uint32_t a1 = C::kRows > 1 ? pack2(s[0][2], s[0][3], false) : 0u;
+      const uint32_t a3 = C::kRows > 1 ? pack2(s[1][2], s[1][3], false) : 0u;
+      const uint32_t vbase = smem_addr(vt);
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          uint32_t wv[4];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int r = 4 * c4 + t, b = 32 * m + 4 * g;
-            wv[t] = r < nvalid ? *reinterpret_cast<const uint32_t*>(vt + r * 128 + (((b >> 4) ^ (r & 7)) << 4) + (b & 15))
-                               : 0u;
-          }
-          const uint32_t x01 = __byte_perm(wv[0], wv[1], 0x5140), x23 = __byte_perm(wv[0], wv[1], 0x7362);
-          const uint32_t y01 = __byte_perm(wv[2], wv[3], 0x5140), y23 = __byte_perm(wv[2], wv[3], 0x7362);
-          mma16816<true>(o[4 * m], a0, a1, a2, a3, e4m3x2_to_f16x2(x01), e4m3x2_to_f16x2(y01));
-          mma16816<true>(o[4 * m + 1], a0, a1, a2, a3, e4m3x2_to_f16x2(x01 >> 16), e4m3x2_to_f16x2(y01 >> 16));
-          mma16816<true>(o[4 * m + 2], a0, a1, a2, a3, e4m3x2_to_f16x2(x23), e4m3x2_to_f16x2(y23));
-          mma16816<true>(o[4 * m + 3], a0, a1, a2, a3, e4m3x2_to_f16x2(x23 >> 16), e4m3x2_to_f16x2(y23 >> 16));
-        }
-      } else {
-        const uint32_t vbase = smem_addr(vt);
-#pragma unroll
-        for (int n = 0; n < C::kNT; n += 2) {
-          const int i = n / 2;
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vbase + voff[i % 4] + (i / 4) * kST * 128, b0, b1, b2, b3);
-          mma16816<false>(o[n], a0, a1, a2, a3, b0, b1);
-          mma16816<false>(o[n + 1], a0, a1, a2, a3, b2, b3);
-        }
+      for (int n = 0; n < C::kNT; n += 2) {
+        const int i = n / 2;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vbase + voff[i % 4] + (i / 4) * kST * 128, b0, b1, b2, b3);
+        mma16816<false>(o[n], a0, a1, a2, a3, b0, b1);
+        mma16816<false>(o[n + 1], a0, a1, a2, a3, b2, b3);
       }
+    }
     }
     __syncwarp();
     ++consumed;  // the slot may be refilled
@@ -794,67 +931,83 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
 
     // ---- end of this warp's part of a row -----------------------------------------
     if (last) {
-#pragma unroll
-      for (int rr = 0; rr < C::kRows; ++rr) {
-        l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 1);
-        l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 2);
-      }
       const int row_id = cc.s * tiles + cc.tile;
       const int row_start = cum[cc.s] + cc.tile * cc.rl;
       const int wf = split.owner(row_start / kST), wl = split.owner((row_start + cc.rl) / kST - 1);
       const int h0 = cc.kvh * p.group + cc.sub * G;
       __nv_bfloat16* outs = static_cast<__nv_bfloat16*>(p.out) + int64_t(cc.s) * p.out_stride_s;
-      if (wf == wl) {  // the whole row is in this unit: write the output
+      const bool whole = wf == wl;      // the whole row is in this unit: write the output
+      const int slot_id = cu + row_id;  // else its partial slot: distinct for every (row, unit) pair
+      if constexpr (C::kFp8) {
+#pragma unroll
+        for (int ht = 0; ht < kQHT; ++ht)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            l8[ht][e] += __shfl_xor_sync(0xffffffffu, l8[ht][e], 4);
+            l8[ht][e] += __shfl_xor_sync(0xffffffffu, l8[ht][e], 8);
+            l8[ht][e] += __shfl_xor_sync(0xffffffffu, l8[ht][e], 16);
+          }
+        // head 8 ht + 2 c4 + e: columns 16 g .. 16 g + 15, m-tile mt holding 2 mt, 2 mt + 1
+#pragma unroll
+        for (int ht = 0; ht < kQHT; ++ht)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int hr = 8 * ht + 2 * c4 + e;
+            if (hr < G) {
+              const float inv = l8[ht][e] > 0.f ? vsc / l8[ht][e] : 0.f;
+              if (whole) {
+                uint32_t w[8];
+#pragma unroll
+                for (int mt = 0; mt < C::kMT; ++mt) {
+                  const __nv_bfloat162 v = __floats2bfloat162_rn(o8[mt][ht][e] * inv, o8[mt][ht][2 + e] * inv);
+                  w[mt] = *reinterpret_cast<const uint32_t*>(&v);
+                }
+                __nv_bfloat16* out = outs + int64_t(h0 + hr) * p.out_stride_h + 16 * g;
+                *reinterpret_cast<uint4*>(out) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4*>(out + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+              } else {
+                const int64_t pr = int64_t(slot_id) * G + hr;
+                float* po = p.part_o + pr * D + 16 * g;
+#pragma unroll
+                for (int q4 = 0; q4 < C::kMT / 2; ++q4)
+                  *reinterpret_cast<float4*>(po + 4 * q4) =
+                      make_float4(o8[2 * q4][ht][e] * inv, o8[2 * q4][ht][2 + e] * inv,
+                                  o8[2 * q4 + 1][ht][e] * inv, o8[2 * q4 + 1][ht][2 + e] * inv);
+                if (g == 0) {
+                  p.part_m[pr] = m8[ht][e];
+                  p.part_l[pr] = l8[ht][e];
+                }
+              }
+            }
+          }
+      } else {
+#pragma unroll
+        for (int rr = 0; rr < C::kRows; ++rr) {
+          l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 1);
+          l_run[rr] += __shfl_xor_sync(0xffffffffu, l_run[rr], 2);
+        }
 #pragma unroll
         for (int rr = 0; rr < C::kRows; ++rr) {
           const int hr = g + 8 * rr;
           if (hr < G) {
             const float inv = l_run[rr] > 0.f ? vsc / l_run[rr] : 0.f;
-            __nv_bfloat16* out = outs + int64_t(h0 + hr) * p.out_stride_h;
-            if constexpr (C::kFp8) {  // n-tile 4 m + i, column 2 c4 + e: d = 32 m + 8 c4 + 4 e + i
-#pragma unroll
-              for (int m = 0; m < 4; ++m)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                  const __nv_bfloat162 lo = __floats2bfloat162_rn(o[4 * m][2 * rr + e] * inv, o[4 * m + 1][2 * rr + e] * inv);
-                  const __nv_bfloat162 hi = __floats2bfloat162_rn(o[4 * m + 2][2 * rr + e] * inv, o[4 * m + 3][2 * rr + e] * inv);
-                  *reinterpret_cast<uint2*>(out + 32 * m + 8 * c4 + 4 * e) =
-                      make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
-                }
-            } else {
+            if (whole) {
+              __nv_bfloat16* out = outs + int64_t(h0 + hr) * p.out_stride_h;
 #pragma unroll
               for (int n = 0; n < C::kNT; ++n)
                 *reinterpret_cast<__nv_bfloat162*>(out + n * 8 + 2 * c4) =
                     __floats2bfloat162_rn(o[n][2 * rr] * inv, o[n][2 * rr + 1] * inv);
-            }
-          }
-        }
-      } else {
-        const int slot_id = cu + row_id;  // distinct for every (row, unit) pair: < units + rows
-#pragma unroll
-        for (int rr = 0; rr < C::kRows; ++rr) {
-          const int hr = g + 8 * rr;
-          if (hr < G) {
-            const int64_t pr = int64_t(slot_id) * G + hr;
-            const float inv = l_run[rr] > 0.f ? vsc / l_run[rr] : 0.f;
-            float* po = p.part_o + pr * D;
-            if constexpr (C::kFp8) {
-#pragma unroll
-              for (int m = 0; m < 4; ++m)
-#pragma unroll
-                for (int e = 0; e < 2; ++e)
-                  *reinterpret_cast<float4*>(po + 32 * m + 8 * c4 + 4 * e) =
-                      make_float4(o[4 * m][2 * rr + e] * inv, o[4 * m + 1][2 * rr + e] * inv,
-                                  o[4 * m + 2][2 * rr + e] * inv, o[4 * m + 3][2 * rr + e] * inv);
             } else {
+              const int64_t pr = int64_t(slot_id) * G + hr;
+              float* po = p.part_o + pr * D;
 #pragma unroll
               for (int n = 0; n < C::kNT; ++n)
                 *reinterpret_cast<float2*>(po + n * 8 + 2 * c4) =
                     make_float2(o[n][2 * rr] * inv, o[n][2 * rr + 1] * inv);
-            }
-            if (c4 == 0) {
-              p.part_m[pr] = m_ref[rr];
-              p.part_l[pr] = l_run[rr];
+              if (c4 == 0) {
+                p.part_m[pr] = m_ref[rr];
+                p.part_l[pr] = l_run[rr];
+              }
             }
           }
         }

@@ -38,10 +38,10 @@ cudaError_t launch_tpl(const DecodeParams& p, cudaStream_t stream) {
       return e;
     if (dev >= 0 && dev < kMapCacheDevices) smem_set[dev] = smem;
   }
-  static_assert(mma::kWarps == kMmaWarps, "warps per block");
+  if (C::kWarps != p.block_warps) return cudaErrorInvalidValue;  // the partial slots assume it
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(p.grid));
-  cfg.blockDim = dim3(unsigned(mma::kThreads));
+  cfg.blockDim = dim3(unsigned(C::kThreads));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

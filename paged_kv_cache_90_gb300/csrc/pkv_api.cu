@@ -27,6 +27,7 @@ std::atomic<int64_t> g_opt_decode_kernel{0};
 std::atomic<int64_t> g_opt_dynamic_share{-1};
 std::atomic<int64_t> g_opt_dynamic_chunk{4};
 std::atomic<int64_t> g_opt_fused_append{0};
+std::atomic<int64_t> g_opt_prefill_kernel{0};
 
 thread_local std::string t_last_error;
 
@@ -343,9 +344,10 @@ pkv_status decode_prepare(const pkv_tensor* out, const pkv_tensor* query, const 
     const int64_t share = g_opt_dynamic_share.load();
     p.dyn_share = share >= 0 ? int(share) : (p.kv_dtype == kE4M3 ? 0 : 256);
     p.dyn_chunk = int(g_opt_dynamic_chunk.load());
-    p.dyn_units_max = 2 * p.grid * kMmaWarps;
+    p.block_warps = mma_block_warps(p.kv_dtype);
+    p.dyn_units_max = 2 * p.grid * p.block_warps;
     const int64_t rows = int64_t(S) * (Hq / p.heads_per_item);
-    p.partial_rows = (int64_t(p.grid) * kMmaWarps + p.dyn_units_max + rows) * p.heads_per_item;
+    p.partial_rows = (int64_t(p.grid) * p.block_warps + p.dyn_units_max + rows) * p.heads_per_item;
   }
   if (p.partial_rows) *ws_bytes = kWorkspaceHeader + size_t(p.partial_rows) * (size_t(D) + 2) * 4;
   return PKV_OK;
@@ -480,6 +482,10 @@ pkv_status pkv_set_option(int32_t option, int64_t value) {
       if (value < 0 || value > 2) return fail(PKV_ERR_INVALID_ARG, "fused append is 0, 1 or 2");
       g_opt_fused_append = value;
       return PKV_OK;
+    case PKV_OPT_PREFILL_KERNEL:
+      if (value < 0 || value > 2) return fail(PKV_ERR_INVALID_ARG, "prefill kernel is 0, 1 or 2");
+      g_opt_prefill_kernel = value;
+      return PKV_OK;
     default:
       return fail(PKV_ERR_INVALID_ARG, "unknown option %d", option);
   }
@@ -494,6 +500,7 @@ int64_t pkv_get_option(int32_t option) {
     case PKV_OPT_DYNAMIC_SHARE: return g_opt_dynamic_share.load();
     case PKV_OPT_DYNAMIC_CHUNK: return g_opt_dynamic_chunk.load();
     case PKV_OPT_FUSED_APPEND: return g_opt_fused_append.load();
+    case PKV_OPT_PREFILL_KERNEL: return g_opt_prefill_kernel.load();
     default: return -1;
   }
 }
@@ -518,7 +525,7 @@ int64_t pkv_decode_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t 
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       num_sms = 256;
-    const int64_t units = 3 * int64_t(num_sms) * kMmaWarps;
+    const int64_t units = 3 * int64_t(num_sms) * kMmaMaxWarps;
     tc = int64_t(kWorkspaceHeader) + (units * G + int64_t(num_seqs) * num_heads) * (head_dim + 2) * 4;
   }
   return core > tc ? core : tc;
@@ -657,12 +664,16 @@ pkv_status pkv_paged_attention_prefill(const pkv_tensor* out, const pkv_tensor* 
     return fail(PKV_ERR_UNSUPPORTED, "prefill needs bf16 queries, outputs and caches, head_dim 64/128, block size "
                 "8/16/32, at most %d table entries per sequence, 16-byte aligned query/out rows",
                 kPrefillMaxTableEntries);
+  const int64_t want = g_opt_prefill_kernel.load();
+  const bool tc_ok = want != 1 && T > 0 && prefill_tc_supported(p);
+  if (want == 2 && !tc_ok && T > 0)
+    return fail(PKV_ERR_UNSUPPORTED, "the tcgen05 prefill kernel does not support this call");
   if (g_opt_dry_run.load() || S == 0 || T == 0 || Hq == 0) return PKV_OK;
   DeviceState* ds;
   if ((st = device_state(&ds))) return st;
   p.err = ds->err;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  return finish_call(ds, launch_prefill(p, cs), cs, "paged_attention_prefill");
+  return finish_call(ds, tc_ok ? launch_prefill_tc(p, cs) : launch_prefill(p, cs), cs, "paged_attention_prefill");
 }
 
 pkv_status pkv_reshape_and_cache(const pkv_tensor* key, const pkv_tensor* value,

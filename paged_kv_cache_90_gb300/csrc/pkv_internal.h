@@ -101,6 +101,7 @@ struct DecodeParams {
   // tensor-core kernel only
   int kernel;                // 0: CUDA-core kernel, 1: tensor-core kernel
   int heads_per_item;        // query heads per row of work (4, 8 or 16)
+  int block_warps;           // warps per thread block (mma_block_warps)
   int grid;                  // persistent thread blocks
   int dyn_share;             // stages handed out at run time, in 1/1024 of all stages
   int dyn_chunk;             // fewest stages per run-time unit
@@ -143,12 +144,18 @@ int mma_heads_per_item(int group);
 bool mma_decode_supported(const DecodeParams& p);
 // whether the call's shared memory still fits with the fused append's staged tokens
 bool mma_fused_append_fits(const DecodeParams& p);
-constexpr int kMmaWarps = 8;  // warps per thread block of the tensor-core kernel
+// warps per thread block of the tensor-core kernel: 12 for an 8-bit cache, else 8
+inline int mma_block_warps(int kv_dtype) { return kv_dtype == kE4M3 ? 12 : 8; }
+constexpr int kMmaMaxWarps = 12;
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream);
 // Prefill (prefill_mma.cuh, launched from decode_mma.cu): whether it handles a call,
 // and its launch.
 bool prefill_supported(const DecodeParams& p);
 cudaError_t launch_prefill(const DecodeParams& p, cudaStream_t stream);
+// Prefill on the fifth-generation tensor cores (prefill_tc.cu): whether it handles a
+// call, and its launch.
+bool prefill_tc_supported(const DecodeParams& p);
+cudaError_t launch_prefill_tc(const DecodeParams& p, cudaStream_t stream);
 constexpr int kPrefillMaxTableEntries = 8192;  // block-table entries a prefill CTA holds
 
 // Per-dtype launchers (one translation unit each).

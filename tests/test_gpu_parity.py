@@ -40,6 +40,15 @@ def kernel(request):
     binding.set_option("decode_kernel", 0)
 
 
+@pytest.fixture(params=["tcgen05", "mma_sync"])
+def pkernel(request):
+    """Run a prefill test on the tcgen05 kernel (accumulators in tensor memory), then on
+    the mma.sync one."""
+    binding.set_option("prefill_kernel", 2 if request.param == "tcgen05" else 1)
+    yield request.param
+    binding.set_option("prefill_kernel", 0)
+
+
 @pytest.fixture
 def partition_tokens():
     def set_(n):
@@ -235,7 +244,7 @@ def test_continuous_batching_full(bs, kv, kernel):
 
 @pytest.mark.parametrize("bs", [8, 16, 32])
 @pytest.mark.parametrize("heads", [(32, 8), (16, 16), (16, 8), (32, 2), (12, 4)])
-def test_prefill_small(bs, heads):
+def test_prefill_small(bs, heads, pkernel):
     """Prompts and later chunks of different lengths (tile edges, prefixes off the
     stage grid), GQA groups 1 to 16, every unused slot NaN."""
     hq, hk = heads
@@ -244,7 +253,7 @@ def test_prefill_small(bs, heads):
                                       head_dim=128 if hq != 12 else 64, block_size=bs, poison=True))
 
 
-def test_prefill_empty_chunk_and_single_tokens():
+def test_prefill_empty_chunk_and_single_tokens(pkernel):
     """A sequence with no new token leaves nothing to write; one-token chunks equal
     decode (checked against the oracle like every prefill)."""
     check_workload(wl.chunked_prefill(seed=95, prefix_lens=(10, 300, 0, 47), chunk_lens=(1, 1, 1, 1), poison=True))
@@ -259,7 +268,7 @@ def test_prefill_empty_chunk_and_single_tokens():
     check_workload(w)
 
 
-def test_prefill_full():
+def test_prefill_full(pkernel):
     """Llama-3-8B-shaped prefill: two 2048-token prompts and two 512-token chunks of
     long prompts (prefixes 512 and 1536)."""
     check_workload(wl.chunked_prefill())
@@ -774,7 +783,7 @@ def test_tensor_core_kernel_rejects_what_it_cannot_run():
 
 
 @pytest.mark.parametrize("bs", [8, 16, 32])
-def test_prefill_over_prefix_cached_blocks(bs):
+def test_prefill_over_prefix_cached_blocks(bs, pkernel):
     """Prompts sharing a system prompt's cached blocks through the prefix cache: every
     sequence of the step reads the same physical prefix blocks and prefills its own
     suffix (unused slots NaN)."""
