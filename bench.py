@@ -50,6 +50,8 @@ UNIT = "GB/s"
 L2_FLUSH_BYTES = 256 << 20
 DECODE_SOURCES = ["decode_core.cuh", "decode_mma.cuh", "decode_mma.cu", "decode_mma_launch.cuh", "merge.cuh",
                   "decode_dispatch.cu", "device_common.cuh", "pkv_internal.h"]
+PREFILL_SOURCES = ["prefill_tc.cu", "tcgen05.cuh", "prefill_mma.cuh", "decode_mma_launch.cuh", "device_common.cuh",
+                   "pkv_internal.h"]
 
 
 # ---- workloads -----------------------------------------------------------------------
@@ -133,9 +135,9 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
-def source_digest() -> str:
+def source_digest(kind: str = "decode") -> str:
     h = hashlib.sha256()
-    for name in DECODE_SOURCES:
+    for name in (DECODE_SOURCES if kind == "decode" else PREFILL_SOURCES):
         p = os.path.join(ROOT, "paged_kv_cache_90_gb300", "csrc", name)
         if os.path.exists(p):
             with open(p, "rb") as f:
@@ -143,16 +145,17 @@ def source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """dram read+write bytes per decode launch from the committed ncu summary for this
-    workload, if it was taken on the current kernel sources."""
-    p = os.path.join(ROOT, "profiles", f"paged_decode_{workload}.md")
+def profiled_traffic(workload: str, kind: str = "decode"):
+    """dram read+write bytes per launch of the decode call (kind "decode") or of the
+    prefill kernel ("prefill") from the committed ncu summary for this workload, if it
+    was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", f"paged_{kind}_{workload}.md")
     if not os.path.exists(p):
         return None
     text = open(p).read()
     m_src = re.search(r"kernel sources digest:\s*`?([0-9a-f]+)`?", text)
     m_tr = re.search(r"dram bytes per launch \(read \+ write\):\s*([0-9]+)", text)
-    if not m_src or not m_tr or m_src.group(1) != source_digest():
+    if not m_src or not m_tr or m_src.group(1) != source_digest(kind):
         return None
     return int(m_tr.group(1))
 
@@ -405,8 +408,10 @@ def run_prefill_gpu(args, world, rank, local, w, dw, dev, flush_l2, barrier):
                    "l2": "flushed between steps (256 MiB write + 256 MiB read, untimed)", "accumulate": "f32",
                    "prefill_us": round(pre_ms * 1e3, 2), "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
-                     "kernel": "paged_prefill_kernel (mma.sync bf16)", "peak_kind": peak_kind},
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload, "prefill"),
+                     "kernel": ("paged_prefill_kernel (mma.sync bf16)" if args.prefill_kernel == "mma_sync" else
+                                "paged_prefill_tc_kernel (tcgen05, accumulators in tensor memory)"),
+                     "peak_kind": peak_kind},
         "cpu_baseline": cpu_base,
         "e2e": {"value": round(e2e, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": int(launches),
@@ -500,6 +505,7 @@ def run_gpu(args, world, rank, local):
     dev = torch.device("cuda", local)
     binding.load_library()
     binding.set_option("decode_kernel", {"auto": 0, "core": 1, "tensor": 2}[args.decode_kernel])
+    binding.set_option("prefill_kernel", {"auto": 0, "mma_sync": 1, "tcgen05": 2}[args.prefill_kernel])
     w = make_workload(args.workload, rank)
     dw = DeviceWorkload(w, dev)
     nsteps = len(w.steps)
@@ -701,6 +707,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle CPU time")
     ap.add_argument("--decode-kernel", choices=["auto", "tensor", "core"], default="auto",
                     help="decode kernel: chosen by the library, tensor-core, or CUDA-core")
+    ap.add_argument("--prefill-kernel", choices=["auto", "tcgen05", "mma_sync"], default="auto",
+                    help="prefill kernel: chosen by the library (tcgen05 where supported), or forced")
     ap.add_argument("--step-mode", choices=sorted(STEP_MODES), default="joint",
                     help="how a decode step's cache write is issued: joint (write + dependent decode "
                          "launch in one call), fused (the write inside the decode kernel), or split "

@@ -40,8 +40,11 @@ __device__ __forceinline__ void raise_amax(float* amax, int h, float x) {
 // Same dtype in and out: bit copy of each token's Hk x D row, 16 bytes at a time.
 __global__ void __launch_bounds__(kWriteThreads) cache_write_copy_kernel(const CacheWriteParams p,
                                                                          int elt_bytes) {
-  // a decode launched behind this write as a programmatic dependent may start its
-  // preparation now (it waits for this grid before it reads the cache)
+  // Launched as a programmatic dependent itself: nothing is read or written before the
+  // kernel ahead of it on the stream has completed.  Then a decode launched behind this
+  // write as its programmatic dependent may start its preparation (it waits for this
+  // grid before it reads the cache).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const int64_t t = blockIdx.x;
   const int64_t slot = p.slot_mapping[t];
@@ -108,7 +111,8 @@ __device__ __forceinline__ void load8<F32>(const unsigned char* p, float* f) {
 // bf16 / f32 source -> e4m3 cache, 8 elements per step.
 template <typename Src>
 __global__ void __launch_bounds__(kWriteThreads) cache_write_e4m3_kernel(const CacheWriteParams p) {
-  asm volatile("griddepcontrol.launch_dependents;");  // as in the copying write
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // as in the copying write
+  asm volatile("griddepcontrol.launch_dependents;");
   const int64_t t = blockIdx.x;
   const int64_t slot = p.slot_mapping[t];
   if (slot < 0) return;
@@ -189,17 +193,28 @@ __global__ void __launch_bounds__(kCheckThreads) copy_pairs_check_kernel(const C
 
 cudaError_t launch_reshape_and_cache(const CacheWriteParams& p, cudaStream_t stream) {
   if (p.num_tokens == 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>(p.num_tokens));
+  // a programmatic dependent of the kernel before it (the kernels wait for it first):
+  // its launch overlaps that kernel's end
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.num_tokens));
+  cfg.blockDim = dim3(kWriteThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
   if (p.cache_dtype == p.src_dtype) {
     const int elt = p.cache_dtype == kF32 ? 4 : p.cache_dtype == kBF16 ? 2 : 1;
-    cache_write_copy_kernel<<<grid, kWriteThreads, 0, stream>>>(p, elt);
+    e = cudaLaunchKernelEx(&cfg, cache_write_copy_kernel, p, elt);
   } else if (p.src_dtype == kBF16) {
-    cache_write_e4m3_kernel<BF16><<<grid, kWriteThreads, 0, stream>>>(p);
+    e = cudaLaunchKernelEx(&cfg, cache_write_e4m3_kernel<BF16>, p);
   } else {
-    cache_write_e4m3_kernel<F32><<<grid, kWriteThreads, 0, stream>>>(p);
+    e = cudaLaunchKernelEx(&cfg, cache_write_e4m3_kernel<F32>, p);
   }
   note_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_copy_blocks(const CopyBlocksParams& p, cudaStream_t stream) {

@@ -118,6 +118,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_split_rows_kernel(const D
       merge_smem + merge_cum_bytes(S), merge::rows_per_block(S * tiles, gridDim.x));
   merge::plan<kMergeThreads>(p, cum, split, sc, blockIdx.x, gridDim.x);
   asm volatile("griddepcontrol.wait;" ::: "memory");  // every partial of the main kernel is visible
+  // the next kernel on the stream may launch now: it waits for this grid before it
+  // touches memory
+  asm volatile("griddepcontrol.launch_dependents;");
   if (T == 0) return;
   merge::fold<kMergeThreads>(p, split, sc, blockIdx.x, gridDim.x);
 }
@@ -228,35 +231,76 @@ static size_t mma_smem_bytes(const DecodeParams& p, int G, bool fused_append) {
   return 0;
 }
 
-bool mma_fused_append_fits(const DecodeParams& p) {
-  const size_t smem = mma_smem_bytes(p, mma_heads_per_item(p.group), true);
-  return smem > 0 && smem <= 227 * 1024;
+bool mma_fused_append_fits(const DecodeParams& p) { return mma_seqs_per_launch(p, true) == p.num_seqs; }
+
+// Whether a launch over `S` sequences fits: the main kernel's per-sequence offsets in
+// its shared memory, the merge kernel's offsets and scratch in the default 48 KB, the
+// flattened (sequence, head group, token) space in 31 bits.
+static bool mma_launch_fits(const DecodeParams& p, int G, int S, bool fused_append) {
+  if (S < 1) return false;
+  const int64_t max_ctx = int64_t(p.max_blocks_per_seq) * p.block_size;
+  if (int64_t(S) * (max_ctx + 16) * (p.num_heads / G) >= (int64_t(1) << 31)) return false;
+  DecodeParams q = p;
+  q.num_seqs = S;
+  const size_t smem = mma_smem_bytes(q, G, fused_append);
+  // (the kernel's own static shared memory comes on top of the dynamic part)
+  if (smem == 0 || smem + 1024 > 227 * 1024) return false;
+  return p.grid >= 1 && merge_smem_bytes(S, G, p.num_heads, p.grid) <= 46 * 1024;
+}
+
+int mma_seqs_per_launch(const DecodeParams& p, bool fused_append) {
+  const int G = mma_heads_per_item(p.group);
+  if (G == 0 || p.num_seqs < 1) return 0;
+  if (mma_launch_fits(p, G, p.num_seqs, fused_append)) return p.num_seqs;
+  int lo = 0, hi = p.num_seqs;  // the largest S that fits (the needs grow with S)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    if (mma_launch_fits(p, G, mid, fused_append)) lo = mid; else hi = mid - 1;
+  }
+  return lo;
 }
 
 bool mma_decode_supported(const DecodeParams& p) {
   const int G = mma_heads_per_item(p.group);
   if (G == 0 || p.q_dtype != kBF16 || p.out_dtype != kBF16) return false;
   if (!(p.block_size == 8 || p.block_size == 16 || p.block_size == 32)) return false;
-  if (p.num_seqs < 1 || p.num_seqs > 4096) return false;
+  if (p.num_seqs < 1) return false;
   if (!encode_fn()) return false;
   // 8-byte query loads and 4-byte output stores
   if ((reinterpret_cast<uintptr_t>(p.query) & 15) || (p.q_stride_s & 7) || (p.q_stride_h & 7)) return false;
   if ((reinterpret_cast<uintptr_t>(p.out) & 15) || (p.out_stride_s & 7) || (p.out_stride_h & 7)) return false;
-  // the flattened (sequence, head group, token) space must fit in 31 bits
-  const int64_t max_ctx = int64_t(p.max_blocks_per_seq) * p.block_size;
-  if (int64_t(p.num_seqs) * (max_ctx + 16) * (p.num_heads / G) >= (int64_t(1) << 31)) return false;
-  const size_t smem = mma_smem_bytes(p, G, false);
-  if (smem == 0) return false;
-  // the merge kernel's offsets and scratch fit the default 48 KB
-  if (p.grid < 1 || merge_smem_bytes(p.num_seqs, G, p.num_heads, p.grid) > 46 * 1024) return false;
-  return smem > 0 && smem <= 227 * 1024;
+  // larger batches run as several launches over ranges of sequences
+  return mma_seqs_per_launch(p, false) >= 1;
 }
 
 cudaError_t launch_decode_mma_main(const DecodeParams& p, cudaStream_t stream) {
   return p.fused_append ? launch_decode_mma_main_append(p, stream) : launch_main<false>(p, stream);
 }
 
-cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_decode_mma(const DecodeParams& all, cudaStream_t stream) {
+  // A batch whose per-sequence offsets do not fit one launch runs as launches over
+  // consecutive ranges of sequences, in stream order (each launch leaves the claim
+  // counters at zero for the next; each waits for the one before it).
+  const int chunk = mma_seqs_per_launch(all, all.fused_append);
+  // (the fused append is only chosen when the whole batch fits one launch)
+  if (chunk < 1 || (all.fused_append && chunk < all.num_seqs)) return cudaErrorInvalidValue;
+  for (int s0 = 0; s0 < all.num_seqs; s0 += chunk) {
+    DecodeParams p = all;
+    p.num_seqs = all.num_seqs - s0 < chunk ? all.num_seqs - s0 : chunk;
+    if (s0 > 0) {
+      p.overlap_prologue = false;  // its predecessor is the previous range's merge
+      p.query = static_cast<const uint16_t*>(all.query) + int64_t(s0) * all.q_stride_s;
+      p.out = static_cast<uint16_t*>(all.out) + int64_t(s0) * all.out_stride_s;
+      p.block_tables = all.block_tables + int64_t(s0) * all.bt_stride;
+      p.context_lens = all.context_lens + s0;
+    }
+    const cudaError_t e = launch_decode_mma_range(p, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode_mma_range(const DecodeParams& p, cudaStream_t stream) {
   cudaError_t e = launch_decode_mma_main(p, stream);
   if (e != cudaSuccess) return e;
   // programmatic dependent launch: the merge grid is queued behind the main one and

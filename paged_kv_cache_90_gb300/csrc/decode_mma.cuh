@@ -271,7 +271,14 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
   const int tiles = p.num_heads / G;
   const Geometry geo{cum, lens, tiles, p.group / G, max_ctx, p.sliding_window, p.block_size};
 
-  // the merge kernel behind this one may be scheduled now (it waits for our writes)
+  // Every launch is a programmatic dependent of the kernel before it on the stream, so
+  // that its launch overlaps that kernel's end.  Unless that kernel is this library's
+  // cache write queued by the same call (which produces none of the inputs read before
+  // the later wait, and lets this grid launch only once its own predecessor is done),
+  // nothing is read before the predecessor has completed.
+  if (!p.overlap_prologue) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the merge kernel behind this one may be scheduled now (it reads only inputs before
+  // it waits for this grid's results)
   asm volatile("griddepcontrol.launch_dependents;");
 
   // ---- prologue: flattened offsets of the sequences; zero rows for empty ones ------

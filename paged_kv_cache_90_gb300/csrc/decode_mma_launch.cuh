@@ -48,7 +48,7 @@ cudaError_t launch_tpl(const DecodeParams& p, cudaStream_t stream) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = p.overlap_prologue ? 1 : 0;
+  cfg.numAttrs = 1;  // the kernel waits for its predecessor itself (see the kernel's start)
   e = cudaLaunchKernelEx(&cfg, kern, mk, mv, p);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();

@@ -107,9 +107,10 @@ struct DecodeParams {
   int dyn_chunk;             // fewest stages per run-time unit
   int dyn_units_max;         // most run-time units (bounds the partial slots)
   int* work_ctr;             // [2]: next run-time unit, warps finished; zero between launches
-  // host only: launch the main kernel as a programmatic dependent of the kernel before
-  // it on the stream (set only when that kernel is this library's cache write, whose
-  // own launch ordered it after everything the caller queued)
+  // the main kernel may read its inputs before its predecessor on the stream has
+  // completed (set only when that kernel is this library's cache write queued by the
+  // same call, which writes none of them and was itself ordered after everything the
+  // caller queued); otherwise it waits for the predecessor first
   bool overlap_prologue;
 };
 
@@ -148,6 +149,10 @@ bool mma_fused_append_fits(const DecodeParams& p);
 inline int mma_block_warps(int kv_dtype) { return kv_dtype == kE4M3 ? 12 : 8; }
 constexpr int kMmaMaxWarps = 12;
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream);
+// one launch pair (main + merge) over all of p's sequences, which must fit one launch
+cudaError_t launch_decode_mma_range(const DecodeParams& p, cudaStream_t stream);
+// most sequences one launch of the tensor-core kernel takes (shared-memory offsets)
+int mma_seqs_per_launch(const DecodeParams& p, bool fused_append);
 // Prefill (prefill_mma.cuh, launched from decode_mma.cu): whether it handles a call,
 // and its launch.
 bool prefill_supported(const DecodeParams& p);

@@ -4,27 +4,32 @@
 // Sequence s holds L cached tokens, the last n of them new (written by the cache write
 // first); new token i sits at position L - n + i and attends to positions 0 .. itself.
 //
-// One thread block takes 128 query rows: TQ = 128 / GP new tokens of one sequence times
-// the GP query heads of one KV head's group that share the block, row r = token r / GP,
-// head r % GP, so every K/V tile it streams serves all GP heads.  Per tile of 128 keys:
-//   S = Q K^T      M = 128 rows, N = 128 keys, K = head_dim: Q and K from shared memory
-//                  (K-major, 128-byte swizzle), S in tensor memory (f32)
-//   P = 2^(S * scale * log2 e - m)   one row per thread of the softmax warpgroup, read
-//                  from tensor memory and written back over S as bf16 pairs
-//   O += P V       M = 128, N = head_dim, K = 128 keys: P from tensor memory, V from
-//                  shared memory (its rows are keys: MN-major), O in tensor memory
-// S is double-buffered, so the MMAs of tile j + 1's scores run while the softmax of tile
-// j does.  The running max m moves (and O is rescaled in tensor memory) only when a row's
-// max grows by more than 2^8, as in the decode kernel.
+// One thread block takes two query tiles A and B of 128 rows each: tile t holds TQ =
+// 128 / GP new tokens of one sequence times the GP query heads of one KV head's group
+// (row r = token t * TQ + r / GP, head r % GP), so every K/V tile the block streams
+// serves 2 x 128 rows.  Per tile j of 128 keys and query tile t:
+//   S_t = Q_t K_j^T     M = 128, N = 128 keys, K = head_dim: Q and K from shared memory
+//                       (K-major, 128-byte swizzle), S_t in tensor memory (f32)
+//   P_t = 2^(S_t * scale * log2 e - m)   one row per thread of t's softmax warpgroup,
+//                       read from tensor memory and written back over S_t as bf16 pairs
+//   O_t += P_t V_j      M = 128, N = head_dim, K = 128 keys: P_t from tensor memory, V
+//                       from shared memory (its rows are keys: MN-major), O_t in tensor
+//                       memory
+// The MMAs are issued as S_A(j), S_B(j), then PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), ...,
+// so that while one tile's softmax runs the tensor cores work on the other tile, and
+// each K/V tile is read once for both.  The running max m moves (and O_t is rescaled in
+// tensor memory) only when a row's max grows by more than 2^8, as in the decode kernel.
 //
-// Warps: 0 allocates tensor memory and streams Q once and K and V tiles (two-deep rings
-// each, TMA tensor copies with 128-byte swizzle, one box per block or 16 slots of a
-// block); 1 issues the MMAs (one thread); 4-7 are the softmax warpgroup, warp 4 + q
-// owning tensor-memory lanes 32q .. 32q + 31 (rows).  Keys past the context in the last
-// tile are cut from the scores and their value rows zeroed in shared memory before the
-// value MMA (a stale slot may hold a NaN).  Every wait is bounded; on a timeout the block
-// sets an error bit and an abort flag, every role stops, the copies and MMAs in flight
-// are waited for and the tensor memory is freed.
+// Warps: 0 allocates tensor memory and streams Q once and K and V tiles (two-deep rings,
+// K one tile ahead of V; TMA tensor copies with 128-byte swizzle, one box per block or
+// per 16 slots of a block, issued by the warp's lanes); 1 issues the MMAs (one thread);
+// 4-7 are the softmax warpgroup, which takes tile A's scores then tile B's for every key
+// tile, warp w owning tensor-memory lanes 32 (w % 4) .. 32 (w % 4) + 31 and a thread
+// holding its row's 128 scores in registers.  Keys past the context in the last tile are cut
+// from the scores and their value rows zeroed in shared memory before the value MMAs (a
+// stale slot may hold a NaN).  Every wait is bounded; on a timeout the block sets an
+// error bit and an abort flag, every role stops, the copies and MMAs in flight are
+// waited for and the tensor memory is freed.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -36,9 +41,10 @@
 namespace pkv {
 namespace prefill_tc {
 
-constexpr int kBM = 128;          // query rows per block
+constexpr int kBM = 128;          // query rows per tile
 constexpr int kBN = 128;          // keys per tile
-constexpr int kThreads = 256;
+constexpr int kWarps = 8;  // (2 warps per scheduler: a softmax row of 128 scores fits in registers)
+constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kTmemCols = 512;
 
 template <int D>
@@ -46,17 +52,19 @@ struct Cfg {
   static constexpr int kHalves = D / 64;                 // 128-byte rows of a 64-column half
   static constexpr uint32_t kHalfBytes = kBM * 128;      // one half of a 128-row operand: 16 KB
   static constexpr uint32_t kOpBytes = kHalves * kHalfBytes;
-  // from the 1024-aligned base: Q | K[2] | V[2] | barriers | table entries
+  // from the 1024-aligned base: Q[2] | K[2] | V[2] | barriers | table entries
   static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kOpBytes;
+  static constexpr uint32_t kK = 2 * kOpBytes;
   static constexpr uint32_t kV = kK + 2 * kOpBytes;
   static constexpr uint32_t kBar = kV + 2 * kOpBytes;
   static constexpr uint32_t kTable = kBar + 256;
   static size_t smem_bytes(int entries) { return kTable + size_t(entries) * 4 + 1024; }
+  // tensor memory: S_A, S_B (128 columns each), then O_A, O_B (D columns each)
+  static constexpr uint32_t kS = 0, kO = 2 * kBN;
 };
 
-enum Bar { kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5, kVEmpty = 7, kSFull = 9, kPFull = 11, kSFree = 13,
-           kODone = 15, kDrain = 16, kNumBars = 17 };
+enum Bar { kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5, kVEmpty = 7, kSFull = 9, kPFull = 11, kODone = 13,
+           kDrain = 15, kNumBars = 16 };
 
 // Bounded wait that also gives up when another role has aborted.
 __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -68,12 +76,27 @@ __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, volatile in
   return false;
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+
 template <int D, int GP>
 __global__ void __launch_bounds__(kThreads, 1)
 paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                         const __grid_constant__ CUtensorMap tmv, const DecodeParams p) {
   using C = Cfg<D>;
-  constexpr int TQ = kBM / GP;  // new tokens per block
+  constexpr int TQ = kBM / GP;  // new tokens per query tile; a block takes 2 TQ
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
@@ -86,8 +109,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_co
   const int kvh = h0 / p.group;
   const int S = p.num_seqs;
 
-  // ---- the block's (sequence, tile): sequence s has ceil(n_s / TQ) tiles; blocks run over
-  // them sequence by sequence, each sequence's last (longest) tile first
+  // ---- the block's (sequence, tile pair): sequence s has ceil(n_s / 2 TQ) of them;
+  // blocks run over them sequence by sequence, each sequence's last (longest) first
   if (warp == 0) {
     int base = 0, found = 0;
     for (int s0 = 0; s0 < S && !found; s0 += 32) {
@@ -95,7 +118,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_co
       int nt = 0;
       if (s < S) {
         const int n = p.query_start_loc[s + 1] - p.query_start_loc[s];
-        nt = n > 0 ? (n + TQ - 1) / TQ : 0;
+        nt = n > 0 ? (n + 2 * TQ - 1) / (2 * TQ) : 0;
       }
       int incl = nt;
 #pragma unroll
@@ -116,19 +139,20 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_co
   }
   __syncthreads();
   const int s = item[0];
-  if (s < 0) return;  // beyond the last tile (the grid is an upper bound)
+  if (s < 0) return;  // beyond the last tile pair (the grid is an upper bound)
   const int t = item[1];
   const int max_ctx = p.max_blocks_per_seq * p.block_size;
   const int L = p.context_lens[s];
   const int q0 = p.query_start_loc[s];
   const int n = p.query_start_loc[s + 1] - q0;
   if (L < 0 || L > max_ctx || n > L) {
-    if (tid == 0 && blockIdx.y == 0 && t == (n + TQ - 1) / TQ - 1) raise_device_error(p.err, kErrContextLen);
+    if (tid == 0 && blockIdx.y == 0 && t == (n + 2 * TQ - 1) / (2 * TQ) - 1) raise_device_error(p.err, kErrContextLen);
     return;
   }
-  const int tq0 = t * TQ;                  // first new token of the block, within the chunk
+  const int tq0 = t * 2 * TQ;              // first new token of the block, within the chunk
   const int P0 = L - n + tq0;              // its position
-  const int nq = min(TQ, n - tq0);
+  const int nq = min(2 * TQ, n - tq0);     // the block's new tokens
+  const bool twoB = nq > TQ;               // tile B holds rows
   const int kv_end = P0 + nq;              // keys any row of the block sees: [0, kv_end)
   const int ntiles = (kv_end + kBN - 1) / kBN;
   const int bs = p.block_size;
@@ -153,50 +177,48 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_co
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tO = tmem + 2 * kBN;
   const uint32_t sbase = smem_addr(smem);
 
   if (warp == 0) {
-    // ---- copies: Q once, then K and V of tile j into slot j % 2 ---------------------
+    // ---- copies: Q of both tiles once, then K_j and V_j into slot j % 2, K one tile
+    // ahead (K_0, K_1, V_0, K_2, V_1, ...); lane i issues copy i of a tile ----------
     if (lane == 0) {
-      mbar_arrive_expect_tx(&bars[kQFull], C::kOpBytes);
-      for (int h = 0; h < C::kHalves; ++h)
-        asm volatile(
-            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-            "[%0], [%1, {%2, %3, %4}], [%5];"
-            ::"r"(sbase + C::kQ + h * C::kHalfBytes), "l"(reinterpret_cast<uint64_t>(&tmq)), "r"(64 * h), "r"(h0),
-              "r"(q0 + tq0), "r"(smem_addr(&bars[kQFull]))
-            : "memory");
-      const int box = bs < 16 ? bs : 16;
-      int kissued = 0, vissued = 0;
-      for (int j = 0; j < ntiles && !*abort_flag; ++j) {
-        const int slot = j & 1;
-        const int j0 = j * kBN;
-        const int nrows = min(kBN, kv_end - j0);          // keys of the tile in the context
-        const int nbox = (nrows + box - 1) / box;
-        const uint32_t bytes = uint32_t(nbox) * box * 128u * C::kHalves;
-        for (int tensor = 0; tensor < 2; ++tensor) {      // K, then V
-          const int eb = tensor ? kVEmpty : kKEmpty, fb = tensor ? kVFull : kKFull;
-          if (j >= 2 && !wait(&bars[eb + slot], uint32_t((j - 2) >> 1) & 1u, abort_flag)) break;
-          mbar_arrive_expect_tx(&bars[fb + slot], bytes);
-          const uint32_t dst = sbase + (tensor ? C::kV : C::kK) + slot * C::kOpBytes;
-          const uint64_t map = reinterpret_cast<uint64_t>(tensor ? &tmv : &tmk);
-          const uint32_t bar = smem_addr(&bars[fb + slot]);
-          for (int b = 0; b < nbox; ++b) {
-            const int key = j0 + b * box;
-            const int blk = tbl[key / bs];
-            for (int h = 0; h < C::kHalves; ++h)
-              asm volatile(
-                  "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-                  "[%0], [%1, {%2, %3, %4, %5}], [%6];"
-                  ::"r"(dst + h * C::kHalfBytes + uint32_t(b * box * 128)), "l"(map), "r"(64 * h),
-                    "r"(key & (bs - 1)), "r"(kvh), "r"(blk), "r"(bar)
-                  : "memory");
-          }
-          if (tensor) ++vissued; else ++kissued;
-        }
+      mbar_arrive_expect_tx(&bars[kQFull], (twoB ? 2u : 1u) * C::kOpBytes);
+      for (int qt = 0; qt < (twoB ? 2 : 1); ++qt)
+        for (int h = 0; h < C::kHalves; ++h)
+          tma_load_3d(sbase + C::kQ + qt * C::kOpBytes + h * C::kHalfBytes, &tmq, 64 * h, h0, q0 + tq0 + qt * TQ,
+                      smem_addr(&bars[kQFull]));
+    }
+    const int box = bs < 16 ? bs : 16;
+    int kissued = 0, vissued = 0;
+    auto load = [&](int j, int tensor) -> bool {  // K (0) or V (1) of tile j
+      const int slot = j & 1;
+      const int j0 = j * kBN;
+      const int nbox = (min(kBN, kv_end - j0) + box - 1) / box;
+      const int eb = tensor ? kVEmpty : kKEmpty, fb = tensor ? kVFull : kKFull;
+      bool ok = true;
+      if (lane == 0 && j >= 2) ok = wait(&bars[eb + slot], uint32_t((j - 2) >> 1) & 1u, abort_flag);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+      if (lane == 0) mbar_arrive_expect_tx(&bars[fb + slot], uint32_t(nbox) * box * 128u * C::kHalves);
+      __syncwarp();
+      const uint32_t dst = sbase + (tensor ? C::kV : C::kK) + slot * C::kOpBytes;
+      const CUtensorMap* map = tensor ? &tmv : &tmk;
+      for (int i = lane; i < nbox * C::kHalves; i += 32) {
+        const int bx = i / C::kHalves, h = i % C::kHalves;
+        const int key = j0 + bx * box;
+        tma_load_4d(dst + h * C::kHalfBytes + uint32_t(bx * box * 128), map, 64 * h, key & (bs - 1), kvh,
+                    tbl[key / bs], smem_addr(&bars[fb + slot]));
       }
-      // the copies in flight land before the block may exit
+      if (tensor) ++vissued; else ++kissued;
+      return true;
+    };
+    bool ok = load(0, 0);
+    for (int j = 0; ok && j < ntiles && !*abort_flag; ++j) {
+      if (j + 1 < ntiles) ok = load(j + 1, 0);
+      if (ok) ok = load(j, 1);
+    }
+    // the copies in flight land before the block may exit
+    if (lane == 0) {
       for (int j = kissued - 2 < 0 ? 0 : kissued - 2; j < kissued; ++j)
         (void)mbar_wait_bounded(&bars[kKFull + (j & 1)], uint32_t(j >> 1) & 1u);
       for (int j = vissued - 2 < 0 ? 0 : vissued - 2; j < vissued; ++j)
@@ -207,39 +229,49 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_co
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16(kBM, kBN, 0, 0);
       constexpr uint32_t idO = tc::idesc_bf16(kBM, D, 0, 1);
+      const int ntile_q = twoB ? 2 : 1;
       bool ok = wait(&bars[kQFull], 0, abort_flag);
-      auto pv = [&](int i) -> bool {  // O += P_i V_i
-        const int b = i & 1;
-        if (!wait(&bars[kPFull + b], uint32_t(i >> 1) & 1u, abort_flag)) return false;
-        if (!wait(&bars[kVFull + b], uint32_t(i >> 1) & 1u, abort_flag)) return false;
+      auto scores = [&](int qt, int j) -> bool {  // S_qt = Q_qt K_j^T
+        if (j >= 1 && !wait(&bars[kODone + qt], uint32_t(j - 1) & 1u, abort_flag)) return false;  // P_qt read
         tc::fence_after();
-        const uint32_t vaddr = sbase + C::kV + b * C::kOpBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          tc::mma_ts(tO, (tmem + uint32_t(b) * kBN) + 8 * kk, tc::desc_sw128(vaddr + kk * 16 * 128, C::kHalfBytes, 1024), idO,
-                     (i > 0 || kk > 0) ? 1u : 0u);
-        tc::commit(&bars[kODone]);
-        tc::commit(&bars[kSFree + b]);
-        tc::commit(&bars[kVEmpty + b]);
-        return true;
-      };
-      for (int j = 0; ok && j < ntiles; ++j) {
-        const int b = j & 1;
-        if (!wait(&bars[kKFull + b], uint32_t(j >> 1) & 1u, abort_flag)) { ok = false; break; }
-        if (j >= 2 && !wait(&bars[kSFree + b], uint32_t((j - 2) >> 1) & 1u, abort_flag)) { ok = false; break; }
-        tc::fence_after();
-        const uint32_t kaddr = sbase + C::kK + b * C::kOpBytes;
+        const uint32_t kaddr = sbase + C::kK + (j & 1) * C::kOpBytes;
+        const uint32_t qaddr = sbase + C::kQ + qt * C::kOpBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-          tc::mma_ss((tmem + uint32_t(b) * kBN), tc::desc_sw128(sbase + C::kQ + off, 16, 1024), tc::desc_sw128(kaddr + off, 16, 1024),
-                     idS, kk > 0 ? 1u : 0u);
+          tc::mma_ss(tmem + C::kS + qt * kBN, tc::desc_sw128(qaddr + off, 16, 1024),
+                     tc::desc_sw128(kaddr + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
         }
-        tc::commit(&bars[kSFull + b]);
-        tc::commit(&bars[kKEmpty + b]);
-        if (j >= 1 && !pv(j - 1)) { ok = false; break; }
+        tc::commit(&bars[kSFull + qt]);
+        return true;
+      };
+      auto values = [&](int qt, int j) -> bool {  // O_qt += P_qt V_j
+        if (!wait(&bars[kPFull + qt], uint32_t(j) & 1u, abort_flag)) return false;
+        tc::fence_after();
+        const uint32_t vaddr = sbase + C::kV + (j & 1) * C::kOpBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          tc::mma_ts(tmem + C::kO + qt * D, tmem + C::kS + qt * kBN + 8 * kk,
+                     tc::desc_sw128(vaddr + kk * 16 * 128, C::kHalfBytes, 1024), idO, (j > 0 || kk > 0) ? 1u : 0u);
+        tc::commit(&bars[kODone + qt]);
+        return true;
+      };
+      auto kfull = [&](int j) { return wait(&bars[kKFull + (j & 1)], uint32_t(j >> 1) & 1u, abort_flag); };
+      if (ok) ok = kfull(0);
+      for (int qt = 0; ok && qt < ntile_q; ++qt) ok = scores(qt, 0);
+      if (ok) tc::commit(&bars[kKEmpty + 0]);
+      for (int j = 0; ok && j < ntiles; ++j) {
+        if (!(ok = wait(&bars[kVFull + (j & 1)], uint32_t(j >> 1) & 1u, abort_flag))) break;
+        const bool more = j + 1 < ntiles;
+        if (more && !(ok = kfull(j + 1))) break;
+        for (int qt = 0; ok && qt < ntile_q; ++qt) {
+          ok = values(qt, j);
+          if (ok && more) ok = scores(qt, j + 1);
+        }
+        if (!ok) break;
+        tc::commit(&bars[kVEmpty + (j & 1)]);
+        if (more) tc::commit(&bars[kKEmpty + ((j + 1) & 1)]);
       }
-      if (ok) ok = pv(ntiles - 1);
       // every MMA issued has completed before the tensor memory is freed
       tc::commit(&bars[kDrain]);
       (void)mbar_wait_bounded(&bars[kDrain], 0);
@@ -249,103 +281,127 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_co
       }
     }
   } else if (warp >= 4) {
-    // ---- softmax warpgroup: row r = 32 (warp - 4) + lane -----------------------------
-    const int q = warp - 4;
+    // ---- softmax warpgroup: tile A then tile B of every key tile; row r = 32 (warp % 4)
+    // + lane (a warp reaches the tensor-memory lanes of its warp index mod 4) ---------
+    const int q = warp & 3;
     const int r = 32 * q + lane;
     const uint32_t lane_off = uint32_t(32 * q) << 16;
-    const int tok = r / GP;
-    const int qpos = P0 + tok;               // this row's position (rows past nq: unused)
     const float sl = p.qk_scale_log2;
-    float m_ref = -INFINITY, l_run = 0.f;
+    const int ntile_q = twoB ? 2 : 1;
+    float m_ref[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
-      const int b = j & 1;
-      if (!wait(&bars[kSFull + b], uint32_t(j >> 1) & 1u, abort_flag)) { ok = false; break; }
-      tc::fence_after();
+    for (int j = 0; ok && j < ntiles; ++j) {
       const int j0 = j * kBN;
-      float v[kBN];
+      for (int qt = 0; qt < ntile_q; ++qt) {
+        const uint32_t tS = tmem + C::kS + qt * kBN + lane_off;
+        const uint32_t tO = tmem + C::kO + qt * D + lane_off;
+        const int qpos = P0 + qt * TQ + r / GP;  // the row's position (rows past nq: unused)
+        if (!wait(&bars[kSFull + qt], uint32_t(j) & 1u, abort_flag)) { ok = false; break; }
+        tc::fence_after();
+        const bool cut = j0 + kBN - 1 > P0 + qt * TQ || j0 + kBN > kv_end;  // some key masked
+        // the row's scores (keys after the row's position or past the context cut; a
+        // stale key may be NaN), all loaded before one wait, and their max
+        float v[kBN];
+        {
+          uint32_t w[kBN / 32][32];
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t w[32];
-        tc::ld32((tmem + uint32_t(b) * kBN) + lane_off + 32 * c, w);
-        tc::wait_ld();
+          for (int c = 0; c < kBN / 32; ++c) tc::ld32(tS + 32 * c, w[c]);
+          tc::wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[32 * c + i] = __uint_as_float(w[i]);
-      }
-      // cut keys after the row's position or past the context (a stale key may be NaN)
-      if (j0 + kBN - 1 > P0 || j0 + kBN > kv_end) {
+          for (int c = 0; c < kBN / 32; ++c)
 #pragma unroll
-        for (int i = 0; i < kBN; ++i)
-          if (j0 + i > qpos || j0 + i >= kv_end) v[i] = -INFINITY;
-      }
-      float mx = v[0];
+            for (int i = 0; i < 32; ++i) v[32 * c + i] = __uint_as_float(w[c][i]);
+        }
+        if (cut) {
 #pragma unroll
-      for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, v[i]);
-      mx *= sl;
-      if (mx > m_ref + mma::kRescaleGap || (m_ref == -INFINITY && mx != -INFINITY)) {
-        if (j > 0 && m_ref != -INFINITY) {
-          // O holds tile j - 1's product once its MMAs are done: rescale it in place
-          if (!wait(&bars[kODone], uint32_t(j - 1) & 1u, abort_flag)) { ok = false; break; }
-          tc::fence_after();
-          const float alpha = fast_exp2(m_ref - mx);
+          for (int i = 0; i < kBN; ++i)
+            if (j0 + i > qpos || j0 + i >= kv_end) v[i] = -INFINITY;
+        }
+        float t8[8];
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t w[32];
-            tc::ld32(tO + lane_off + 32 * c, w);
-            tc::wait_ld();
+        for (int k = 0; k < 8; ++k) t8[k] = v[k];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
-            tc::st32(tO + lane_off + 32 * c, w);
+        for (int i = 8; i < kBN; i += 8)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) t8[k] = fmaxf(t8[k], v[i + k]);
+        float mx = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])), fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+        mx *= sl;
+        if (mx > m_ref[qt] + mma::kRescaleGap || (m_ref[qt] == -INFINITY && mx != -INFINITY)) {
+          if (j > 0 && m_ref[qt] != -INFINITY) {
+            // O_qt holds tile j - 1's product (its MMAs completed before S_qt(j) was
+            // issued): rescale it in place
+            const float alpha = fast_exp2(m_ref[qt] - mx);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t w[32];
+              tc::ld32(tO + 32 * c, w);
+              tc::wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
+              tc::st32(tO + 32 * c, w);
+            }
+            tc::wait_st();
+            l_run[qt] *= alpha;
           }
-          tc::wait_st();
-          l_run *= alpha;
+          m_ref[qt] = mx;
         }
-        m_ref = mx;
-      }
-      const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-      // the last tile's value rows past the context are zeroed before the value MMA
-      if (j0 + kBN > kv_end) {
-        if (!wait(&bars[kVFull + b], uint32_t(j >> 1) & 1u, abort_flag)) { ok = false; break; }
-        const int first_bad = kv_end - j0;
-        unsigned char* vt = smem + C::kV + b * C::kOpBytes;
-        for (int i = tid - 128; i < (kBN - first_bad) * 8 * C::kHalves; i += 128) {
-          const int h = i / ((kBN - first_bad) * 8), rem = i % ((kBN - first_bad) * 8);
-          *reinterpret_cast<uint4*>(vt + h * C::kHalfBytes + (first_bad + rem / 8) * 128 + (rem % 8) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
+        const float mu = m_ref[qt] == -INFINITY ? 0.f : m_ref[qt];
+        // the last tile's value rows past the context are zeroed before its value MMAs
+        if (qt == 0 && j0 + kBN > kv_end) {
+          if (!wait(&bars[kVFull + (j & 1)], uint32_t(j >> 1) & 1u, abort_flag)) { ok = false; break; }
+          const int first_bad = kv_end - j0;
+          unsigned char* vt = smem + C::kV + (j & 1) * C::kOpBytes;
+          for (int i = tid - 128; i < (kBN - first_bad) * 8 * C::kHalves; i += 128) {
+            const int h = i / ((kBN - first_bad) * 8), rem = i % ((kBN - first_bad) * 8);
+            *reinterpret_cast<uint4*>(vt + h * C::kHalfBytes + (first_bad + rem / 8) * 128 + (rem % 8) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
-      }
-      float psum = 0.f;
+        // weights, written back over S as bf16 pairs
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t w[16];
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float a = fast_exp2(v[32 * c + 2 * i] * sl - mu), bb = fast_exp2(v[32 * c + 2 * i + 1] * sl - mu);
-          psum += a + bb;
-          const __nv_bfloat162 pr = __floats2bfloat162_rn(a, bb);
-          w[i] = *reinterpret_cast<const uint32_t*>(&pr);
+          for (int i = 0; i < 16; ++i) {
+            const float a = fast_exp2(fmaf(v[32 * c + 2 * i], sl, -mu));
+            const float bb = fast_exp2(fmaf(v[32 * c + 2 * i + 1], sl, -mu));
+            ps[i & 3] += a + bb;
+            const __nv_bfloat162 pr = __floats2bfloat162_rn(a, bb);
+            pk[i] = *reinterpret_cast<const uint32_t*>(&pr);
+          }
+          tc::st16(tS + 16 * c, pk);
         }
-        tc::st16((tmem + uint32_t(b) * kBN) + lane_off + 16 * c, w);
+        l_run[qt] += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        tc::wait_st();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[kPFull + qt]);
       }
-      l_run += psum;
-      tc::wait_st();
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kPFull + b]);
     }
-    // ---- out = O / l for this row (the barrier is then at most one phase behind) ------
-    if (ok && ntiles >= 2) ok = wait(&bars[kODone], uint32_t(ntiles - 2) & 1u, abort_flag);
-    if (ok && wait(&bars[kODone], uint32_t(ntiles - 1) & 1u, abort_flag)) {
+    // ---- out = O / l for this row of each tile (the last value MMAs of a tile: the
+    // barrier is at most one phase behind, as every earlier one completed before the
+    // tile's last scores) --------------------------------------------------------------
+    for (int qt = 0; qt < ntile_q; ++qt) {
+      if (!(ok && wait(&bars[kODone + qt], uint32_t(ntiles - 1) & 1u, abort_flag))) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          raise_device_error(p.err, kErrTimeout);
+        }
+        break;
+      }
       tc::fence_after();
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      const uint32_t tO = tmem + C::kO + qt * D + lane_off;
+      const int tok = qt * TQ + r / GP;
+      const float inv = l_run[qt] > 0.f ? 1.f / l_run[qt] : 0.f;
       const bool row_ok = tok < nq;
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + int64_t(q0 + tq0 + tok) * p.out_stride_s +
                            int64_t(h0 + r % GP) * p.out_stride_h;
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t w[32];
-        tc::ld32(tO + lane_off + 32 * c, w);
+        tc::ld32(tO + 32 * c, w);
         tc::wait_ld();
         if (row_ok) {
           uint32_t o16[16];
@@ -361,9 +417,6 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_co
                 make_uint4(o16[4 * i], o16[4 * i + 1], o16[4 * i + 2], o16[4 * i + 3]);
         }
       }
-    } else if (lane == 0) {
-      *abort_flag = 1;
-      raise_device_error(p.err, kErrTimeout);
     }
   }
   tc::fence_before();
@@ -433,10 +486,10 @@ cudaError_t launch_prefill_tc_tpl(const DecodeParams& p, cudaStream_t stream) {
       return e;
     if (dev >= 0 && dev < kMapCacheDevices) smem_set[dev] = smem;
   }
-  // one block per (query tile, group of GP heads); the tiles of all sequences number at
-  // most ceil(T / TQ) + S, surplus blocks exit at once
-  constexpr int TQ = prefill_tc::kBM / GP;
-  const dim3 grid(unsigned((p.num_tokens + TQ - 1) / TQ + p.num_seqs), unsigned(p.num_heads / GP));
+  // one block per (pair of query tiles, group of GP heads); the pairs of all sequences
+  // number at most ceil(T / 2 TQ) + S, surplus blocks exit at once
+  constexpr int TQ2 = 2 * (prefill_tc::kBM / GP);  // new tokens per block
+  const dim3 grid(unsigned((p.num_tokens + TQ2 - 1) / TQ2 + p.num_seqs), unsigned(p.num_heads / GP));
   kern<<<grid, prefill_tc::kThreads, smem, stream>>>(mq, mk, mv, p);
   note_launch();
   return cudaGetLastError();

@@ -793,10 +793,10 @@ def test_prefill_over_prefix_cached_blocks(bs, pkernel):
 
 @pytest.mark.parametrize("kv", ["bf16", "e4m3"])
 def test_largest_batch_of_the_tensor_core_kernel(kv, kernel):
-    """4096 sequences (the most the tensor-core kernel takes: its per-sequence offsets
-    fill shared memory) of 1 to 40 tokens, unused slots NaN; steps as write + decode,
-    joint, and with the in-kernel append forced (which falls back to two launches when
-    its staged tokens no longer fit)."""
+    """4096 sequences (about the most one launch of the 16-bit tensor-core kernel takes:
+    its per-sequence offsets fill shared memory) of 1 to 40 tokens, unused slots NaN;
+    steps as write + decode, joint, and with the in-kernel append forced (which falls
+    back to two launches when its staged tokens no longer fit)."""
     w = wl.variable_length_decode(f"max_batch_{kv}", 73, torch.randint(1, 41, (4096,),
                                   generator=torch.Generator().manual_seed(73)).tolist(),
                                   32, 8, 128, 16, kv, poison=True)
@@ -814,20 +814,24 @@ def test_largest_batch_of_the_tensor_core_kernel(kv, kernel):
     assert torch.equal(runs["joint"], runs["forced"])
 
 
-def test_one_sequence_past_the_tensor_core_kernels_batch_limit():
-    """4097 sequences: the library runs the CUDA-core kernel on its own, and refuses the
-    forced tensor-core kernel with PKV_ERR_UNSUPPORTED."""
-    lens = [1 + (i % 23) for i in range(4097)]
-    w = wl.variable_length_decode("past_max_batch", 74, lens, 32, 8, 128, 16, "bf16", poison=True)
-    check_workload(w)
-    dw = DeviceWorkload(w)
+@pytest.mark.parametrize("kv,num_seqs", [("bf16", 4400), ("bf16", 8192), ("e4m3", 12000)])
+def test_batches_past_one_launch_run_as_several(kv, num_seqs):
+    """More sequences than one launch's shared memory holds offsets for: the tensor-core
+    kernel (forced) runs consecutive ranges of sequences as launches of their own, in
+    stream order, and matches the oracle; the automatic choice takes the same path."""
+    lens = [1 + (i * 7 % 37) for i in range(num_seqs)]
+    w = wl.variable_length_decode(f"past_one_launch_{kv}_{num_seqs}", 74, lens, 32, 8, 128, 16, kv, poison=True)
     binding.set_option("decode_kernel", 2)
     try:
-        with pytest.raises(binding.PkvError) as ei:
-            dw.run_step(0)
-        assert ei.value.status == 2
+        n0 = binding.launch_count()
+        check_workload(w)
+        launches = binding.launch_count() - n0
     finally:
         binding.set_option("decode_kernel", 0)
+    assert launches >= 1 + 2 * 2, launches        # the write, then at least two main + merge pairs
+    a = run_device(w)[0]
+    for x, y in zip(a, check_workload(w)[0]):
+        assert torch.equal(x, y)
 
 
 @pytest.mark.parametrize("draw", range(12))
