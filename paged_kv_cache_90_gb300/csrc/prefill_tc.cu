@@ -20,9 +20,9 @@
 // each K/V tile is read once for both.  The running max m moves (and O_t is rescaled in
 // tensor memory) only when a row's max grows by more than 2^8, as in the decode kernel.
 //
-// Warps: 0 allocates tensor memory and streams Q once and K and V tiles (two-deep rings,
-// K one tile ahead of V; TMA tensor copies with 128-byte swizzle, one box per block or
-// per 16 slots of a block, issued by the warp's lanes); 1 issues the MMAs (one thread);
+// Warps: 0 allocates tensor memory and streams Q once and the K tiles, 2 streams the V
+// tiles (two-deep rings; TMA tensor copies with 128-byte swizzle, one box per block or
+// per 16 slots of a block, issued by the warps' lanes); 1 issues the MMAs (one thread);
 // 4-7 are the softmax warpgroup, which takes tile A's scores then tile B's for every key
 // tile, warp w owning tensor-memory lanes 32 (w % 4) .. 32 (w % 4) + 31 and a thread
 // holding its row's 128 scores in registers.  Keys past the context in the last tile are cut
@@ -179,10 +179,12 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_co
   const uint32_t tmem = *tmem_slot;
   const uint32_t sbase = smem_addr(smem);
 
-  if (warp == 0) {
-    // ---- copies: Q of both tiles once, then K_j and V_j into slot j % 2, K one tile
-    // ahead (K_0, K_1, V_0, K_2, V_1, ...); lane i issues copy i of a tile ----------
-    if (lane == 0) {
+  if (warp == 0 || warp == 2) {
+    // ---- copies: warp 0 streams Q of both tiles once, then K_j into slot j % 2; warp 2
+    // streams V_j (the two run independently, so K runs ahead of V); lane i issues copy
+    // i of a tile (one box of `box` slots x one 64-column half) ----------------------
+    const int tensor = warp == 2;
+    if (!tensor && lane == 0) {
       mbar_arrive_expect_tx(&bars[kQFull], (twoB ? 2u : 1u) * C::kOpBytes);
       for (int qt = 0; qt < (twoB ? 2 : 1); ++qt)
         for (int h = 0; h < C::kHalves; ++h)
@@ -190,40 +192,32 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_co
                       smem_addr(&bars[kQFull]));
     }
     const int box = bs < 16 ? bs : 16;
-    int kissued = 0, vissued = 0;
-    auto load = [&](int j, int tensor) -> bool {  // K (0) or V (1) of tile j
+    const int eb = tensor ? kVEmpty : kKEmpty, fb = tensor ? kVFull : kKFull;
+    const uint32_t region = sbase + (tensor ? C::kV : C::kK);
+    const CUtensorMap* map = tensor ? &tmv : &tmk;
+    int issued = 0;
+    for (int j = 0; j < ntiles && !*abort_flag; ++j) {
       const int slot = j & 1;
       const int j0 = j * kBN;
       const int nbox = (min(kBN, kv_end - j0) + box - 1) / box;
-      const int eb = tensor ? kVEmpty : kKEmpty, fb = tensor ? kVFull : kKFull;
       bool ok = true;
       if (lane == 0 && j >= 2) ok = wait(&bars[eb + slot], uint32_t((j - 2) >> 1) & 1u, abort_flag);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       if (lane == 0) mbar_arrive_expect_tx(&bars[fb + slot], uint32_t(nbox) * box * 128u * C::kHalves);
       __syncwarp();
-      const uint32_t dst = sbase + (tensor ? C::kV : C::kK) + slot * C::kOpBytes;
-      const CUtensorMap* map = tensor ? &tmv : &tmk;
+      const uint32_t dst = region + slot * C::kOpBytes;
       for (int i = lane; i < nbox * C::kHalves; i += 32) {
         const int bx = i / C::kHalves, h = i % C::kHalves;
         const int key = j0 + bx * box;
         tma_load_4d(dst + h * C::kHalfBytes + uint32_t(bx * box * 128), map, 64 * h, key & (bs - 1), kvh,
                     tbl[key / bs], smem_addr(&bars[fb + slot]));
       }
-      if (tensor) ++vissued; else ++kissued;
-      return true;
-    };
-    bool ok = load(0, 0);
-    for (int j = 0; ok && j < ntiles && !*abort_flag; ++j) {
-      if (j + 1 < ntiles) ok = load(j + 1, 0);
-      if (ok) ok = load(j, 1);
+      ++issued;
     }
     // the copies in flight land before the block may exit
-    if (lane == 0) {
-      for (int j = kissued - 2 < 0 ? 0 : kissued - 2; j < kissued; ++j)
-        (void)mbar_wait_bounded(&bars[kKFull + (j & 1)], uint32_t(j >> 1) & 1u);
-      for (int j = vissued - 2 < 0 ? 0 : vissued - 2; j < vissued; ++j)
-        (void)mbar_wait_bounded(&bars[kVFull + (j & 1)], uint32_t(j >> 1) & 1u);
-    }
+    if (lane == 0)
+      for (int j = issued - 2 < 0 ? 0 : issued - 2; j < issued; ++j)
+        (void)mbar_wait_bounded(&bars[fb + (j & 1)], uint32_t(j >> 1) & 1u);
   } else if (warp == 1) {
     // ---- MMAs (one thread) --------------------------------------------------------
     if (lane == 0) {
