@@ -66,6 +66,21 @@ struct Cfg {
 enum Bar { kQFull = 0, kKFull = 1, kKEmpty = 3, kVFull = 5, kVEmpty = 7, kSFull = 9, kPFull = 11, kODone = 13,
            kDrain = 15, kNumBars = 16 };
 
+// The same, polling without suspending the thread: for the waits on the critical path
+// (the MMA issuer, the softmax), where a suspended thread wakes late.
+__device__ __forceinline__ bool wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  for (uint32_t i = 0; i < (kWaitPolls << 4); ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+    if (done) return true;
+    if ((i & 1023u) == 1023u && *abort) return false;
+  }
+  *abort = 1;
+  return false;
+}
+
 // Bounded wait that also gives up when another role has aborted.
 __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   for (uint32_t i = 0; i < kWaitPolls; ++i) {
@@ -225,8 +240,9 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_co
       constexpr uint32_t idO = tc::idesc_bf16(kBM, D, 0, 1);
       const int ntile_q = twoB ? 2 : 1;
       bool ok = wait(&bars[kQFull], 0, abort_flag);
+      // S_qt(j + 1) overwrites the columns P_qt(j) was read from by the value MMAs issued
+      // just before it: MMAs issued by one thread execute in order, so no wait is needed
       auto scores = [&](int qt, int j) -> bool {  // S_qt = Q_qt K_j^T
-        if (j >= 1 && !wait(&bars[kODone + qt], uint32_t(j - 1) & 1u, abort_flag)) return false;  // P_qt read
         tc::fence_after();
         const uint32_t kaddr = sbase + C::kK + (j & 1) * C::kOpBytes;
         const uint32_t qaddr = sbase + C::kQ + qt * C::kOpBytes;
@@ -240,7 +256,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_co
         return true;
       };
       auto values = [&](int qt, int j) -> bool {  // O_qt += P_qt V_j
-        if (!wait(&bars[kPFull + qt], uint32_t(j) & 1u, abort_flag)) return false;
+        if (!wait_spin(&bars[kPFull + qt], uint32_t(j) & 1u, abort_flag)) return false;
         tc::fence_after();
         const uint32_t vaddr = sbase + C::kV + (j & 1) * C::kOpBytes;
 #pragma unroll
@@ -250,12 +266,12 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_co
         tc::commit(&bars[kODone + qt]);
         return true;
       };
-      auto kfull = [&](int j) { return wait(&bars[kKFull + (j & 1)], uint32_t(j >> 1) & 1u, abort_flag); };
+      auto kfull = [&](int j) { return wait_spin(&bars[kKFull + (j & 1)], uint32_t(j >> 1) & 1u, abort_flag); };
       if (ok) ok = kfull(0);
       for (int qt = 0; ok && qt < ntile_q; ++qt) ok = scores(qt, 0);
       if (ok) tc::commit(&bars[kKEmpty + 0]);
       for (int j = 0; ok && j < ntiles; ++j) {
-        if (!(ok = wait(&bars[kVFull + (j & 1)], uint32_t(j >> 1) & 1u, abort_flag))) break;
+        if (!(ok = wait_spin(&bars[kVFull + (j & 1)], uint32_t(j >> 1) & 1u, abort_flag))) break;
         const bool more = j + 1 < ntiles;
         if (more && !(ok = kfull(j + 1))) break;
         for (int qt = 0; ok && qt < ntile_q; ++qt) {
@@ -290,7 +306,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_co
         const uint32_t tS = tmem + C::kS + qt * kBN + lane_off;
         const uint32_t tO = tmem + C::kO + qt * D + lane_off;
         const int qpos = P0 + qt * TQ + r / GP;  // the row's position (rows past nq: unused)
-        if (!wait(&bars[kSFull + qt], uint32_t(j) & 1u, abort_flag)) { ok = false; break; }
+        if (!wait_spin(&bars[kSFull + qt], uint32_t(j) & 1u, abort_flag)) { ok = false; break; }
         tc::fence_after();
         const bool cut = j0 + kBN - 1 > P0 + qt * TQ || j0 + kBN > kv_end;  // some key masked
         // the row's scores (keys after the row's position or past the context cut; a
