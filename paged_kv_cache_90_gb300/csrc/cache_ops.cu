@@ -26,11 +26,6 @@ struct AmaxAcc {
   __device__ float value() const { return nan ? __uint_as_float(0x7fc00000u) : m; }
 };
 
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t w) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
-  return __half22float2(*reinterpret_cast<const __half2*>(&h));
-}
-
 // Raise amax[h] to x >= 0 (non-negative floats order like their bit patterns, so an
 // integer max is a float max; the NaN pattern used here is above every finite value's).
 __device__ __forceinline__ void raise_amax(float* amax, int h, float x) {
@@ -80,13 +75,13 @@ __global__ void __launch_bounds__(kWriteThreads) cache_write_copy_kernel(const C
           av.add(__uint_as_float(wv[q] << 16));
           av.add(__uint_as_float(wv[q] & 0xffff0000u));
         } else {  // four e4m3 codes per word
+          float fk[4], fv[4];
+          e4m3x4_to_f32x4(wk[q], fk);
+          e4m3x4_to_f32x4(wv[q], fv);
 #pragma unroll
-          for (int b = 0; b < 2; ++b) {
-            const float2 fk = e4m3x2_to_float2(wk[q] >> (16 * b)), fv = e4m3x2_to_float2(wv[q] >> (16 * b));
-            ak.add(fk.x);
-            ak.add(fk.y);
-            av.add(fv.x);
-            av.add(fv.y);
+          for (int b = 0; b < 4; ++b) {
+            ak.add(fk[b]);
+            av.add(fv[b]);
           }
         }
       }

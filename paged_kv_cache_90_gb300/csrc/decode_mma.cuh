@@ -118,12 +118,6 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u), true);
 }
 
-// Two e4m3 codes (low 16 bits) -> f16x2, exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
-  return (uint32_t(h.y) << 16) | uint32_t(h.x);
-}
-
 // ---- compile-time shape of one instance ----------------------------------------------
 template <typename KV, int D, int G>
 struct Cfg {
@@ -741,8 +735,9 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
         const uint32_t kwb[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
 #pragma unroll
         for (int kk = 0; kk < kQKS; ++kk) {
-          const uint32_t a0 = e4m3x2_to_f16x2(kwa[kk]), a2 = e4m3x2_to_f16x2(kwa[kk] >> 16);
-          const uint32_t a1 = e4m3x2_to_f16x2(kwb[kk]), a3 = e4m3x2_to_f16x2(kwb[kk] >> 16);
+          uint32_t a0, a1, a2, a3;
+          e4m3x4_to_f16x2x2(kwa[kk], a0, a2);
+          e4m3x4_to_f16x2x2(kwb[kk], a1, a3);
 #pragma unroll
           for (int ht = 0; ht < kQHT; ++ht)
             mma16816<true>(kk & 1 ? s2[ht] : s[ht], a0, a1, a2, a3, qb[ht][kk][0], qb[ht][kk][1]);
@@ -822,10 +817,11 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
         const uint32_t x0 = (&wv[0].x)[j], x1 = (&wv[1].x)[j], y0 = (&wv[2].x)[j], y1 = (&wv[3].x)[j];
         const uint32_t x01 = __byte_perm(x0, x1, 0x5140), x23 = __byte_perm(x0, x1, 0x7362);
         const uint32_t y01 = __byte_perm(y0, y1, 0x5140), y23 = __byte_perm(y0, y1, 0x7362);
-        const uint32_t a0 = e4m3x2_to_f16x2(x01), a1 = e4m3x2_to_f16x2(x01 >> 16);
-        const uint32_t a2 = e4m3x2_to_f16x2(y01), a3 = e4m3x2_to_f16x2(y01 >> 16);
-        const uint32_t c0 = e4m3x2_to_f16x2(x23), c1 = e4m3x2_to_f16x2(x23 >> 16);
-        const uint32_t c2 = e4m3x2_to_f16x2(y23), c3 = e4m3x2_to_f16x2(y23 >> 16);
+        uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+        e4m3x4_to_f16x2x2(x01, a0, a1);
+        e4m3x4_to_f16x2x2(y01, a2, a3);
+        e4m3x4_to_f16x2x2(x23, c0, c1);
+        e4m3x4_to_f16x2x2(y23, c2, c3);
 #pragma unroll
         for (int ht = 0; ht < kQHT; ++ht) {
           mma16816<true>(o8[2 * j][ht], a0, a1, a2, a3, pb[ht][0], pb[ht][1]);

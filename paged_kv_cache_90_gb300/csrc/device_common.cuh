@@ -36,11 +36,22 @@ struct E4M3 { using storage = uint8_t; static constexpr int bytes = 1; };
 __device__ __forceinline__ float bf16_lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi_to_f32(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Two e4m3 codes (low 16 bits of w) -> two floats, exact (e4m3 -> f16 is exact).
-__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t w) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
-  __half2 hh = *reinterpret_cast<__half2*>(&h);
-  return __half22float2(hh);
+// Four e4m3 codes (a 32-bit word, code 0 in the low byte) -> two f16x2 words, exact
+// (every e4m3 value is an f16 value): codes 0, 1 -> lo and codes 2, 3 -> hi, the lower
+// code in the lower half.  Each 16-bit half of the word goes to the conversion as it is.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi) : "r"(w));
+}
+
+// Four e4m3 codes (a 32-bit word) -> four floats, exact.
+__device__ __forceinline__ void e4m3x4_to_f32x4(uint32_t w, float* f) {
+  uint32_t lo, hi;
+  e4m3x4_to_f16x2x2(w, lo, hi);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
 }
 
 // Expand one 16-byte chunk of stored elements into floats (4, 8 or 16 of them).
@@ -64,13 +75,10 @@ template <> struct Chunk<BF16> {
 template <> struct Chunk<E4M3> {
   static constexpr int n = 16;
   __device__ __forceinline__ static void expand(const uint4& v, float* f) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float2 a = e4m3x2_to_f32x2(w[i]);
-      float2 b = e4m3x2_to_f32x2(w[i] >> 16);
-      f[4 * i + 0] = a.x; f[4 * i + 1] = a.y; f[4 * i + 2] = b.x; f[4 * i + 3] = b.y;
-    }
+    e4m3x4_to_f32x4(v.x, f);
+    e4m3x4_to_f32x4(v.y, f + 4);
+    e4m3x4_to_f32x4(v.z, f + 8);
+    e4m3x4_to_f32x4(v.w, f + 12);
   }
 };
 
@@ -99,14 +107,14 @@ template <> struct SmallLoad<BF16, 4> {
 };
 template <> struct SmallLoad<E4M3, 2> {
   __device__ __forceinline__ static void load(const void* p, float* f) {
-    uint32_t w = *reinterpret_cast<const uint16_t*>(p); float2 a = e4m3x2_to_f32x2(w); f[0] = a.x; f[1] = a.y;
+    float g[4];
+    e4m3x4_to_f32x4(*reinterpret_cast<const uint16_t*>(p), g);
+    f[0] = g[0]; f[1] = g[1];
   }
 };
 template <> struct SmallLoad<E4M3, 4> {
   __device__ __forceinline__ static void load(const void* p, float* f) {
-    uint32_t w = *reinterpret_cast<const uint32_t*>(p);
-    float2 a = e4m3x2_to_f32x2(w), b = e4m3x2_to_f32x2(w >> 16);
-    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    e4m3x4_to_f32x4(*reinterpret_cast<const uint32_t*>(p), f);
   }
 };
 
