@@ -118,6 +118,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_split_rows_kernel(const D
       merge_smem + merge_cum_bytes(S), merge::rows_per_block(S * tiles, gridDim.x));
   merge::plan<kMergeThreads>(p, cum, split, sc, blockIdx.x, gridDim.x);
   asm volatile("griddepcontrol.wait;" ::: "memory");  // every partial of the main kernel is visible
+  // the main grid has completed and no claim is left: zero its claim counter for the
+  // next launch (which waits for this grid before it claims)
+  if (blockIdx.x == 0 && tid == 0) p.work_ctr[0] = 0;
   // the next kernel on the stream may launch now: it waits for this grid before it
   // touches memory
   asm volatile("griddepcontrol.launch_dependents;");
@@ -279,8 +282,8 @@ cudaError_t launch_decode_mma_main(const DecodeParams& p, cudaStream_t stream) {
 
 cudaError_t launch_decode_mma(const DecodeParams& all, cudaStream_t stream) {
   // A batch whose per-sequence offsets do not fit one launch runs as launches over
-  // consecutive ranges of sequences, in stream order (each launch leaves the claim
-  // counters at zero for the next; each waits for the one before it).
+  // consecutive ranges of sequences, in stream order (each range's merge leaves the
+  // claim counter at zero for the next; each launch waits for the one before it).
   const int chunk = mma_seqs_per_launch(all, all.fused_append);
   // (the fused append is only chosen when the whole batch fits one launch)
   if (chunk < 1 || (all.fused_append && chunk < all.num_seqs)) return cudaErrorInvalidValue;
@@ -317,6 +320,8 @@ cudaError_t launch_decode_mma_range(const DecodeParams& p, cudaStream_t stream) 
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, merge_split_rows_kernel, p);
   note_launch();
+  // without the merge the claim counter would stay raised: zero it in stream order
+  if (e != cudaSuccess) (void)cudaMemsetAsync(p.work_ctr, 0, sizeof(int), stream);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

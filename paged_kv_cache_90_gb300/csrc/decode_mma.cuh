@@ -1027,16 +1027,8 @@ paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_co
       (void)mbar_wait_bounded(&bars[j % C::kStages], (j / C::kStages) & 1u);
     __syncwarp();
   }
-  // The last warp to finish zeroes the counters for the next launch: every warp's
-  // claims precede its finish count, so none can claim after the reset.
-  if (lane == 0) {
-    __threadfence();
-    if (atomicAdd(p.work_ctr + 1, 1) == GW - 1) {
-      __threadfence();
-      atomicExch(p.work_ctr, 0);
-      atomicExch(p.work_ctr + 1, 0);
-    }
-  }
+  // (the claim counter is zeroed for the next launch by the merge kernel, once this
+  // grid has completed: no fence or count at this warp's end)
 
 }
 

@@ -106,7 +106,7 @@ struct DecodeParams {
   int dyn_share;             // stages handed out at run time, in 1/1024 of all stages
   int dyn_chunk;             // fewest stages per run-time unit
   int dyn_units_max;         // most run-time units (bounds the partial slots)
-  int* work_ctr;             // [2]: next run-time unit, warps finished; zero between launches
+  int* work_ctr;             // [2]: next run-time unit (word 1 unused); zeroed by the merge kernel
   // the main kernel may read its inputs before its predecessor on the stream has
   // completed (set only when that kernel is this library's cache write queued by the
   // same call, which writes none of them and was itself ordered after everything the

@@ -717,7 +717,7 @@ def work_split():
 def test_tensor_kernel_work_split_settings(share, chunk, work_split):
     """How much of the work warps claim at run time changes which warp runs which
     stages, not the values: every setting matches the oracle, and launches in a row
-    (the kernel zeroes its claim counter for the next one) give identical bits."""
+    (the merge kernel zeroes the claim counter for the next one) give identical bits."""
     work_split(share, chunk)
     check_workload(wl.llama3_8b_decode(seed=31, num_seqs=8, len_range=(1, 900), poison=True))
     check_workload(wl.continuous_batching(block_size=8, kv_dtype="e4m3", num_seqs=24, num_steps=2,
