@@ -120,37 +120,127 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_co
   int* item = reinterpret_cast<int*>(smem + C::kBar + kNumBars * 8 + 8);  // sequence, tile
   int32_t* tbl = reinterpret_cast<int32_t*>(smem + C::kTable);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h0 = blockIdx.y * GP;     // first query head of the block
+  const int HG = p.num_heads / GP;                    // head groups
+  const int npb = int(gridDim.x / unsigned(HG));      // tile-pair slots per head group
+  const int hg = int(blockIdx.x / unsigned(npb));     // the block's head group
+  const int rank = int(blockIdx.x % unsigned(npb));   // and the rank of its tile pair
+  const int h0 = hg * GP;     // first query head of the block
   const int kvh = h0 / p.group;
   const int S = p.num_seqs;
 
-  // ---- the block's (sequence, tile pair): sequence s has ceil(n_s / 2 TQ) of them;
-  // blocks run over them sequence by sequence, each sequence's last (longest) first
+  // ---- the block's (sequence, tile pair): sequence s has ceil(n_s / 2 TQ) of them.
+  // A pair's work grows with the keys its rows see (kv_end: the chunk's first position
+  // plus the pair's end; the last pair ends at L).  Head group by head group (whose
+  // blocks share the K/V tiles of their KV head through L2), blocks take the pairs in
+  // decreasing kv_end (equal ones by sequence), so the lightest pairs fill each group's
+  // last blocks.  Up to 64 sequences the rank is found by a search over kv_end; beyond,
+  // the pairs run sequence by sequence, each sequence's last (longest) first.
   if (warp == 0) {
-    int base = 0, found = 0;
-    for (int s0 = 0; s0 < S && !found; s0 += 32) {
-      const int s = s0 + lane;
-      int nt = 0;
-      if (s < S) {
-        const int n = p.query_start_loc[s + 1] - p.query_start_loc[s];
-        nt = n > 0 ? (n + 2 * TQ - 1) / (2 * TQ) : 0;
-      }
-      int incl = nt;
+    if (S <= 64) {
+      constexpr int kPairShift = __builtin_ctz(2 * TQ);  // 2 TQ is a power of two
+      static_assert((2 * TQ) == (1 << kPairShift), "tile pair");
+      int Ls[2], Pb[2], nts[2];
+      int maxL = 0;
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += v;
+      for (int j = 0; j < 2; ++j) {
+        const int s = lane + 32 * j;
+        Ls[j] = Pb[j] = nts[j] = 0;
+        if (s < S) {
+          const int n = p.query_start_loc[s + 1] - p.query_start_loc[s];
+          if (n > 0) {
+            // (a sequence whose L is out of range ranks as if L = n; its block reports it)
+            const int L = p.context_lens[s];
+            Ls[j] = L >= n && L <= max(p.max_blocks_per_seq * p.block_size, n) ? L : n;
+            Pb[j] = Ls[j] - n;
+            nts[j] = (n + 2 * TQ - 1) >> kPairShift;
+            maxL = max(maxL, Ls[j]);
+          }
+        }
       }
-      const int lo = base + incl - nt;
-      const bool mine = nt > 0 && int(blockIdx.x) >= lo && int(blockIdx.x) < base + incl;
-      if (mine) {
-        item[0] = s;
-        item[1] = nt - 1 - (int(blockIdx.x) - lo);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) maxL = max(maxL, __shfl_xor_sync(0xffffffffu, maxL, off));
+      // pairs with kv_end > c >= 0: of sequence s, its last pair if L > c, and pair
+      // t < nt - 1 (kv_end Pb + (t + 1) 2TQ) when t + 1 >= m, the least such multiple
+      auto count_gt = [&](int c) -> int {
+        int cnt = 0;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          if (nts[j] > 0 && Ls[j] > c) {
+            const int d = c - Pb[j];
+            const int m = d < 0 ? 1 : (d >> kPairShift) + 1;
+            cnt += 1 + max(0, nts[j] - m);
+          }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+        return cnt;
+      };
+      int found_s = -1, found_t = 0;
+      if (rank < count_gt(0)) {  // (every kv_end is at least 1)
+        // the least c with count_gt(c) <= rank is the pair's kv_end
+        int lo = 0, hi = maxL;  // count_gt(lo) > rank >= count_gt(hi) = 0
+        while (hi - lo > 1) {
+          const int mid = lo + (hi - lo) / 2;
+          if (count_gt(mid) <= rank) hi = mid; else lo = mid;
+        }
+        const int k = rank - count_gt(hi);  // among the pairs with kv_end == hi, by sequence
+        int before = 0;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          bool has = false;
+          int t = 0;
+          if (nts[j] > 0) {
+            const int d = hi - Pb[j];
+            if (Ls[j] == hi) {
+              has = true;
+              t = nts[j] - 1;
+            } else if (d > 0 && (d & (2 * TQ - 1)) == 0 && (d >> kPairShift) <= nts[j] - 1) {
+              has = true;
+              t = (d >> kPairShift) - 1;
+            }
+          }
+          const uint32_t bal = __ballot_sync(0xffffffffu, has);
+          const int pos = before + __popc(bal & ((1u << lane) - 1u));
+          if (has && pos == k) {
+            found_s = lane + 32 * j;
+            found_t = t;
+          }
+          before += __popc(bal);
+        }
       }
-      found = __any_sync(0xffffffffu, mine);
-      base += __shfl_sync(0xffffffffu, incl, 31);
+      const uint32_t who = __ballot_sync(0xffffffffu, found_s >= 0);
+      if (lane == 0) item[0] = -1;
+      __syncwarp();
+      if (found_s >= 0 && lane == __ffs(who) - 1) {
+        item[0] = found_s;
+        item[1] = found_t;
+      }
+    } else {
+      int base = 0, found = 0;
+      for (int s0 = 0; s0 < S && !found; s0 += 32) {
+        const int s = s0 + lane;
+        int nt = 0;
+        if (s < S) {
+          const int n = p.query_start_loc[s + 1] - p.query_start_loc[s];
+          nt = n > 0 ? (n + 2 * TQ - 1) / (2 * TQ) : 0;
+        }
+        int incl = nt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += v;
+        }
+        const int lo = base + incl - nt;
+        const bool mine = nt > 0 && rank >= lo && rank < base + incl;
+        if (mine) {
+          item[0] = s;
+          item[1] = nt - 1 - (rank - lo);
+        }
+        found = __any_sync(0xffffffffu, mine);
+        base += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0 && !found) item[0] = -1;
     }
-    if (lane == 0 && !found) item[0] = -1;
   }
   __syncthreads();
   const int s = item[0];
@@ -161,7 +251,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_co
   const int q0 = p.query_start_loc[s];
   const int n = p.query_start_loc[s + 1] - q0;
   if (L < 0 || L > max_ctx || n > L) {
-    if (tid == 0 && blockIdx.y == 0 && t == (n + 2 * TQ - 1) / (2 * TQ) - 1) raise_device_error(p.err, kErrContextLen);
+    if (tid == 0 && hg == 0 && t == (n + 2 * TQ - 1) / (2 * TQ) - 1) raise_device_error(p.err, kErrContextLen);
     return;
   }
   const int tq0 = t * 2 * TQ;              // first new token of the block, within the chunk
@@ -496,10 +586,12 @@ cudaError_t launch_prefill_tc_tpl(const DecodeParams& p, cudaStream_t stream) {
       return e;
     if (dev >= 0 && dev < kMapCacheDevices) smem_set[dev] = smem;
   }
-  // one block per (pair of query tiles, group of GP heads); the pairs of all sequences
-  // number at most ceil(T / 2 TQ) + S, surplus blocks exit at once
+  // one block per (group of GP heads, pair of query tiles), the pair fastest; the pairs
+  // of all sequences number at most ceil(T / 2 TQ) + S, surplus blocks exit at once
   constexpr int TQ2 = 2 * (prefill_tc::kBM / GP);  // new tokens per block
-  const dim3 grid(unsigned((p.num_tokens + TQ2 - 1) / TQ2 + p.num_seqs), unsigned(p.num_heads / GP));
+  const int64_t blocks = (int64_t(p.num_tokens + TQ2 - 1) / TQ2 + p.num_seqs) * (p.num_heads / GP);
+  if (blocks > int64_t(INT32_MAX)) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(blocks));
   kern<<<grid, prefill_tc::kThreads, smem, stream>>>(mq, mk, mv, p);
   note_launch();
   return cudaGetLastError();

@@ -268,6 +268,17 @@ def test_prefill_empty_chunk_and_single_tokens(pkernel):
     check_workload(w)
 
 
+@pytest.mark.parametrize("num_seqs", [40, 70])
+def test_prefill_many_sequences(num_seqs, pkernel):
+    """Many sequences, prefix and chunk lengths repeating (so that tile pairs see equal
+    key counts): up to 64 sequences the tcgen05 kernel takes the pairs in decreasing
+    key count, equal counts by sequence, beyond 64 sequence by sequence; either way
+    every pair is computed once (unused slots NaN)."""
+    prefix = tuple((i % 5) * 60 for i in range(num_seqs))
+    chunks = tuple(1 + (i % 7) * 30 for i in range(num_seqs))
+    check_workload(wl.chunked_prefill(seed=97 + num_seqs, prefix_lens=prefix, chunk_lens=chunks, poison=True))
+
+
 def test_prefill_full(pkernel):
     """Llama-3-8B-shaped prefill: two 2048-token prompts and two 512-token chunks of
     long prompts (prefixes 512 and 1536)."""
