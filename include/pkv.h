@@ -140,8 +140,10 @@ typedef void* pkv_stream; /* a cudaStream_t */
  * on demand (growth synchronises the device; it is refused while the stream is being
  * captured — size it beforehand with pkv_reserve_workspace).  All decode calls on a
  * device share that workspace: calls ordered on one stream are safe, calls whose GPU
- * work may overlap (unordered streams) race on it.  Host threads may call at the same
- * time; the library serialises each device's workspace use from growth to launch.
+ * work may overlap (unordered streams) race on it (the overlapping calls' outputs are
+ * then unspecified; later ordered calls are not affected: the claim counter is zeroed
+ * after every launch's grid has completed).  Host threads may call at the same time;
+ * the library serialises each device's workspace use from growth to launch.
  */
 pkv_status pkv_paged_attention_decode(const pkv_tensor* out, const pkv_tensor* query,
                                       const pkv_tensor* key_cache, const pkv_tensor* value_cache,
