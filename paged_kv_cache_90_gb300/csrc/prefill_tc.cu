@@ -58,7 +58,11 @@ struct Cfg {
   static constexpr uint32_t kV = kK + 2 * kOpBytes;
   static constexpr uint32_t kBar = kV + 2 * kOpBytes;
   static constexpr uint32_t kTable = kBar + 256;
-  static size_t smem_bytes(int entries) { return kTable + size_t(entries) * 4 + 1024; }
+  // the table region first holds the ranking's per-sequence data (up to 64 sequences)
+  static constexpr size_t kRankScratch = (4 * 64 + 68) * 4;
+  static size_t smem_bytes(int entries) {
+    return kTable + (size_t(entries) * 4 > kRankScratch ? size_t(entries) * 4 : kRankScratch) + 1024;
+  }
   // tensor memory: S_A, S_B (128 columns each), then O_A, O_B (D columns each)
   static constexpr uint32_t kS = 0, kO = 2 * kBN;
 };
@@ -133,89 +137,62 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_co
   // plus the pair's end; the last pair ends at L).  Head group by head group (whose
   // blocks share the K/V tiles of their KV head through L2), blocks take the pairs in
   // decreasing kv_end (equal ones by sequence), so the lightest pairs fill each group's
-  // last blocks.  Up to 64 sequences the rank is found by a search over kv_end; beyond,
-  // the pairs run sequence by sequence, each sequence's last (longest) first.
-  if (warp == 0) {
-    if (S <= 64) {
-      constexpr int kPairShift = __builtin_ctz(2 * TQ);  // 2 TQ is a power of two
-      static_assert((2 * TQ) == (1 << kPairShift), "tile pair");
-      int Ls[2], Pb[2], nts[2];
-      int maxL = 0;
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int s = lane + 32 * j;
-        Ls[j] = Pb[j] = nts[j] = 0;
-        if (s < S) {
-          const int n = p.query_start_loc[s + 1] - p.query_start_loc[s];
-          if (n > 0) {
-            // (a sequence whose L is out of range ranks as if L = n; its block reports it)
-            const int L = p.context_lens[s];
-            Ls[j] = L >= n && L <= max(p.max_blocks_per_seq * p.block_size, n) ? L : n;
-            Pb[j] = Ls[j] - n;
-            nts[j] = (n + 2 * TQ - 1) >> kPairShift;
-            maxL = max(maxL, Ls[j]);
-          }
-        }
+  // last blocks.  Up to 64 sequences and 65536 (pair, sequence) products, every thread
+  // ranks some of the pairs (per sequence, the pairs ahead of a pair have a closed form)
+  // and the one holding the block's rank names its pair; beyond, the pairs run sequence
+  // by sequence, each sequence's last (longest) first.
+  constexpr int kPairShift = __builtin_ctz(2 * TQ);  // 2 TQ is a power of two
+  static_assert((2 * TQ) == (1 << kPairShift), "tile pair");
+  int* rk_L = reinterpret_cast<int*>(smem + C::kTable);  // [64] L (as ranked)
+  int* rk_P = rk_L + 64;                                  // [64] chunk start L - n
+  int* rk_n = rk_P + 64;                                  // [64] pairs
+  int* rk_f = rk_n + 64;                                  // [65] first pair index
+  int npairs = 0;
+  if (S <= 64) {
+    if (tid < S) {
+      const int n = p.query_start_loc[tid + 1] - p.query_start_loc[tid];
+      const int L = p.context_lens[tid];
+      // (a sequence whose L is out of range ranks as if L = n; its block reports it)
+      const int Lr = n > 0 && L >= n && L <= max(p.max_blocks_per_seq * p.block_size, n) ? L : max(n, 0);
+      rk_L[tid] = Lr;
+      rk_P[tid] = Lr - max(n, 0);
+      rk_n[tid] = n > 0 ? (n + 2 * TQ - 1) >> kPairShift : 0;
+    }
+    if (tid == 0) item[0] = -1;
+    __syncthreads();
+    if (tid == 0) {
+      int f = 0;
+      for (int q = 0; q < S; ++q) {
+        rk_f[q] = f;
+        f += rk_n[q];
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) maxL = max(maxL, __shfl_xor_sync(0xffffffffu, maxL, off));
-      // pairs with kv_end > c >= 0: of sequence s, its last pair if L > c, and pair
-      // t < nt - 1 (kv_end Pb + (t + 1) 2TQ) when t + 1 >= m, the least such multiple
-      auto count_gt = [&](int c) -> int {
-        int cnt = 0;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          if (nts[j] > 0 && Ls[j] > c) {
-            const int d = c - Pb[j];
-            const int m = d < 0 ? 1 : (d >> kPairShift) + 1;
-            cnt += 1 + max(0, nts[j] - m);
-          }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
-        return cnt;
-      };
-      int found_s = -1, found_t = 0;
-      if (rank < count_gt(0)) {  // (every kv_end is at least 1)
-        // the least c with count_gt(c) <= rank is the pair's kv_end
-        int lo = 0, hi = maxL;  // count_gt(lo) > rank >= count_gt(hi) = 0
-        while (hi - lo > 1) {
-          const int mid = lo + (hi - lo) / 2;
-          if (count_gt(mid) <= rank) hi = mid; else lo = mid;
-        }
-        const int k = rank - count_gt(hi);  // among the pairs with kv_end == hi, by sequence
-        int before = 0;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          bool has = false;
-          int t = 0;
-          if (nts[j] > 0) {
-            const int d = hi - Pb[j];
-            if (Ls[j] == hi) {
-              has = true;
-              t = nts[j] - 1;
-            } else if (d > 0 && (d & (2 * TQ - 1)) == 0 && (d >> kPairShift) <= nts[j] - 1) {
-              has = true;
-              t = (d >> kPairShift) - 1;
-            }
-          }
-          const uint32_t bal = __ballot_sync(0xffffffffu, has);
-          const int pos = before + __popc(bal & ((1u << lane) - 1u));
-          if (has && pos == k) {
-            found_s = lane + 32 * j;
-            found_t = t;
-          }
-          before += __popc(bal);
-        }
+      rk_f[S] = f;
+    }
+    __syncthreads();
+    npairs = rk_f[S];
+  }
+  if (S <= 64 && int64_t(npairs) * S <= 65536) {
+    for (int pi = tid; pi < npairs; pi += kThreads) {
+      int sq = 0;
+      while (rk_f[sq + 1] <= pi) ++sq;
+      const int tq = pi - rk_f[sq];
+      const int c = tq == rk_n[sq] - 1 ? rk_L[sq] : rk_P[sq] + ((tq + 1) << kPairShift);  // its kv_end
+      int r = 0;
+      for (int q = 0; q < S; ++q) {
+        const int nq = rk_n[q];
+        if (nq == 0) continue;
+        const int Lq = rk_L[q], d = c - rk_P[q];
+        // pairs of q with kv_end > c: the last one if L > c, pair t < nq - 1 when
+        // (t + 1) 2TQ > d; and with kv_end == c, ahead when q < sq
+        if (Lq > c) r += 1 + max(0, nq - (d < 0 ? 1 : (d >> kPairShift) + 1));
+        if (q < sq && (Lq == c || (d > 0 && (d & (2 * TQ - 1)) == 0 && (d >> kPairShift) <= nq - 1))) ++r;
       }
-      const uint32_t who = __ballot_sync(0xffffffffu, found_s >= 0);
-      if (lane == 0) item[0] = -1;
-      __syncwarp();
-      if (found_s >= 0 && lane == __ffs(who) - 1) {
-        item[0] = found_s;
-        item[1] = found_t;
+      if (r == rank) {
+        item[0] = sq;
+        item[1] = tq;
       }
-    } else {
+    }
+  } else if (warp == 0) {
       int base = 0, found = 0;
       for (int s0 = 0; s0 < S && !found; s0 += 32) {
         const int s = s0 + lane;
@@ -240,7 +217,6 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_co
         base += __shfl_sync(0xffffffffu, incl, 31);
       }
       if (lane == 0 && !found) item[0] = -1;
-    }
   }
   __syncthreads();
   const int s = item[0];
