@@ -188,6 +188,34 @@ def decode_step(out, query, key, value, slot_mapping, key_cache, value_cache, bl
     return out
 
 
+def prepare_decode_step(out, query, key, value, slot_mapping, key_cache, value_cache, block_tables,
+                        context_lens, num_kv_heads: int, scale: float, block_size: int, max_blocks_per_seq: int,
+                        k_scale: float = 1.0, v_scale: float = 1.0, stream=None, sliding_window: int = 0,
+                        k_head_scales=None, v_head_scales=None):
+    """decode_step's arguments marshalled once: the returned callable issues that same
+    call (same tensors, same stream, resolved now) each time it is called, with nothing
+    rebuilt, for serving loops that reuse their buffers every step.  The tensors must
+    stay alive, on the same storage, shapes and strides, while the callable is used (it
+    holds references to them).  Each call returns ``out``."""
+    lib = load_library()
+    keep = (out, query, key, value, slot_mapping, key_cache, value_cache, block_tables, context_lens,
+            k_head_scales, v_head_scales)
+    descs = [describe(out), describe(query), describe(key), describe(value), describe(slot_mapping),
+             describe(key_cache, k_scale, k_head_scales), describe(value_cache, v_scale, v_head_scales),
+             describe(block_tables), describe(context_lens)]
+    args = tuple(ctypes.byref(d) for d in descs) + (
+        ctypes.c_int32(int(num_kv_heads)), ctypes.c_float(float(scale)), ctypes.c_int32(int(block_size)),
+        ctypes.c_int32(int(max_blocks_per_seq)), ctypes.c_int32(int(sliding_window)), _stream(stream))
+    fn = lib.pkv_decode_step
+
+    def call() -> torch.Tensor:
+        _check(fn(*args))
+        return out
+
+    call.tensors, call.descriptors = keep, descs  # kept alive with the callable
+    return call
+
+
 def decode_append(out, query, key, value, slot_mapping, key_cache, value_cache, block_tables, context_lens,
                   num_kv_heads: int, scale: float, block_size: int, max_blocks_per_seq: int,
                   k_scale: float = 1.0, v_scale: float = 1.0, stream=None, sliding_window: int = 0,

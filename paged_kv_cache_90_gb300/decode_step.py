@@ -66,6 +66,19 @@ class DeviceWorkload:
         return out
 
 
+def prepare_step(w: Workload, key_cache, value_cache, st: DeviceStep, out, stream=None, joint=True,
+                 k_head_scales=None, v_head_scales=None):
+    """A callable that runs the step as run_decode_step does.  A joint decode step with no
+    copy-on-write pairs is marshalled once (binding.prepare_decode_step); other steps
+    call run_decode_step each time."""
+    if joint is True and st.query_start_loc is None and not st.cow_pairs.numel():
+        return binding.prepare_decode_step(out, st.query, st.new_key, st.new_value, st.slot_mapping, key_cache,
+                                           value_cache, st.block_tables, st.context_lens, w.num_kv_heads, w.scale,
+                                           w.block_size, w.max_blocks_per_seq, w.k_scale, w.v_scale, stream,
+                                           w.sliding_window, k_head_scales, v_head_scales)
+    return lambda: run_decode_step(w, key_cache, value_cache, st, out, stream, joint, k_head_scales, v_head_scales)
+
+
 def run_decode_step(w: Workload, key_cache, value_cache, st: DeviceStep, out, stream=None,
                     joint=True, k_head_scales=None, v_head_scales=None) -> None:
     if st.cow_pairs.numel():

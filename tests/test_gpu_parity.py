@@ -12,7 +12,7 @@ import oracle
 from paged_kv_cache_90_gb300 import binding
 from paged_kv_cache_90_gb300 import build as pkv_build
 from paged_kv_cache_90_gb300 import workloads as wl
-from paged_kv_cache_90_gb300.decode_step import DeviceWorkload
+from paged_kv_cache_90_gb300.decode_step import DeviceWorkload, prepare_step
 
 pytestmark = pytest.mark.gpu
 
@@ -637,6 +637,26 @@ def test_copy_blocks_overlap_check_under_debug_sync():
         binding.set_option("debug_sync", 0)
     binding.copy_blocks(d, torch.tensor([[1, 5], [2, 5]], dtype=torch.int64, device="cuda"))
     assert binding.read_device_errors() == 0              # not checked without debug sync
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_prepared_decode_step_matches_the_call(kv):
+    """The prepared form of pkv_decode_step (arguments marshalled once, reissued) gives
+    the same cache bytes and outputs as the ordinary call, step after step."""
+    w = wl.continuous_batching(seed=78, num_seqs=24, num_steps=3, median=300, cap=3000, kv_dtype=kv, poison=True)
+    a, b = DeviceWorkload(w), DeviceWorkload(w)
+    for k in range(len(w.steps)):
+        ra = a.run_step(k, out=torch.empty_like(a.out)).clone()
+        out_b = torch.empty_like(b.out)
+        call = prepare_step(w, b.key_cache, b.value_cache, b.steps[k], out_b, None, True,
+                            b.k_head_scales, b.v_head_scales)
+        rb = call().clone()
+        torch.cuda.synchronize()
+        assert torch.equal(ra, rb)
+        # (the caches' unused slots hold NaN: compare the bytes)
+        assert torch.equal(a.key_cache.view(torch.uint8), b.key_cache.view(torch.uint8))
+        assert torch.equal(a.value_cache.view(torch.uint8), b.value_cache.view(torch.uint8))
+    assert binding.read_device_errors() == 0
 
 
 def test_launch_count_and_determinism(kernel):
