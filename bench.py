@@ -50,7 +50,7 @@ from paged_kv_cache_90_gb300.decode_step import DeviceStep, DeviceWorkload, prep
 METRIC = "paged decode attention: effective KV-read GB/s (% of HBM peak), µs/step"
 UNIT = "GB/s"
 L2_FLUSH_BYTES = 256 << 20
-DECODE_SOURCES = ["decode_core.cuh", "decode_mma.cuh", "decode_mma.cu", "decode_mma_launch.cuh", "merge.cuh",
+DECODE_SOURCES = ["decode_core.cuh", "decode_mma.cuh", "decode_mma.cu", "decode_mma_small.cu", "decode_mma_launch.cuh", "merge.cuh",
                   "decode_dispatch.cu", "device_common.cuh", "pkv_internal.h"]
 PREFILL_SOURCES = ["prefill_tc.cu", "tcgen05.cuh", "prefill_mma.cuh", "decode_mma_launch.cuh", "device_common.cuh",
                    "pkv_internal.h"]
@@ -80,6 +80,10 @@ def make_workload(name: str, rank: int = 0) -> wl.Workload:
     if m:   # N fresh prompts of T tokens each
         n, t = int(m.group(1)), int(m.group(2))
         return wl.chunked_prefill(seed=8 + seed_off, prefix_lens=[0] * n, chunk_lens=[t] * n)
+    if name == "mha_decode":  # multi-head attention (one query head per KV head), Llama-3-8B-shaped batch
+        g = torch.Generator().manual_seed(9 + seed_off)
+        lens = (torch.randint(128, 2049, (64,), generator=g) + 1).tolist()
+        return wl.variable_length_decode("mha_decode", 9 + seed_off, lens, 32, 32, 128, 16, "bf16")
     if name == "tiny":
         return wl.tiny(seed=1 + seed_off)
     raise SystemExit(f"unknown workload {name}")
@@ -578,12 +582,12 @@ def run_gpu(args, world, rank, local):
 
     def time_back_to_back(fn, count):
         """Total time (ms) of `count` calls queued back to back between two events.  A
-        device-side spin queued before the first event (about 0.1 ms per call, at most
-        6.4 ms) holds the stream while the host queues the calls, so that the GPU does
+        device-side spin queued before the first event (about 0.25 ms per call, at most
+        16 ms) holds the stream while the host queues the calls, so that the GPU does
         not wait inside the timed region for the host's first launches (a benchmark
         harness's "blocking kernel"); the events bracket exactly the `count` calls."""
         a, _, c = ev[0]
-        torch.cuda._sleep(int(min(count, 64) * 2.0e5))
+        torch.cuda._sleep(int(min(count, 64) * 5.0e5))
         a.record(stream)
         for k in range(count):
             fn(k)
@@ -719,7 +723,7 @@ def main():
     ap.add_argument("--workload", default="llama3_8b_decode",
                     help="llama3_8b_decode, long_context[_bs32], shared_prefix_cow, "
                          "continuous_batching_bs{8,16,32}_{bf16,e4m3}[_headscales], sliding_window[_bs32], "
-                         "chunked_prefill, prefill_<N>x<T>, tiny")
+                         "mha_decode, chunked_prefill, prefill_<N>x<T>, tiny")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle CPU time")
     ap.add_argument("--decode-kernel", choices=["auto", "tensor", "core"], default="auto",

@@ -131,6 +131,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_split_rows_kernel(const D
 template <typename KV, int D>
 size_t smem_for(int G, int S, bool fused_append) {
   switch (G) {
+    case 1: return mma::Cfg<KV, D, 1>::smem_bytes(S, fused_append);
+    case 2: return mma::Cfg<KV, D, 2>::smem_bytes(S, fused_append);
     case 4: return mma::Cfg<KV, D, 4>::smem_bytes(S, fused_append);
     case 8: return mma::Cfg<KV, D, 8>::smem_bytes(S, fused_append);
     case 16: return mma::Cfg<KV, D, 16>::smem_bytes(S, fused_append);
@@ -220,11 +222,14 @@ cudaError_t launch_prefill(const DecodeParams& p, cudaStream_t stream) {
   return cudaErrorInvalidValue;
 }
 
+// Query heads of one KV head's group that a row of work takes (the MMA tile pads them
+// to its 16 rows, or 8 columns for an 8-bit cache): the largest of 16, 8, 4, 2, 1 that
+// divides the group.
 int mma_heads_per_item(int group) {
-  if (group % 16 == 0) return 16;
-  if (group % 8 == 0) return 8;
-  if (group % 4 == 0) return 4;
-  return 0;
+  if (group < 1) return 0;
+  for (int g : {16, 8, 4, 2})
+    if (group % g == 0) return g;
+  return 1;
 }
 
 static size_t mma_smem_bytes(const DecodeParams& p, int G, bool fused_append) {
@@ -234,7 +239,10 @@ static size_t mma_smem_bytes(const DecodeParams& p, int G, bool fused_append) {
   return 0;
 }
 
-bool mma_fused_append_fits(const DecodeParams& p) { return mma_seqs_per_launch(p, true) == p.num_seqs; }
+// (the fused-append instances exist for 4, 8 and 16 heads per row)
+bool mma_fused_append_fits(const DecodeParams& p) {
+  return mma_heads_per_item(p.group) >= 4 && mma_seqs_per_launch(p, true) == p.num_seqs;
+}
 
 // Whether a launch over `S` sequences fits: the main kernel's per-sequence offsets in
 // its shared memory, the merge kernel's offsets and scratch in the default 48 KB, the

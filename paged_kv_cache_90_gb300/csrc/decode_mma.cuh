@@ -139,7 +139,7 @@ struct Cfg {
   static constexpr int kHT = (G + 7) / 8;                  // 8-bit cache: head tiles (MMA N = 8 heads)
   static constexpr int kMT = D / 16;                       // 8-bit cache: head_dim tiles of the value MMA
   static_assert(kFp8 ? D == 128 : (D == 64 || D == 128), "head_dim");
-  static_assert(G == 4 || G == 8 || G == 16, "heads per item");
+  static_assert(G == 1 || G == 2 || G == 4 || G == 8 || G == 16, "heads per item");
   static_assert(kRawTile % 1024 == 0 || kRawRowBytes == 64, "tiles are whole swizzle atoms");
   static constexpr size_t kWarpBytes = size_t(kStages) * kStageBytes + kVConv;
   // fused append: a ring slot's copy of the appended token's K and V rows (as given:

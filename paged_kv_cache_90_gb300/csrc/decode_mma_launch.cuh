@@ -18,6 +18,8 @@ cudaError_t cached_cache_map(CUtensorMap* out, const void* base, const DecodePar
 
 // the fused-append instantiations (decode_mma_append.cu)
 cudaError_t launch_decode_mma_main_append(const DecodeParams& p, cudaStream_t stream);
+// the plain instantiations for 1 or 2 query heads per row (decode_mma_small.cu)
+cudaError_t launch_decode_mma_main_small(const DecodeParams& p, cudaStream_t stream);
 
 template <typename KV, int D, int G, bool kAppend>
 cudaError_t launch_tpl(const DecodeParams& p, cudaStream_t stream) {
@@ -59,6 +61,7 @@ cudaError_t launch_tpl(const DecodeParams& p, cudaStream_t stream) {
 template <bool kAppend>
 cudaError_t launch_main(const DecodeParams& p, cudaStream_t stream) {
   const int G = p.heads_per_item;
+  if (G < 4) return kAppend ? cudaErrorInvalidValue : launch_decode_mma_main_small(p, stream);
 #define PKV_MMA_CASE(KVT, DD, GG) \
   if (G == GG) return launch_tpl<KVT, DD, GG, kAppend>(p, stream);
   if (p.kv_dtype == kBF16 && p.head_dim == 128) {

@@ -332,7 +332,7 @@ pkv_status decode_prepare(const pkv_tensor* out, const pkv_tensor* query, const 
   if (want == 2 && !mma_ok)
     return fail(PKV_ERR_UNSUPPORTED, "the tensor-core decode kernel does not support this call "
                 "(needs bf16 queries, a bf16 cache with head_dim 64/128 or an e4m3 cache with head_dim 128, "
-                "query heads per KV head a multiple of 4, block size 8/16/32)");
+                "block size 8/16/32)");
   p.partial_rows = parts > 1 ? int64_t(S) * Hq * parts : 0;
   if (mma_ok) {
     // one partial per (row, unit of work) pair a row spans: fewer than units + rows of

@@ -100,7 +100,7 @@ struct DecodeParams {
   unsigned int* err;
   // tensor-core kernel only
   int kernel;                // 0: CUDA-core kernel, 1: tensor-core kernel
-  int heads_per_item;        // query heads per row of work (4, 8 or 16)
+  int heads_per_item;        // query heads per row of work (1, 2, 4, 8 or 16)
   int block_warps;           // warps per thread block (mma_block_warps)
   int grid;                  // persistent thread blocks
   int dyn_share;             // stages handed out at run time, in 1/1024 of all stages

@@ -659,6 +659,22 @@ def test_prepared_decode_step_matches_the_call(kv):
     assert binding.read_device_errors() == 0
 
 
+@pytest.mark.parametrize("hq,hk,d,kv", [(32, 32, 128, "bf16"), (12, 4, 128, "bf16"), (24, 4, 64, "bf16"),
+                                        (16, 16, 128, "e4m3"), (12, 2, 128, "e4m3")])
+def test_tensor_kernel_groups_not_a_multiple_of_four(hq, hk, d, kv):
+    """Query-head groups of 1, 3 and 6 (rows of 1 or 2 heads, the MMA tile padded) run
+    on the tensor-core kernel (forced, and chosen automatically) and match the oracle."""
+    w = wl.variable_length_decode(f"g{hq // hk}_{kv}_{d}", 100 + hq + hk, [1, 17, 300, 1200, 2500], hq, hk, d, 16,
+                                  kv, poison=True)
+    binding.set_option("decode_kernel", 2)
+    try:
+        forced = check_workload(w)[0]
+    finally:
+        binding.set_option("decode_kernel", 0)
+    for x, y in zip(forced, run_device(w)[0]):
+        assert torch.equal(x, y)
+
+
 def test_launch_count_and_determinism(kernel):
     w = wl.llama3_8b_decode(seed=99, num_seqs=4, len_range=(600, 1500))
     dw = DeviceWorkload(w)
@@ -802,7 +818,7 @@ def test_auto_selects_tensor_core_kernel_for_gqa_bf16():
 
 
 def test_tensor_core_kernel_rejects_what_it_cannot_run():
-    w = wl.variable_length_decode("nt", 97, [10, 20], 6, 2, 128, 16, "bf16")   # 3 heads per KV head
+    w = wl.variable_length_decode("nt", 97, [10, 20], 8, 2, 128, 4, "bf16")   # block size 4
     dw = DeviceWorkload(w)
     binding.set_option("decode_kernel", 2)
     try:
