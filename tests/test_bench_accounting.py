@@ -46,6 +46,16 @@ def test_decode_bytes_count_every_attended_token():
     assert b.decode_bytes(w, w.steps[0]) == _brute_decode_bytes(w, w.steps[0])
 
 
+def test_mha_workload_counts_every_kv_head():
+    """The multi-head workload (one query head per KV head) counts K and V of all 32 KV
+    heads for every attended token."""
+    b = _bench()
+    w = b.make_workload("mha_decode")
+    assert (w.num_heads, w.num_kv_heads, w.num_seqs) == (32, 32, 64)
+    st = w.steps[0]
+    assert b.decode_bytes(w, st) == _brute_decode_bytes(w, st)
+
+
 def test_step_bytes_add_the_write_and_the_copies():
     b = _bench()
     w = wl.shared_prefix_cow(num_groups=2, group_size=4, prefix_blocks=2, suffix_range=(16, 60))
