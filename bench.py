@@ -631,11 +631,21 @@ def run_gpu(args, world, rank, local):
 
     # ---- end to end through the public API from pinned host buffers (e2e) ----
     fields = ("query", "new_key", "new_value", "slot_mapping", "block_tables", "context_lens", "cow_pairs")
-    staged = [staged_inputs(st, fields, dev) for st in w.steps]
+    e2e_steps = max(10, min(args.steps, 200))
+    if back_to_back:
+        # Pipelined like a serving loop: each step's inputs go in, and its output comes
+        # back, on a copy stream while the neighbouring steps compute.  An even number
+        # (at least two) of device input buffers and two output buffers, so that no copy
+        # overwrites what a step still reads or writes.
+        nbuf = nsteps if nsteps % 2 == 0 else 2 * nsteps
+        staged = [staged_inputs(w.steps[j % nsteps], fields, dev) for j in range(nbuf)]
+        outs = [dw.out, torch.empty_like(dw.out)]
+    else:
+        staged = [staged_inputs(st, fields, dev) for st in w.steps]
+        outs = [dw.out]
     out_host = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
     h2d = staged[0][3]
     d2h = out_host.numel() * out_host.element_size()
-    e2e_steps = max(10, min(args.steps, 200))
     for k in range(3):
         i = k % nsteps
         staged[i][1].copy_(staged[i][0], non_blocking=True)
@@ -644,19 +654,55 @@ def run_gpu(args, world, rank, local):
         out_host.copy_(dw.out, non_blocking=True)
     torch.cuda.synchronize(dev)
     # each staged step's call marshalled once (the library's prepared form of the call)
-    e2e_steps_fn = [prepare_step(w, dw.key_cache, dw.value_cache, staged[i][2], dw.out, None, joint,
-                                 dw.k_head_scales, dw.v_head_scales) for i in range(nsteps)]
+    e2e_steps_fn = [prepare_step(w, dw.key_cache, dw.value_cache, staged[j][2], outs[j % len(outs)], None, joint,
+                                 dw.k_head_scales, dw.v_head_scales) for j in range(len(staged))]
 
-    def e2e_call(k):
-        i = k % nsteps
-        staged[i][1].copy_(staged[i][0], non_blocking=True)   # every input of the step, one copy
-        e2e_steps_fn[i]()
-        out_host.copy_(dw.out, non_blocking=True)             # and its result back
     if back_to_back:
-        # timed like the device steps: back to back on the stream, each step's two
-        # copies in line with its kernels (no copy overlaps a kernel)
-        e_ms = time_back_to_back(e2e_call, e2e_steps)
+        xs = torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(e2e_steps)]
+        ev_done = [torch.cuda.Event() for _ in range(e2e_steps)]
+        ev_last = torch.cuda.Event()
+
+        def h2d_copy(k):
+            with torch.cuda.stream(xs):
+                staged[k % nbuf][1].copy_(staged[k % nbuf][0], non_blocking=True)
+                ev_in[k].record(xs)
+
+        def pipelined(count, start=None):
+            """Step k's input copy runs while step k-1 computes; its output copy while
+            step k+1 computes.  On the copy stream the input copy of step k+1 follows
+            the output copy of step k-1, which follows step k-1's kernels: the input
+            buffer it overwrites and the output buffer step k+1 writes are free."""
+            if start is not None:
+                xs.wait_event(start)
+            h2d_copy(0)
+            for k in range(count):
+                if k + 1 < count:
+                    h2d_copy(k + 1)
+                stream.wait_event(ev_in[k])
+                e2e_steps_fn[k % nbuf]()
+                ev_done[k].record(stream)
+                xs.wait_event(ev_done[k])
+                with torch.cuda.stream(xs):
+                    out_host.copy_(outs[k % 2], non_blocking=True)
+            ev_last.record(xs)
+            stream.wait_event(ev_last)
+
+        pipelined(min(3, e2e_steps))
+        torch.cuda.synchronize(dev)
+        a, _, c = ev[0]
+        torch.cuda._sleep(int(min(e2e_steps, 64) * 5.0e5))   # as in time_back_to_back
+        a.record(stream)
+        pipelined(e2e_steps, start=a)
+        c.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = a.elapsed_time(c)
     else:
+        def e2e_call(k):
+            i = k % nsteps
+            staged[i][1].copy_(staged[i][0], non_blocking=True)   # every input of the step, one copy
+            e2e_steps_fn[i]()
+            out_host.copy_(dw.out, non_blocking=True)             # and its result back
         e_ms = 0.0
         for k in range(e2e_steps):
             flush_l2()
