@@ -22,7 +22,10 @@ write's dirty lines are written back before the step starts); the flushed per-st
 figures of the large workloads are reported beside the back-to-back ones.  A step issues
 the cache write and the decode as one pkv_decode_step call.  The roofline entry times
 the decode kernels alone (main kernel + merge of split rows) in a second loop of decode
-calls on the same resident caches, timed the same way.
+calls on the same resident caches, timed the same way.  The end-to-end entry times the
+step from pinned host memory: each step's inputs go in as one copy and its output comes
+back inside the timed region; back-to-back workloads pipeline those copies on a second
+stream beside the neighbouring steps' kernels, as a serving loop would.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 """
@@ -327,6 +330,26 @@ def staged_inputs(st, fields, dev):
         views.setdefault(f, None)
     return host, devb, DeviceStep(**views), sum(getattr(st, f).numel() * getattr(st, f).element_size()
                                                 for f in fields)
+
+
+def e2e_pipeline_ops(count: int) -> list:
+    """The order in which the pipelined end-to-end loop issues its work, as (stream, op,
+    step) with stream "copy" or "compute".  Ops: "h2d" (step k's inputs into device input
+    buffer k mod nbuf), "record_in"/"wait_in" (the event after that copy, waited on by the
+    compute stream), "call" (the step's library call, writing output buffer k mod 2),
+    "record_done"/"wait_done" (the event after the call, waited on by the copy stream),
+    "d2h" (the step's output back to the host).  Step k+1's input copy is issued before
+    step k's call, and step k's output copy after it, so that each copy runs beside the
+    neighbouring steps' kernels; the copy stream's order (input copy of k+1 behind the
+    output copy of k-1, which waits for step k-1's call) keeps every buffer free when it
+    is reused, for any even number of input buffers."""
+    ops = [("copy", "h2d", 0), ("copy", "record_in", 0)]
+    for k in range(count):
+        if k + 1 < count:
+            ops += [("copy", "h2d", k + 1), ("copy", "record_in", k + 1)]
+        ops += [("compute", "wait_in", k), ("compute", "call", k), ("compute", "record_done", k),
+                ("copy", "wait_done", k), ("copy", "d2h", k)]
+    return ops
 
 
 def run_prefill_gpu(args, world, rank, local, w, dw, dev, flush_l2, barrier):
@@ -663,28 +686,27 @@ def run_gpu(args, world, rank, local):
         ev_done = [torch.cuda.Event() for _ in range(e2e_steps)]
         ev_last = torch.cuda.Event()
 
-        def h2d_copy(k):
-            with torch.cuda.stream(xs):
-                staged[k % nbuf][1].copy_(staged[k % nbuf][0], non_blocking=True)
-                ev_in[k].record(xs)
-
         def pipelined(count, start=None):
-            """Step k's input copy runs while step k-1 computes; its output copy while
-            step k+1 computes.  On the copy stream the input copy of step k+1 follows
-            the output copy of step k-1, which follows step k-1's kernels: the input
-            buffer it overwrites and the output buffer step k+1 writes are free."""
+            """Issue e2e_pipeline_ops(count) on the compute and copy streams."""
             if start is not None:
                 xs.wait_event(start)
-            h2d_copy(0)
-            for k in range(count):
-                if k + 1 < count:
-                    h2d_copy(k + 1)
-                stream.wait_event(ev_in[k])
-                e2e_steps_fn[k % nbuf]()
-                ev_done[k].record(stream)
-                xs.wait_event(ev_done[k])
-                with torch.cuda.stream(xs):
-                    out_host.copy_(outs[k % 2], non_blocking=True)
+            for _, op, k in e2e_pipeline_ops(count):
+                if op == "h2d":
+                    with torch.cuda.stream(xs):
+                        staged[k % nbuf][1].copy_(staged[k % nbuf][0], non_blocking=True)
+                elif op == "record_in":
+                    ev_in[k].record(xs)
+                elif op == "wait_in":
+                    stream.wait_event(ev_in[k])
+                elif op == "call":
+                    e2e_steps_fn[k % nbuf]()
+                elif op == "record_done":
+                    ev_done[k].record(stream)
+                elif op == "wait_done":
+                    xs.wait_event(ev_done[k])
+                else:   # d2h
+                    with torch.cuda.stream(xs):
+                        out_host.copy_(outs[k % 2], non_blocking=True)
             ev_last.record(xs)
             stream.wait_event(ev_last)
 

@@ -1,7 +1,7 @@
 """The measurement's own arithmetic (CPU): the algorithmic bytes a decode step must move
 and the FLOPs of a prefill step (the numerators of bench.py's throughputs and roofline),
-counted here token by token, and the packing of a step's inputs for the end-to-end
-timing."""
+counted here token by token; the packing of a step's inputs for the end-to-end timing;
+and the pipelined end-to-end loop's order, checked for races."""
 import importlib.util
 import os
 
@@ -109,3 +109,79 @@ def test_profile_digest_covers_existing_sources():
     for name in b.DECODE_SOURCES:
         assert os.path.exists(os.path.join(csrc, name)), name
     assert len(b.source_digest()) == 16
+
+
+def _happens_before(ops):
+    """For each op of a two-stream schedule, the set of ops certain to finish before it
+    starts: a stream runs its ops in issue order, and a wait on an event follows the
+    last op its stream issued before the event was recorded (a wait must come after its
+    record in issue order, as for CUDA events)."""
+    before, last, rec = [], {}, {}
+    for i, (where, op, k) in enumerate(ops):
+        preds = set()
+        if where in last:
+            preds.add(last[where])
+        last[where] = i
+        if op.startswith("record_"):
+            rec[(op[len("record_"):], k)] = i
+        if op.startswith("wait_"):
+            preds.add(rec[(op[len("wait_"):], k)])
+        s = set()
+        for p in preds:
+            s |= before[p]
+            s.add(p)
+        before.append(s)
+    return before
+
+
+def _pipeline_hazards(ops, nbuf):
+    """Races of the pipelined end-to-end loop: a step's call not behind its input copy,
+    an input copy overwriting a buffer an earlier call may still read, a call writing an
+    output buffer whose earlier output copy may still run, an output copy not behind its
+    call."""
+    before = _happens_before(ops)
+    at = {(op, k): i for i, (_, op, k) in enumerate(ops)}
+    steps = sorted({k for _, op, k in ops if op == "call"})
+    bad = []
+    for k in steps:
+        if at[("h2d", k)] not in before[at[("call", k)]]:
+            bad.append(("call before its input", k))
+        if at[("call", k)] not in before[at[("d2h", k)]]:
+            bad.append(("output copied before its call", k))
+        for m in steps:
+            if m < k and m % nbuf == k % nbuf and at[("call", m)] not in before[at[("h2d", k)]]:
+                bad.append(("input buffer overwritten while read", m, k))
+            if m < k and m % 2 == k % 2 and at[("d2h", m)] not in before[at[("call", k)]]:
+                bad.append(("output buffer written while copied", m, k))
+    return bad
+
+
+def test_e2e_pipeline_has_no_buffer_races():
+    """The pipelined end-to-end schedule, checked for every race between its copies and
+    its calls, with two or more (even) input buffers and two output buffers."""
+    b = _bench()
+    for count in (1, 2, 3, 4, 10, 25):
+        ops = b.e2e_pipeline_ops(count)
+        assert sorted(k for _, op, k in ops if op == "call") == list(range(count))
+        assert sum(op == "h2d" for _, op, _ in ops) == count and sum(op == "d2h" for _, op, _ in ops) == count
+        for nbuf in (2, 4, 10, 20):
+            assert _pipeline_hazards(ops, nbuf) == [], (count, nbuf)
+
+
+def test_e2e_race_check_catches_broken_schedules():
+    """The race check itself: one input buffer, output copies issued without waiting for
+    their calls, and input copies issued two steps ahead are each caught."""
+    b = _bench()
+    ops = b.e2e_pipeline_ops(6)
+    assert ("input buffer overwritten while read", 0, 1) in _pipeline_hazards(ops, 1)
+    no_wait = [x for x in ops if x[1] != "wait_done"]
+    assert ("output copied before its call", 0) in _pipeline_hazards(no_wait, 2)
+    ahead = [("copy", "h2d", 0), ("copy", "record_in", 0), ("copy", "h2d", 1), ("copy", "record_in", 1)]
+    for k in range(6):
+        if k + 2 < 6:
+            ahead += [("copy", "h2d", k + 2), ("copy", "record_in", k + 2)]
+        ahead += [("compute", "wait_in", k), ("compute", "call", k), ("compute", "record_done", k),
+                  ("copy", "wait_done", k), ("copy", "d2h", k)]
+    hazards = _pipeline_hazards(ahead, 2)
+    assert ("input buffer overwritten while read", 0, 2) in hazards
+    assert ("output buffer written while copied", 0, 2) in hazards
