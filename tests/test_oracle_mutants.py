@@ -56,6 +56,21 @@ MUTANTS = [
     ("prefill: keys scaled by the value scale", "orc_load(key_cache, base + d, kv_dtype) * k_scale;",
      "orc_load(key_cache, base + d, kv_dtype) * v_scale;", 0),
     # more decode, format and write mistakes
+    ("prefill: query heads interleaved over KV heads",
+     "for (int64_t h = k * group; h < (k + 1) * group; ++h) {",
+     "for (int64_t h = k; h < num_heads; h += num_kv_heads) {", 1),
+    ("prefill: max shift of the wrong sign", "z[j] = exp(z[j] - zmax);", "z[j] = exp(z[j] + zmax);", 1),
+    ("prefill: softmax not normalised", "for (int64_t j = 0; j <= pos; ++j) z[j] /= den;", ";", 0),
+    ("prefill: values read from the key cache",
+     "V[j * head_dim + d] = orc_load(value_cache, base + d, kv_dtype) * v_scale;",
+     "V[j * head_dim + d] = orc_load(key_cache, base + d, kv_dtype) * v_scale;", 0),
+    ("prefill: offset inside the block off by one", "(j % block_size) * cs_token",
+     "((j + 1) % block_size) * cs_token", 1),
+    ("prefill: block-table row stride dropped", "block_tables[s * max_blocks_per_seq + j / block_size]",
+     "block_tables[s + j / block_size]", 1),
+    ("prefill: own position left out of the weighted sum",
+     "for (int64_t j = 0; j <= pos; ++j)\n          for (int64_t d = 0; d < head_dim; ++d) o[d] += z[j]",
+     "for (int64_t j = 0; j < pos; ++j)\n          for (int64_t d = 0; d < head_dim; ++d) o[d] += z[j]", 0),
     ("decode: keys scaled by the value scale", "orc_load(key_cache, base + d, kv_dtype) * ks;",
      "orc_load(key_cache, base + d, kv_dtype) * vs;", 0),
     ("decode: every KV head takes head 0's scale", "k_head_scales ? (double)k_head_scales[k]",
