@@ -170,8 +170,10 @@ pkv_status pkv_paged_attention_decode(const pkv_tensor* out, const pkv_tensor* q
  * not its sequence's position L - 1 is stored only (as the two-call form would, provided
  * no sequence reads another sequence's new slot in the same step — which a correct block
  * manager never lets happen).  Where the library would run the CUDA-core decode kernel,
- * the call runs the write and the decode as two kernels instead.  Arguments and errors as
- * for pkv_decode_step; num_tokens != num_seqs is PKV_ERR_INVALID_ARG.
+ * where the tensor-core kernel's rows hold fewer than 4 query heads (query-head groups
+ * not a multiple of 4), and where one launch cannot hold the whole batch, the call runs
+ * the write and the decode as two kernels instead.  Arguments and errors as for
+ * pkv_decode_step; num_tokens != num_seqs is PKV_ERR_INVALID_ARG.
  */
 pkv_status pkv_decode_append(const pkv_tensor* out, const pkv_tensor* query, const pkv_tensor* key,
                              const pkv_tensor* value, const pkv_tensor* slot_mapping,

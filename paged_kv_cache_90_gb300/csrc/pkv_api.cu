@@ -773,8 +773,9 @@ pkv_status pkv_decode_append(const pkv_tensor* out, const pkv_tensor* query, con
   // decode_step).  Measured on GB300 that is faster than the write inside the decode
   // kernel for both cache types: the small write kernel runs while the decode kernel
   // prepares, whereas the in-kernel append sits on the critical path of the warps
-  // that hold sequence ends.  The CUDA-core kernel has no fused write, and very many
-  // sequences leave no room for the staged tokens.
+  // that hold sequence ends.  The CUDA-core kernel and the tensor-core rows of 1 or 2
+  // heads have no fused write, and very many sequences leave no room for the staged
+  // tokens.
   const bool fused = g_opt_fused_append.load() == 2;
   if (no_decode || p.kernel != 1 || !fused || !mma_fused_append_fits(p)) {
     if (!no_write) {
