@@ -83,6 +83,30 @@ def test_decode_step_validation(dry):
                                                  slot_mapping=torch.arange(2, dtype=torch.int64))) == 1
 
 
+def test_prepared_step_checks_like_the_call(dry):
+    """A prepared step call (arguments marshalled once) checks them at every call and
+    gives the status pkv_decode_step gives for the same arguments; it returns `out` and
+    keeps its tensors referenced."""
+    def args(**over):
+        a = _decode_args()
+        a.update(key=torch.zeros(3, 2, 128, dtype=torch.bfloat16), value=torch.zeros(3, 2, 128, dtype=torch.bfloat16),
+                 slot_mapping=torch.arange(3, dtype=torch.int64))
+        a.update(over)
+        return a
+    for over in ({}, {"slot_mapping": torch.arange(3, dtype=torch.int32)}, {"num_kv_heads": 3},
+                 {"block_size": 8}, {"query": torch.zeros(3, 8, 64, dtype=torch.bfloat16)}):
+        a = args(**over)
+        want = _status(binding.decode_step, **a)
+        step = binding.prepare_decode_step(**a)
+        for _ in range(2):
+            assert _status(step) == want, over
+        if want == 0:
+            assert step() is a["out"]
+    a = args()
+    step = binding.prepare_decode_step(**a)
+    assert step.tensors[0] is a["out"] and step.tensors[5] is a["key_cache"] and step.tensors[8] is a["context_lens"]
+
+
 def test_head_scales_and_amax_validation(dry):
     """Per-head scales belong to 8-bit caches only and must be 4-byte aligned; the
     per-tensor scale is not checked when they are given; amax arrays must be aligned."""
